@@ -1,0 +1,147 @@
+/*
+ * kda.h -- C ABI of libkda, Kimi Delta Attention (KDA) on NVIDIA GB300 (sm_103a).
+ *
+ * KDA is the per-channel gated delta rule.  For one head with key width dk and
+ * value width dv, state S (dk x dv, fp32) and tokens t = 1, 2, ...:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t
+ *
+ * The pages define the step in words: "Kimi K3 Architecture Teardown",
+ * section "Hybrid Attention for 1M Tokens", Visual 5 -- decay every key
+ * channel of the state, erase a beta-scaled share of what it holds under the
+ * current key, write the new key-value pair scaled by the same beta;
+ * "Kimi K3 Architecture: KDA, MoE, and Attention", section "Memory as a
+ * First-Class Problem" -- alpha is a per-channel decay, one beta erases and
+ * writes, and the output queries the UPDATED state.  A checkpointed state can
+ * resume prefill (prefix-cache hit): "Kimi K3 Architecture Teardown", section
+ * "Scale: Total vs Active Parameters and Serving Economics", and "Kimi K3
+ * architecture: KDA, MLA and MoE", section "Serving K3 means managing two
+ * cache lifecycles".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers to row-major, contiguous memory
+ *   owned by the caller.  The library allocates no memory and keeps no state
+ *   between calls, except one device status word used to report a timed-out
+ *   wait inside a kernel (see kda_device_status).
+ * - Layouts (T = shape->total_tokens, N = shape->num_seqs):
+ *     q, k       [T, H, dk]   dtype
+ *     v, out     [T, H, dv]   dtype
+ *     log_alpha  [T, H, dk]   fp32, log of the decay alpha in (0, 1], so <= 0;
+ *                             -inf (alpha = 0) is allowed
+ *     beta       [T, H]       dtype, the write strength (no clamp is applied)
+ *     states     [N, H, dk, dv] fp32
+ *   A dense batch [B, T', H, d] is the same memory with N = B, T = B*T' and
+ *   cu_seqlens = NULL.
+ * - q and k are expected to be L2-normalised by the caller; the library does
+ *   not normalise them.  There is no query scale: o_t = S_t^T q_t exactly.
+ * - Supported: dtype KDA_BF16 or KDA_F32; dk, dv in {64, 128}.
+ * - Pointers q, k, v, out, log_alpha and the state pointers must be 16-byte
+ *   aligned (else KDA_ERR_UNSUPPORTED); beta must be aligned to its element.
+ * - Every call is asynchronous on `stream`: it validates its arguments on the
+ *   host, enqueues kernels and returns.  On any error nothing is enqueued.
+ * - Arithmetic: fp32 accumulation and an fp32 state throughout.  With bf16
+ *   inputs and dk = dv = 128 prefill runs the chunkwise tensor-core kernel
+ *   (bf16 operands, fp32 accumulators); other shapes run an fp32 recurrent
+ *   kernel.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad cu_seqlens  */
+    KDA_ERR_UNSUPPORTED = 2,  /* dtype / head size / alignment not supported  */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed          */
+    KDA_ERR_TIMEOUT = 4       /* a bounded in-kernel wait gave up (see below)  */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+typedef struct {
+    int32_t num_seqs;       /* N: sequences (prefill) or rows (decode), >= 0  */
+    int64_t total_tokens;   /* T: packed token count, >= 0                     */
+    int32_t H;              /* heads, >= 1                                    */
+    int32_t dk;             /* key / query width per head                     */
+    int32_t dv;             /* value width per head                           */
+    kda_dtype dtype;        /* dtype of q, k, v, beta and out                 */
+} kda_shape;
+
+/*
+ * kda_prefill -- run the recurrence over N packed sequences.
+ *
+ * cu_seqlens: DEVICE int32 [N+1], cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[N] = T; tokens cu_seqlens[n] .. cu_seqlens[n+1]-1 form
+ *   sequence n.  NULL means N equal sequences of T/N tokens (T % N must be
+ *   0).  The device copy cannot be checked on the host without a sync; the
+ *   kernels clamp every offset into [0, T] and treat a reversed range as an
+ *   empty sequence, so a bad table never causes an out-of-bounds access.
+ *   kda_check_cu_seqlens validates a host copy.
+ * initial_state: [N, H, dk, dv] fp32 state each sequence starts from, or NULL
+ *   for zeros (a prefix-cache hit passes the checkpointed state here).
+ * final_state: [N, H, dk, dv] fp32 state after each sequence's last token,
+ *   or NULL (not written).  It may alias initial_state.
+ * out: [T, H, dv] in dtype, o_t for every token.
+ * Errors: KDA_ERR_INVALID_ARG for a NULL shape, q, k, v, log_alpha, beta or
+ *   out (when T > 0), negative sizes, N = 0 with T > 0, or T % N != 0 without
+ *   cu_seqlens; KDA_ERR_UNSUPPORTED for an unsupported dtype, head size or
+ *   alignment; KDA_ERR_CUDA if a launch fails.
+ */
+kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k,
+                       const void* v, const float* log_alpha, const void* beta,
+                       const float* initial_state, const int32_t* cu_seqlens,
+                       void* out, float* final_state, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one token for each of N independent sequences.
+ *
+ * shape->total_tokens must equal shape->num_seqs.  q, k, log_alpha are
+ * [N, H, dk], v and out [N, H, dv], beta [N, H]; state_inout [N, H, dk, dv]
+ * fp32 is read once and overwritten in place with S_t.  out receives
+ * o_t = S_t^T q_t.  Same error rules as kda_prefill; state_inout must not be
+ * NULL.
+ */
+kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
+                           const void* v, const float* log_alpha,
+                           const void* beta, float* state_inout, void* out,
+                           kda_stream_t stream);
+
+/*
+ * kda_check_cu_seqlens -- validate a HOST copy of a cu_seqlens table:
+ * cu[0] == 0, non-decreasing, cu[num_seqs] == total_tokens.  Returns KDA_OK
+ * or KDA_ERR_INVALID_ARG.  No CUDA call.
+ */
+kda_status kda_check_cu_seqlens(const int32_t* host_cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens);
+
+/*
+ * kda_device_status -- synchronise `stream`, then read and clear the device
+ * status word.  Returns KDA_ERR_TIMEOUT if a kernel's bounded wait gave up
+ * since the last call (that kernel's outputs are then undefined), KDA_OK
+ * otherwise, or KDA_ERR_CUDA if the synchronisation fails.  Setting the
+ * environment variable KDA_DEBUG_SYNC=1 makes kda_prefill and kda_decode_step
+ * call this themselves before returning.
+ */
+kda_status kda_device_status(kda_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kda_status_string(kda_status status);
+
+/* Library version string, e.g. "kda-gb300 0.1.0 sm_103a". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

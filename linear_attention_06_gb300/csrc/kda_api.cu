@@ -1,0 +1,168 @@
+// kda_api.cu -- the extern "C" boundary of libkda (declared in include/kda.h).
+//
+// Validates every argument on the host before any CUDA call, picks the kernel
+// (chunkwise tensor-core prefill for bf16 with dk = dv = 128, the fp32
+// recurrent kernel otherwise) and enqueues it on the caller's stream.  Nothing
+// is allocated; the only library state is one device status word that the
+// tensor-core kernel sets if one of its bounded waits gives up.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+// Device status word; bit kda::kStatusTimeout is set by a kernel whose bounded
+// wait ran out.  Read and cleared by kda_device_status.
+__device__ unsigned int g_kda_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Address of the status word on the current device (looked up once per
+// device with that device current; cudaGetSymbolAddress does not allocate).
+unsigned int* status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool env_flag(const char* name) {
+    const char* v = getenv(name);
+    return v && v[0] && strcmp(v, "0") != 0;
+}
+
+// Common shape checks.  Returns KDA_OK or the error to report.
+kda_status check_shape(const kda_shape* s) {
+    if (!s) return KDA_ERR_INVALID_ARG;
+    if (s->num_seqs < 0 || s->total_tokens < 0 || s->H <= 0 || s->dk <= 0 || s->dv <= 0)
+        return KDA_ERR_INVALID_ARG;
+    if (s->dtype != KDA_BF16 && s->dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if ((s->dk != 64 && s->dk != 128) || (s->dv != 64 && s->dv != 128)) return KDA_ERR_UNSUPPORTED;
+    if (s->H > 65535) return KDA_ERR_UNSUPPORTED;   // grid.y
+    if ((int64_t)s->num_seqs * s->H > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status check_tensor_ptrs(const kda_shape* s, const void* q, const void* k, const void* v,
+                             const float* log_alpha, const void* beta, const void* out) {
+    if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
+    const size_t esz = s->dtype == KDA_BF16 ? 2 : 4;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+        !aligned(log_alpha, 16) || !aligned(beta, esz))
+        return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status finish(cudaError_t e, cudaStream_t st) {
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (env_flag("KDA_DEBUG_SYNC")) return kda_device_status(st);
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_check_cu_seqlens(const int32_t* cu, int32_t num_seqs, int64_t total_tokens) {
+    if (!cu || num_seqs < 0 || total_tokens < 0) return KDA_ERR_INVALID_ARG;
+    if (cu[0] != 0) return KDA_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        if (cu[n + 1] < cu[n]) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)cu[num_seqs] != total_tokens) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k, const void* v,
+                       const float* log_alpha, const void* beta, const float* initial_state,
+                       const int32_t* cu_seqlens, void* out, float* final_state,
+                       kda_stream_t stream) {
+    kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens && shape->num_seqs > 0 && shape->total_tokens % shape->num_seqs != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_UNSUPPORTED;
+    if (shape->total_tokens > 0) {
+        st = check_tensor_ptrs(shape, q, k, v, log_alpha, beta, out);
+        if (st != KDA_OK) return st;
+    }
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
+        return KDA_ERR_UNSUPPORTED;
+    if (shape->num_seqs == 0) return KDA_OK;
+
+    unsigned int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    kda::PrefillArgs a{q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                       shape->total_tokens, shape->num_seqs, shape->H, shape->dk, shape->dv,
+                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, status};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const char* force = getenv("KDA_PREFILL_IMPL");
+    const bool want_recurrent = force && strcmp(force, "recurrent") == 0;
+    cudaError_t e;
+    if (!want_recurrent && kda::chunk_tc_supported(a))
+        e = kda::launch_chunk_tc_prefill(a, s);
+    else
+        e = kda::launch_recurrent_prefill(a, s);
+    return finish(e, s);
+}
+
+kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k, const void* v,
+                           const float* log_alpha, const void* beta, float* state_inout,
+                           void* out, kda_stream_t stream) {
+    kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->total_tokens != shape->num_seqs) return KDA_ERR_INVALID_ARG;
+    if (shape->num_seqs == 0) return KDA_OK;
+    if (!state_inout) return KDA_ERR_INVALID_ARG;
+    st = check_tensor_ptrs(shape, q, k, v, log_alpha, beta, out);
+    if (st != KDA_OK) return st;
+    if (!aligned(state_inout, 16)) return KDA_ERR_UNSUPPORTED;
+    kda::DecodeArgs a{q, k, v, log_alpha, beta, state_inout, out, shape->num_seqs, shape->H,
+                      shape->dk, shape->dv,
+                      shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return finish(kda::launch_decode(a, s), s);
+}
+
+kda_status kda_device_status(kda_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    unsigned int* p = status_word();
+    if (!p) return KDA_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (word) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    return (word & kda::kStatusTimeout) ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_version(void) { return "kda-gb300 0.1.0 sm_103a"; }
+
+}  // extern "C"

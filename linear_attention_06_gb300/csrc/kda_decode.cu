@@ -1,0 +1,140 @@
+// kda_decode.cu -- one KDA decode step, memory-bound.
+//
+// For each (sequence, head) the fp32 state S (dk x dv) is streamed from HBM
+// once and written back once, in place.  With alpha = exp(log_alpha):
+//   S' = Diag(alpha) S                         decay ("Kimi K3 Architecture
+//                                              Teardown", Visual 5, step one)
+//   r  = S'^T k,  y = S'^T q                   one pass over S'
+//   delta = beta (v - r)                       erase + write with one beta
+//                                              ("Kimi K3 Architecture: KDA,
+//                                              MoE, and Attention", section
+//                                              "Memory as a First-Class Problem")
+//   S  = S' + k delta^T                        written back in place
+//   o  = S^T q = y + (k . q) delta             read after write
+//
+// Layout of the work: one block of 256 threads per (sequence, head).  A row of
+// S (dv fp32) is covered by dv/4 threads with 16-byte loads, so each warp
+// instruction moves whole 512-byte rows; each thread keeps its rows in
+// registers between the read and the write, so S crosses HBM exactly twice.
+// The two column reductions are done per thread over its rows, then across
+// row groups through shared memory.  Loads and stores use the streaming cache
+// hints (each byte is touched once).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void store_as(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_as(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+template <int DK, int DV, typename Tin>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+              const float* __restrict__ log_alpha, const Tin* __restrict__ beta,
+              float* __restrict__ S, Tin* __restrict__ out) {
+    constexpr int LANES = DV / 4;          // threads per row (float4 each)
+    constexpr int RG = kThreads / LANES;   // row groups
+    constexpr int RPT = DK / RG;           // rows per thread
+    static_assert(RPT * RG == DK, "row split");
+
+    const size_t p = blockIdx.x;           // (sequence, head) pair
+    const int c4 = threadIdx.x % LANES;
+    const int g = threadIdx.x / LANES;
+    float4* Sp = reinterpret_cast<float4*>(S + p * DK * DV);
+
+    // Issue the whole state read first so it overlaps the small loads.
+    float4 s[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (size_t)(g + RG * m) * LANES + c4);
+
+    __shared__ float ks[DK], qs[DK], al[DK], vs[DV], dl[DV];
+    __shared__ float red_r[RG][DV], red_y[RG][DV];
+    __shared__ float kq_s;
+    __shared__ float beta_s;
+    for (int i = threadIdx.x; i < DK; i += kThreads) {
+        ks[i] = to_f32(k[p * DK + i]);
+        qs[i] = to_f32(q[p * DK + i]);
+        al[i] = expf(log_alpha[p * DK + i]);
+    }
+    for (int j = threadIdx.x; j < DV; j += kThreads) vs[j] = to_f32(v[p * DV + j]);
+    if (threadIdx.x == 0) beta_s = to_f32(beta[p]);
+    __syncthreads();
+
+    if (threadIdx.x < 32) {               // k . q on warp 0
+        float acc = 0.f;
+        for (int i = threadIdx.x; i < DK; i += 32) acc = fmaf(ks[i], qs[i], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (threadIdx.x == 0) kq_s = acc;
+    }
+
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f), y = r;
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const int i = g + RG * m;
+        const float a = al[i], ki = ks[i], qi = qs[i];
+        s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
+        r.x = fmaf(s[m].x, ki, r.x); r.y = fmaf(s[m].y, ki, r.y);
+        r.z = fmaf(s[m].z, ki, r.z); r.w = fmaf(s[m].w, ki, r.w);
+        y.x = fmaf(s[m].x, qi, y.x); y.y = fmaf(s[m].y, qi, y.y);
+        y.z = fmaf(s[m].z, qi, y.z); y.w = fmaf(s[m].w, qi, y.w);
+    }
+    *reinterpret_cast<float4*>(&red_r[g][4 * c4]) = r;
+    *reinterpret_cast<float4*>(&red_y[g][4 * c4]) = y;
+    __syncthreads();
+
+    for (int j = threadIdx.x; j < DV; j += kThreads) {
+        float rj = 0.f, yj = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < RG; ++gg) { rj += red_r[gg][j]; yj += red_y[gg][j]; }
+        const float d = beta_s * (vs[j] - rj);
+        dl[j] = d;
+        store_as(&out[p * DV + j], fmaf(kq_s, d, yj));
+    }
+    __syncthreads();
+
+    const float4 d4 = *reinterpret_cast<const float4*>(&dl[4 * c4]);
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) {
+        const float ki = ks[g + RG * m];
+        s[m].x = fmaf(ki, d4.x, s[m].x); s[m].y = fmaf(ki, d4.y, s[m].y);
+        s[m].z = fmaf(ki, d4.z, s[m].z); s[m].w = fmaf(ki, d4.w, s[m].w);
+        __stcs(Sp + (size_t)(g + RG * m) * LANES + c4, s[m]);
+    }
+}
+
+template <int DK, int DV>
+cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
+    const unsigned blocks = (unsigned)((size_t)a.num_seqs * a.H);
+    if (a.dtype == DType::F32) {
+        decode_kernel<DK, DV, float><<<blocks, kThreads, 0, st>>>(
+            static_cast<const float*>(a.q), static_cast<const float*>(a.k),
+            static_cast<const float*>(a.v), a.log_alpha, static_cast<const float*>(a.beta),
+            a.state, static_cast<float*>(a.out));
+    } else {
+        decode_kernel<DK, DV, __nv_bfloat16><<<blocks, kThreads, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
+            static_cast<const __nv_bfloat16*>(a.v), a.log_alpha,
+            static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out));
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    if (a.dk == 128 && a.dv == 128) return launch_dims<128, 128>(a, st);
+    if (a.dk == 128 && a.dv == 64) return launch_dims<128, 64>(a, st);
+    if (a.dk == 64 && a.dv == 128) return launch_dims<64, 128>(a, st);
+    return launch_dims<64, 64>(a, st);
+}
+
+}  // namespace kda

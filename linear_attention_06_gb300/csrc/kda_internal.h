@@ -1,0 +1,54 @@
+// kda_internal.h -- launchers shared between the translation units of libkda.
+// Not part of the public ABI (that is include/kda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+enum class DType : int { BF16 = 0, F32 = 1 };
+
+// Everything a prefill launch needs; pointers are device pointers.
+struct PrefillArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const void* beta;
+    const float* initial_state;   // may be null (zeros)
+    const int32_t* cu_seqlens;    // may be null (equal split)
+    void* out;
+    float* final_state;           // may be null
+    int64_t total_tokens;
+    int32_t num_seqs;
+    int32_t H, dk, dv;
+    DType dtype;
+    unsigned int* status;         // device status word (timeouts)
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* log_alpha;
+    const void* beta;
+    float* state;
+    void* out;
+    int32_t num_seqs;
+    int32_t H, dk, dv;
+    DType dtype;
+};
+
+// fp32 recurrent prefill (any supported dtype / head size).
+cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
+// Chunkwise tensor-core prefill: bf16, dk = dv = 128.
+bool chunk_tc_supported(const PrefillArgs& a);
+cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s);
+// One decode step.
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Bits of the device status word.
+constexpr unsigned int kStatusTimeout = 1u;
+
+}  // namespace kda

@@ -1,0 +1,116 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, export every symbol that
+include/kda.h declares, and reject bad arguments on the host before any CUDA
+call (so these calls use placeholder pointers that are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_06_gb300 import _lib
+from linear_attention_06_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+FAKE = 0x10000            # 16-byte aligned, never dereferenced
+FAKE_MIS = 0x10002        # misaligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"kda_prefill", "kda_decode_step", "kda_status_string", "kda_version"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} is declared in kda.h but not exported"
+
+
+def test_status_strings_and_version(L):
+    assert _lib.status_string(0) == "KDA_OK"
+    assert _lib.status_string(4) == "KDA_ERR_TIMEOUT"
+    assert _lib.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert "sm_103a" in _lib.version()
+
+
+@pytest.mark.parametrize("cu,T,ok", [
+    ([0, 3, 5], 5, True), ([0], 0, True), ([0, 0, 0], 0, True),
+    ([1, 3], 3, False), ([0, 3, 2], 2, False), ([0, 3, 5], 6, False)])
+def test_check_cu_seqlens(L, cu, T, ok):
+    if ok:
+        _lib.kda_check_cu_seqlens(cu, T)
+    else:
+        with pytest.raises(_lib.KdaError):
+            _lib.kda_check_cu_seqlens(cu, T)
+
+
+def shape(n=2, T=128, H=4, dk=128, dv=128, dt=_lib.KDA_BF16):
+    return _lib.KdaShape(n, T, H, dk, dv, dt)
+
+
+def prefill(L, sh, q=FAKE, k=FAKE, v=FAKE, la=FAKE, b=FAKE, h0=None, cu=None, out=FAKE, fin=None):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return L.kda_prefill(ctypes.byref(sh) if sh is not None else None, p(q), p(k), p(v), p(la),
+                         p(b), p(h0), p(cu), p(out), p(fin), None)
+
+
+def decode(L, sh, q=FAKE, k=FAKE, v=FAKE, la=FAKE, b=FAKE, S=FAKE, out=FAKE):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    return L.kda_decode_step(ctypes.byref(sh), p(q), p(k), p(v), p(la), p(b), p(S), p(out), None)
+
+
+def test_prefill_rejects_bad_arguments_before_any_cuda_call(L):
+    E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
+    assert prefill(L, None) == E_ARG
+    for kw in ("q", "k", "v", "la", "b", "out"):
+        assert prefill(L, shape(), **{kw: None}) == E_ARG, kw
+    assert prefill(L, shape(n=-1)) == E_ARG
+    assert prefill(L, shape(T=-5)) == E_ARG
+    assert prefill(L, shape(H=0)) == E_ARG
+    assert prefill(L, shape(n=0, T=10)) == E_ARG
+    assert prefill(L, shape(n=3, T=128)) == E_ARG          # 128 % 3 != 0 without cu_seqlens
+    assert prefill(L, shape(dk=96)) == E_UNS
+    assert prefill(L, shape(dv=32)) == E_UNS
+    assert prefill(L, shape(dt=7)) == E_UNS
+    assert prefill(L, shape(), q=FAKE_MIS) == E_UNS
+    assert prefill(L, shape(), la=FAKE + 4) == E_UNS
+    assert prefill(L, shape(), b=FAKE + 1) == E_UNS          # bf16 beta must be 2-byte aligned
+    assert prefill(L, shape(dt=_lib.KDA_F32), b=FAKE + 2) == E_UNS
+    assert prefill(L, shape(), h0=FAKE + 8) == E_UNS
+    assert prefill(L, shape(), fin=FAKE + 8) == E_UNS
+    assert prefill(L, shape(), cu=FAKE + 2) == E_UNS
+
+
+def test_empty_calls_are_noops(L):
+    assert prefill(L, shape(n=0, T=0), q=None, k=None, v=None, la=None, b=None, out=None) == 0
+    assert decode(L, shape(n=0, T=0), q=None, k=None, v=None, la=None, b=None, S=None,
+                  out=None) == 0
+
+
+def test_decode_rejects_bad_arguments(L):
+    E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
+    assert decode(L, shape(n=4, T=5)) == E_ARG               # one token per sequence
+    assert decode(L, shape(n=4, T=4), S=None) == E_ARG
+    assert decode(L, shape(n=4, T=4), q=None) == E_ARG
+    assert decode(L, shape(n=4, T=4), S=FAKE + 4) == E_UNS
+    assert decode(L, shape(n=4, T=4, dk=32)) == E_UNS
+
+
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert prefill(L, shape()) == _lib.KDA_ERR_CUDA

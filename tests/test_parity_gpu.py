@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (relative L2 over the whole tensor, separately for out and for the
+final state): 1e-4 for fp32 inputs, 5e-3 for bf16 inputs.  Full-size
+workloads are checked on sampled heads: every (sequence, head) pair is an
+independent recurrence, so the oracle computes the sampled heads exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_06_gb300 as kda
+from linear_attention_06_gb300 import workloads
+from tests.gpu_helpers import (TOL, compare_prefill, gpu_prefill, np64, oracle_prefill,
+                               rel_l2)
+from oracle import kda_oracle
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from linear_attention_06_gb300 import build
+    build.build()
+
+
+# ---- the tiny fp32 workload (B=1, H=2, T=256, d=64) ---------------------------------
+def test_tiny_fp32_workload():
+    w = workloads.tiny_fp32().to(DEV)
+    e_out, e_fin = compare_prefill(w)
+    assert e_out < 1e-4 and e_fin < 1e-4
+
+
+# ---- small shapes: ragged tails, short sequences, both head sizes, both dtypes ------
+@pytest.mark.parametrize("lens", [[1], [15], [17], [63], [64], [65], [100], [300],
+                                  [1, 64, 65, 130], [5, 0, 200, 16, 129]])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_small_ragged_d128(lens, dtype):
+    cu = workloads.cu_from_lengths(lens)
+    w = workloads.make_inputs(cu[-1], 3, 128, 128, dtype=dtype, seed=sum(lens),
+                              cu_seqlens=cu, state_std=0.05).to(DEV)
+    compare_prefill(w)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_small_head_sizes(dk, dv, dtype):
+    cu = [0, 77, 77 + 190]
+    w = workloads.make_inputs(cu[-1], 2, dk, dv, dtype=dtype, seed=dk + dv,
+                              cu_seqlens=cu, state_std=0.05).to(DEV)
+    compare_prefill(w)
+
+
+def test_dense_batch_without_cu_seqlens():
+    w = workloads.make_inputs(4 * 150, 2, 128, 128, seed=5, num_seqs=4).to(DEV)
+    out, fin = kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, None, None,
+                               final_state=True, num_seqs=4)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(w)
+    assert rel_l2(np64(out), ro) < 5e-3 and rel_l2(np64(fin), rf) < 5e-3
+
+
+def test_host_cu_seqlens_is_validated_and_copied():
+    cu = [0, 33, 140]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=6, cu_seqlens=cu).to(DEV)
+    compare_prefill(w, cu_on_device=False)
+    with pytest.raises(kda.KdaError):
+        kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, None, [0, 50, 40],
+                        final_state=True)
+
+
+# ---- decay and write-strength edge cases --------------------------------------------
+def test_no_write_no_decay_keeps_state():
+    cu = [0, 90, 200]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=7, cu_seqlens=cu, state_std=0.05).to(DEV)
+    w.beta.zero_()
+    w.log_alpha.zero_()
+    out, fin = gpu_prefill(w)
+    assert torch.equal(fin, w.initial_state)
+
+
+@pytest.mark.parametrize("mode", ["strong", "minus_inf", "mixed", "beta_one_two"])
+def test_extreme_decay_and_beta(mode):
+    cu = [0, 64, 64 + 150]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, dtype=torch.bfloat16, seed=8,
+                              cu_seqlens=cu, state_std=0.05).to(DEV)
+    if mode == "strong":
+        w.log_alpha.mul_(40.0)                    # ~ -2 per token: e^-128 over a chunk
+    elif mode == "minus_inf":
+        w.log_alpha[10::37, :, ::3] = float("-inf")
+    elif mode == "mixed":
+        w.log_alpha[:, :, :64] = -30.0            # half the channels forget at once
+    else:
+        w.beta[::2] = 1.0
+        w.beta[1::4] = 2.0
+    compare_prefill(w)
+
+
+# ---- full-size workloads, sampled heads ---------------------------------------------
+def test_prefill_bf16_full_size_sampled_heads():
+    w = workloads.prefill_bf16(device=DEV)
+    compare_prefill(w, heads=[0, 13, 31])
+
+
+def test_long_prefill_resume_equals_full_run():
+    w = workloads.long_prefill(device=DEV)
+    T = w.total_tokens
+    m = T // 2
+    full_out, full_fin = gpu_prefill(w)
+    o1, s1 = kda.kda_prefill(w.q[:m], w.k[:m], w.v[:m], w.log_alpha[:m], w.beta[:m],
+                             None, None, final_state=True)
+    o2, s2 = kda.kda_prefill(w.q[m:], w.k[m:], w.v[m:], w.log_alpha[m:], w.beta[m:],
+                             s1, None, final_state=True)
+    torch.cuda.synchronize()
+    # the split lands on a chunk boundary and the kernels are deterministic
+    assert torch.equal(torch.cat([o1, o2]), full_out)
+    assert torch.equal(s2, full_fin)
+    heads = [0, 31]
+    ro, rf = oracle_prefill(w, heads)
+    assert rel_l2(np64(full_out[:, heads]), ro) < 5e-3
+    assert rel_l2(np64(full_fin[:, heads]), rf) < 5e-3
+
+
+def test_varlen_full_size_sampled_heads():
+    w = workloads.varlen_prefill(device=DEV)
+    compare_prefill(w, heads=[0, 31])
+
+
+def test_decode_full_size():
+    w = workloads.decode_inputs(device=DEV)
+    S = w.initial_state.clone()
+    out = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S)
+    torch.cuda.synchronize()
+    ro, rS = kda_oracle.decode_step(np64(w.q), np64(w.k), np64(w.v), np64(w.log_alpha),
+                                    np64(w.beta), np64(w.initial_state))
+    assert rel_l2(np64(out), ro) < 5e-3
+    assert rel_l2(np64(S), rS) < 5e-3
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_small(dk, dv, dtype):
+    n = 37
+    w = workloads.make_inputs(n, 3, dk, dv, dtype=dtype, seed=dk * 3 + dv,
+                              cu_seqlens=list(range(n + 1)), state_std=0.05).to(DEV)
+    S = w.initial_state.clone()
+    out = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S)
+    torch.cuda.synchronize()
+    ro, rS = kda_oracle.decode_step(np64(w.q), np64(w.k), np64(w.v), np64(w.log_alpha),
+                                    np64(w.beta), np64(w.initial_state))
+    assert rel_l2(np64(out), ro) < TOL[dtype] and rel_l2(np64(S), rS) < TOL[dtype]
+
+
+# ---- internal invariants ------------------------------------------------------------
+def test_decode_equals_one_token_prefill():
+    n = 64
+    w = workloads.make_inputs(n, 4, 128, 128, seed=21, cu_seqlens=list(range(n + 1)),
+                              state_std=0.05).to(DEV)
+    S = w.initial_state.clone()
+    o_d = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S)
+    o_p, S_p = gpu_prefill(w)
+    assert rel_l2(np64(o_d), np64(o_p)) < 5e-3 and rel_l2(np64(S), np64(S_p)) < 5e-3
+
+
+def test_varlen_equals_separate_runs():
+    lens = [70, 1, 300, 64]
+    cu = workloads.cu_from_lengths(lens)
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=22, cu_seqlens=cu, state_std=0.05).to(DEV)
+    out, fin = gpu_prefill(w)
+    for n in range(len(lens)):
+        s, e = cu[n], cu[n + 1]
+        o_n, f_n = kda.kda_prefill(w.q[s:e], w.k[s:e], w.v[s:e], w.log_alpha[s:e], w.beta[s:e],
+                                   w.initial_state[n:n + 1].contiguous(), None, final_state=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o_n, out[s:e]) and torch.equal(f_n[0], fin[n])
+
+
+def test_final_state_may_alias_initial_state():
+    cu = [0, 100, 250]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=23, cu_seqlens=cu, state_std=0.05).to(DEV)
+    _, ref = gpu_prefill(w)
+    S = w.initial_state.clone()
+    kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, S, w.cu_seqlens.to(DEV), final_state=S)
+    torch.cuda.synchronize()
+    assert torch.equal(S, ref)
+
+
+def test_recurrent_and_chunk_paths_agree(monkeypatch):
+    cu = [0, 200, 333]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=24, cu_seqlens=cu, state_std=0.05).to(DEV)
+    o_a, f_a = gpu_prefill(w)
+    monkeypatch.setenv("KDA_PREFILL_IMPL", "recurrent")
+    o_b, f_b = gpu_prefill(w)
+    assert rel_l2(np64(o_a), np64(o_b)) < 5e-3 and rel_l2(np64(f_a), np64(f_b)) < 5e-3
+
+
+def test_device_status_is_clean():
+    assert kda.kda_device_status() == 0
