@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""KDA on GB300: prefill tokens/s (H=32, d=128) and decode-step HBM GB/s.
+
+One step = one KDA prefill pass (kda_prefill, C ABI) over the bf16 workload
+B=4, H=32, T=8192, dk=dv=128 (q, k, v, beta bf16; log_alpha fp32; zero initial
+state; final states returned), inputs resident in HBM.  The decode step
+(kda_decode_step, 256 sequences x H=32, fp32 state in place) is timed in the
+same run and reported under "decode".  Inputs are larger than L2 (1.6 GB and
+1.1 GB), so no flush is needed between iterations.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (one process per GPU, launched by torch.distributed.run) every rank
+runs its own batch (weak scaling, no data-path collective); timing is the max
+over ranks.  --impl reference times the fp64 CPU oracle on a bounded sample of
+the same workload (host cores) and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=32,d=128) + decode-step HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+WORKLOAD = "kda_prefill_bf16_B4_H32_T8192_d128"
+B, T, H, D = 4, 8192, 32, 128
+DEC_N = 256
+# algorithmic bytes per token-head: q, k, v bf16 (768) + log_alpha fp32 (512) + beta (2) + out (256)
+BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 2 + D * 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_bytes(tokens, heads, num_seqs, with_h0=False):
+    return tokens * heads * BYTES_PER_TOKEN_HEAD + num_seqs * heads * D * D * 4 * (2 if with_h0 else 1)
+
+
+def decode_bytes(n, heads):
+    # state read + write (fp32) + q, k, v, out bf16 + log_alpha fp32 + beta bf16
+    return n * heads * (2 * D * D * 4 + 4 * D * 2 + D * 4 + 2)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU works."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_lines(out)
+
+
+def parse_clock_lines(out):
+    """Summarise nvidia-smi CSV samples: median SM clock under load, max clock,
+    and every throttle reason seen active."""
+    rows = []
+    for line in out.strip().splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), hw=parts[5],
+                             hwt=parts[6], swt=parts[7], pcap=parts[8],
+                             util=float(parts[9]) if parts[9] not in ("", "[N/A]") else 0.0))
+        except ValueError:
+            continue
+    busy = [r for r in rows if r["util"] > 0] or rows
+    if not busy:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    sms = sorted(r["sm"] for r in busy)
+    reasons = set()
+    for r in busy:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in busy),
+            "reasons": sorted(reasons), "samples": len(busy)}
+
+
+def source_digest():
+    """Digest of the prefill kernel source; a stored ncu traffic figure is used
+    only while it matches the kernel that is running."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kda_chunk_tc.cu", "sm103_primitives.cuh"):
+        with open(os.path.join(ROOT, "linear_attention_06_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_digest):
+    p = os.path.join(ROOT, "profiles", "ncu_traffic_chunk_tc_prefill.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_digest") != kernel_digest:
+        return None
+    return d.get("dram_bytes_per_launch_full_workload")
+
+
+def oracle_sample(budget_s, threads=0):
+    """Time the fp64 oracle on a bounded sample of the prefill workload (one
+    8192-token sequence, as many heads as fit the time budget)."""
+    import numpy as np
+    from linear_attention_06_gb300 import workloads
+    from oracle import kda_oracle
+    cores = os.cpu_count() or 1
+    used = kda_oracle.max_threads() if threads == 0 else threads
+    w = workloads.make_inputs(T, H, D, D, seed=1, num_seqs=1)       # same recipe, one sequence
+    arr = [np.ascontiguousarray(x.float().numpy().astype(np.float64))
+           for x in (w.q, w.k, w.v, w.log_alpha, w.beta)]
+
+    def run(heads):
+        sl = [a[:, :heads].copy() for a in arr]
+        t0 = time.perf_counter()
+        kda_oracle.prefill(*sl, None, cu_seqlens=[0, T], num_threads=used)
+        return time.perf_counter() - t0
+
+    t1 = run(1)                                    # one (sequence, head) pair = one thread's work
+    per_thread = max(1, int(budget_s / max(t1, 1e-6)))
+    heads = max(1, min(H, per_thread * max(1, used)))
+    return run, heads, cores, used
+
+
+class Ranks:
+    """Process-group plumbing for N > 1: barrier and max over ranks.  Works with
+    nccl (GPU tensors) or gloo (CPU tensors); a single process needs neither."""
+
+    def __init__(self, backend=None, device=None):
+        import torch.distributed as dist
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.device = device
+        if self.world > 1 and not dist.is_initialized():
+            kw = {"device_id": device} if backend == "nccl" else {}
+            dist.init_process_group(backend or "gloo", **kw)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1 and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    budget = max(1.0, args.ref_step_budget)
+    run, heads, cores, used = oracle_sample(budget)
+    for _ in range(args.warmup):
+        run(heads)
+    t = sum(run(heads) for _ in range(args.steps)) / args.steps
+    value = heads * T / t / H                      # token-heads/s over H heads = tokens/s
+    sample = f"fp64 oracle, 1 sequence x {heads} of {H} heads x {T} tokens per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B, "seq_len": T, "heads": H,
+                       "head_dim": D, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    import linear_attention_06_gb300 as kda
+    from linear_attention_06_gb300 import workloads
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ranks = Ranks("nccl", dev)
+    world, rank = ranks.world, ranks.rank
+    barrier, max_over_ranks = ranks.barrier, ranks.max
+
+    stream = torch.cuda.current_stream()
+    w = workloads.prefill_bf16(device=dev, seed=1 + rank)
+    cu = w.cu_seqlens.to(dev)
+    out = torch.empty_like(w.v)
+    fin = torch.empty((B, H, D, D), dtype=torch.float32, device=dev)
+
+    def prefill_step():
+        kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, None, cu, out, fin, stream=stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        prefill_step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        prefill_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_prefill = max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+    prefill_launches = args.steps                 # one kernel launch per prefill step
+
+    # ---- decode step (256 sequences x 32 heads), state updated in place
+    dw = workloads.decode_inputs(device=dev, seed=2 + rank)
+    S = dw.initial_state.clone()
+    dout = torch.empty_like(dw.v)
+
+    def decode_step():
+        kda.kda_decode_step(dw.q, dw.k, dw.v, dw.log_alpha, dw.beta, S, dout, stream=stream)
+
+    for _ in range(args.warmup):
+        decode_step()
+    torch.cuda.synchronize()
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        decode_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_decode = max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+    clocks = sampler.stop()
+
+    # ---- end to end through the public API with host buffers (pinned)
+    e2e = None
+    if not args.no_e2e:
+        host = {k: getattr(w, k).cpu().pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
+        dq, dk_, dv_, dla, db = (torch.empty_like(getattr(w, k)) for k in ("q", "k", "v", "log_alpha", "beta"))
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hfin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
+
+        def e2e_step():
+            dq.copy_(host["q"], non_blocking=True)
+            dk_.copy_(host["k"], non_blocking=True)
+            dv_.copy_(host["v"], non_blocking=True)
+            dla.copy_(host["log_alpha"], non_blocking=True)
+            db.copy_(host["beta"], non_blocking=True)
+            kda.kda_prefill(dq, dk_, dv_, dla, db, None, cu, out, fin, stream=stream)
+            hout.copy_(out, non_blocking=True)
+            hfin.copy_(fin, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t_e2e = max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+        e2e = {"value": world * B * T / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3}
+
+    if rank != 0:
+        ranks.close()
+        return
+
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    pbytes = prefill_bytes(B * T, H, B)
+    achieved = pbytes / t_prefill / 1e9
+    digest = source_digest()
+    dbytes = decode_bytes(DEC_N, H)
+    dec_gbs = dbytes / t_decode / 1e9
+    line = {
+        "metric": METRIC, "value": world * B * T / t_prefill, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_prefill * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world * B, "seq_len": T, "heads": H,
+                   "head_dim": D, "chunk": 64, "initial_state": "zeros", "final_state": "returned",
+                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": stored_traffic(digest),
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "chunk_tc_kernel",
+                     "algorithmic_bytes_per_launch": pbytes, "source_digest": digest},
+        "decode": {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}", "us_per_step": t_decode * 1e6,
+                   "achieved_gbs": dec_gbs, "peak_gbs": hbm, "frac": dec_gbs / hbm,
+                   "algorithmic_bytes_per_launch": dbytes, "kernel": "decode_kernel"},
+        "e2e": e2e, "gpu_launches": prefill_launches, "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        run, heads, cores, used = oracle_sample(args.cpu_budget)
+        t = run(heads)
+        line["cpu_baseline"] = {"value": heads * T / t / H, "unit": UNIT, "cores": used,
+                                "kind": "oracle",
+                                "sample": f"fp64 oracle on 1 sequence x {heads} of {H} heads x {T} tokens "
+                                          f"({t:.1f} s, {cores} host cores)"}
+    print(json.dumps(line), flush=True)
+    ranks.close()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-step-budget", type=float, default=4.0,
+                    help="seconds of oracle work per step in --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
