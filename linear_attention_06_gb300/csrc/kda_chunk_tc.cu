@@ -83,7 +83,11 @@ constexpr uint32_t kPP = kTT + 8192;               // P   64 x 128 B        8 KB
 constexpr uint32_t kWT = kPP + 8192;               // -W'^T 128 x 128 B    16 KB
 constexpr uint32_t kSmemUsed = kWT + 16384;        // 212992
 constexpr uint32_t kSmemDynamic = kSmemUsed + 1024;
-constexpr uint32_t kNStride = 68;                  // fp32 row stride of the N matrix
+// The UT solve works on 16x16 blocks of the strictly lower 64x64 matrix
+// N = Diag(beta) L(A) and of X = (I + N)^-1, kept in the stage's log_alpha slot
+// (free by then) as the 10 lower-triangular blocks each, row stride 20 floats.
+constexpr uint32_t kBlkStride = 20, kBlkBytes = 16 * kBlkStride * 4;          // 1280
+constexpr uint32_t kSolveN = 0, kSolveX = 10 * kBlkBytes, kSolveY = 20 * kBlkBytes;
 constexpr uint32_t kLoadBytes = 81920;             // q, k, v, log_alpha tiles of one chunk
 constexpr uint32_t kReloadBytes = 65536;           // q, k, log_alpha again (split chunks)
 
@@ -145,8 +149,10 @@ __device__ __forceinline__ void issue_tile_loads(uint8_t* stage, const Maps& m, 
 __device__ int next_run(const float* A, int r0, int L) {
     const int c = threadIdx.x;
     if (r0 == 0) {
-        float tot = 0.f;
-        for (int r = 0; r < L; ++r) tot += A[r * D + c];
+        float t4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < C; ++r) t4[r & 3] += (r < L) ? A[r * D + c] : 0.f;
+        const float tot = (t4[0] + t4[1]) + (t4[2] + t4[3]);
         if (!__syncthreads_or(!(fabsf(tot) <= kMaxExponent))) return L;
     }
     float acc = 0.f;
@@ -164,30 +170,41 @@ __device__ int next_run(const float* A, int r0, int L) {
 
 // Khat, Qhat (in place over k, q) and Kb for the rows [r0, r1); other rows are
 // zeroed.  gam[c] = e^{G_c}, the decay of the whole run.  Thread = key channel.
+// The 64 log-decays are first pulled into registers and turned into suffix
+// sums, so the exponentials and the tile stores carry no loop dependency.
 __device__ void build_operands(uint8_t* sm, uint32_t stage, int r0, int r1, float* gam) {
     const int c = threadIdx.x;
     uint8_t* stg = sm + stage;
     const float* A = reinterpret_cast<const float*>(stg + kA);
-    const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
-    float e = 0.f;   // sum of log_alpha over the run's tokens after row r
+    float e[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) e[r] = (r >= r0 && r < r1) ? A[r * D + c] : 0.f;
+    float run = 0.f;   // sum of log_alpha over the run's tokens after row r
+#pragma unroll
     for (int r = C - 1; r >= 0; --r) {
+        const float ar = e[r];
+        e[r] = run;
+        run += ar;
+    }
+    gam[c] = __expf(run);
+    const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
         __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(stg + qk_off(false, r, c));
         __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(stg + qk_off(true, r, c));
         __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(sm + kKB + half_off(r, c));
         if (r >= r0 && r < r1) {
             const float kv = bf2f(*kp), qv = bf2f(*qp);
-            const float up = __expf(-e), dn = __expf(e);
+            const float up = __expf(-e[r]), dn = __expf(e[r]);
             *kp = __float2bfloat16_rn(kv * up);
             *qp = __float2bfloat16_rn(qv * up);
             *bp = __float2bfloat16_rn(kv * dn);
-            e += A[r * D + c];
         } else {
             *kp = zero;
             *qp = zero;
             *bp = zero;
         }
     }
-    gam[c] = __expf(e);
 }
 
 // TMEM S^T (lane j = value channel, column c = key channel): S <- S Diag(gam)
@@ -287,17 +304,23 @@ __device__ void read_gram(uint32_t tb, uint8_t* stage, uint8_t* sm, const float*
     ld64(tb, kTmAP, v);
     const int tid = threadIdx.x;
     if (tid < 64) {
-        const int r = tid;
+        const int r = tid, bi = r >> 4, rr = r & 15;
         const float b = beta_s[r];
-        float* Nr = reinterpret_cast<float*>(stage + kA) + r * kNStride;
+        float* Nbase = reinterpret_cast<float*>(stage + kA + kSolveN);
 #pragma unroll
-        for (int s = 0; s < 64; s += 4) {
-            float4 f;
-            f.x = (s + 0 < r) ? b * __uint_as_float(v[s + 0]) : 0.f;
-            f.y = (s + 1 < r) ? b * __uint_as_float(v[s + 1]) : 0.f;
-            f.z = (s + 2 < r) ? b * __uint_as_float(v[s + 2]) : 0.f;
-            f.w = (s + 3 < r) ? b * __uint_as_float(v[s + 3]) : 0.f;
-            *reinterpret_cast<float4*>(Nr + s) = f;
+        for (int bj = 0; bj < 4; ++bj) {
+            if (bj > bi) break;
+            float* dst = Nbase + (bi * (bi + 1) / 2 + bj) * (kBlkBytes / 4) + rr * kBlkStride;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int s0 = 16 * bj + 4 * q4;
+                float4 f;
+                f.x = (s0 + 0 < r) ? b * __uint_as_float(v[s0 + 0]) : 0.f;
+                f.y = (s0 + 1 < r) ? b * __uint_as_float(v[s0 + 1]) : 0.f;
+                f.z = (s0 + 2 < r) ? b * __uint_as_float(v[s0 + 2]) : 0.f;
+                f.w = (s0 + 3 < r) ? b * __uint_as_float(v[s0 + 3]) : 0.f;
+                *reinterpret_cast<float4*>(dst + 4 * q4) = f;
+            }
         }
     } else {
         const int r = tid - 64;
@@ -317,32 +340,132 @@ __device__ void read_gram(uint32_t tb, uint8_t* stage, uint8_t* sm, const float*
     }
 }
 
-// T = (I + N)^{-1} Diag(beta) by forward substitution, one column per thread
-// (threads 0..63), fp32; written as the bf16 K-major operand TT (row r).
-__device__ void solve_T(const uint8_t* stage, uint8_t* sm, const float* beta_s) {
-    const int j = threadIdx.x;
-    const float* Nm = reinterpret_cast<const float*>(stage + kA);
-    float x[64];
+__device__ __forceinline__ float* blk(float* base, int i, int j) {
+    return base + (i * (i + 1) / 2 + j) * (kBlkBytes / 4);
+}
+
+// One warp computes rows [rb, rb + NR) of C = sign * sum_p A_p B_p for 16x16
+// blocks (NP pairs); each lane owns NR/2 consecutive columns of one row.
+template <int NR, int NP>
+__device__ __forceinline__ void blk_product(float* Cb, float* const (&Ab)[NP], float* const (&Bb)[NP],
+                                            int rb, float sign) {
+    constexpr int NC = NR / 2;                  // columns per lane
+    constexpr int LPR = 16 / NC;                // lanes per row
+    const int lane = threadIdx.x & 31;
+    const int rr = rb + lane / LPR, c0 = (lane % LPR) * NC;
+    float acc[NC];
 #pragma unroll
-    for (int r = 0; r < 64; ++r) x[r] = 0.f;
+    for (int u = 0; u < NC; ++u) acc[u] = 0.f;
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-        float acc = (r == j) ? 1.f : 0.f;
+    for (int p = 0; p < NP; ++p) {
+        float arow[16];
 #pragma unroll
-        for (int s = 0; s < r; s += 4) {
-            const float4 n4 = *reinterpret_cast<const float4*>(Nm + r * kNStride + s);
-            acc = fmaf(-n4.x, x[s + 0], acc);
-            acc = fmaf(-n4.y, x[s + 1], acc);
-            acc = fmaf(-n4.z, x[s + 2], acc);
-            acc = fmaf(-n4.w, x[s + 3], acc);
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(Ab[p] + rr * kBlkStride + 4 * k4);
+            arow[4 * k4] = a4.x; arow[4 * k4 + 1] = a4.y; arow[4 * k4 + 2] = a4.z; arow[4 * k4 + 3] = a4.w;
         }
-        x[r] = acc;
-    }
-    const float bj = beta_s[j];
 #pragma unroll
-    for (int r = 0; r < 64; ++r)
-        *reinterpret_cast<__nv_bfloat16*>(sm + kTT + sw128_offset(r, 2 * j)) =
-            __float2bfloat16_rn(x[r] * bj);
+        for (int k = 0; k < 16; ++k) {
+            const float* brow = Bb[p] + k * kBlkStride + c0;
+#pragma unroll
+            for (int u = 0; u < NC; u += 2) {
+                const float2 b2 = *reinterpret_cast<const float2*>(brow + u);
+                acc[u] = fmaf(arow[k], b2.x, acc[u]);
+                acc[u + 1] = fmaf(arow[k], b2.y, acc[u + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < NC; u += 2)
+        *reinterpret_cast<float2*>(Cb + rr * kBlkStride + c0 + u) = make_float2(sign * acc[u], sign * acc[u + 1]);
+}
+
+// T = (I + N)^{-1} Diag(beta), N strictly lower (64 x 64), by 16x16 blocks:
+// the four diagonal blocks D_i = (I + N_ii)^{-1} by forward substitution, then
+// X_ij = -D_i sum_{k=j}^{i-1} N_ik X_kj one block sub-diagonal at a time.
+// All 128 threads take part; fp32 throughout.  T goes to the bf16 K-major
+// operand tile TT (row r = token, column s).
+__device__ void solve_T(uint8_t* stage, uint8_t* sm, const float* beta_s) {
+    float* Nb = reinterpret_cast<float*>(stage + kA + kSolveN);
+    float* Xb = reinterpret_cast<float*>(stage + kA + kSolveX);
+    float* Yb = reinterpret_cast<float*>(stage + kA + kSolveY);
+    const int tid = threadIdx.x, w = tid >> 5;
+    if (tid < 64) {                                  // diagonal blocks
+        const int i = tid >> 4, jl = tid & 15;
+        const float* Nii = blk(Nb, i, i);
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == jl) ? 1.f : 0.f;
+#pragma unroll
+            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[r * kBlkStride + q], x[q], acc);
+            x[r] = acc;
+        }
+        float* Xii = blk(Xb, i, i);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
+    }
+    __syncthreads();
+    // first sub-diagonal: Y_i = N_{i+1,i} D_i, X_{i+1,i} = -D_{i+1} Y_i
+    if (w < 3) {
+        float* const A1[1] = {blk(Nb, w + 1, w)};
+        float* const B1[1] = {blk(Xb, w, w)};
+        blk_product<16, 1>(Yb + w * (kBlkBytes / 4), A1, B1, 0, 1.f);
+    }
+    __syncthreads();
+    if (w < 3) {
+        float* const A1[1] = {blk(Xb, w + 1, w + 1)};
+        float* const B1[1] = {Yb + w * (kBlkBytes / 4)};
+        blk_product<16, 1>(blk(Xb, w + 1, w), A1, B1, 0, -1.f);
+    }
+    __syncthreads();
+    // second sub-diagonal: Z_i = N_{i+2,i} D_i + N_{i+2,i+1} X_{i+1,i}; X_{i+2,i} = -D_{i+2} Z_i
+    {
+        const int i = w >> 1, rb = (w & 1) * 8;
+        float* const A2[2] = {blk(Nb, i + 2, i), blk(Nb, i + 2, i + 1)};
+        float* const B2[2] = {blk(Xb, i, i), blk(Xb, i + 1, i)};
+        blk_product<8, 2>(Yb + i * (kBlkBytes / 4), A2, B2, rb, 1.f);
+    }
+    __syncthreads();
+    {
+        const int i = w >> 1, rb = (w & 1) * 8;
+        float* const A1[1] = {blk(Xb, i + 2, i + 2)};
+        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
+        blk_product<8, 1>(blk(Xb, i + 2, i), A1, B1, rb, -1.f);
+    }
+    __syncthreads();
+    // third sub-diagonal: Z = N_30 D_0 + N_31 X_10 + N_32 X_20; X_30 = -D_3 Z
+    {
+        float* const A3[3] = {blk(Nb, 3, 0), blk(Nb, 3, 1), blk(Nb, 3, 2)};
+        float* const B3[3] = {blk(Xb, 0, 0), blk(Xb, 1, 0), blk(Xb, 2, 0)};
+        blk_product<4, 3>(Yb, A3, B3, 4 * w, 1.f);
+    }
+    __syncthreads();
+    {
+        float* const A1[1] = {blk(Xb, 3, 3)};
+        float* const B1[1] = {Yb};
+        blk_product<4, 1>(blk(Xb, 3, 0), A1, B1, 4 * w, -1.f);
+    }
+    __syncthreads();
+    // T[r][s] = X[r][s] beta_s, bf16, row r: thread (r, half) writes 32 columns
+    {
+        const int r = tid >> 1, hf = tid & 1, bi = r >> 4, rr = r & 15;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            const int s0 = 32 * hf + 8 * ch, bj = s0 >> 4;
+            uint32_t wv[4];
+            if (bj <= bi) {
+                const float* xr = blk(Xb, bi, bj) + rr * kBlkStride + (s0 & 15);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    wv[u] = pack_bf16x2(xr[2 * u] * beta_s[s0 + 2 * u], xr[2 * u + 1] * beta_s[s0 + 2 * u + 1]);
+            } else {
+                wv[0] = wv[1] = wv[2] = wv[3] = 0u;
+            }
+            *reinterpret_cast<uint4*>(sm + kTT + sw128_offset(r, 16 * (4 * hf + ch))) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    }
 }
 
 // Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
@@ -370,15 +493,27 @@ __device__ void pack_delta(uint32_t tb) {
     tmem_wait_st();
 }
 
-// Lane j holds O^T row j: write out[t0 + r, h, j] for r in [r0, r1).
-__device__ void store_out(uint32_t tb, __nv_bfloat16* out, int64_t t0, int H, int h, int r0, int r1) {
+// Lane j holds O^T row j.  The rows are transposed through a 64 x 256-byte
+// staging tile (the -W'^T slot, dead after the Delta product) and written as
+// 16-byte row segments, rows [r0, r1) only.
+__device__ void store_out(uint32_t tb, uint8_t* sm, __nv_bfloat16* out, int64_t t0, int H, int h,
+                          int r0, int r1) {
     uint32_t v[64];
     ld64(tb, kTmO, v);
-    const int j = threadIdx.x;
+    const int tid = threadIdx.x;
+    uint8_t* stg = sm + kWT;
 #pragma unroll
     for (int r = 0; r < 64; ++r)
-        if (r >= r0 && r < r1)
-            out[((t0 + r) * H + h) * D + j] = __float2bfloat16_rn(__uint_as_float(v[r]));
+        *reinterpret_cast<__nv_bfloat16*>(stg + r * 256 + tid * 2) = __float2bfloat16_rn(__uint_as_float(v[r]));
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int id = tid + kThreads * m, row = id >> 4, ch = id & 15;
+        if (row >= r0 && row < r1) {
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + ch * 16);
+            *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
+        }
+    }
 }
 
 __device__ void load_state(uint32_t tb, const float* h0, size_t base) {
@@ -407,6 +542,21 @@ __device__ void store_state(uint32_t tb, float* hT, size_t base) {
         for (int i = 0; i < 32; ++i) hT[base + (size_t)(32 * cb + i) * D + j] = __uint_as_float(r[i]);
     }
 }
+
+#ifdef KDA_PHASE_TIMING
+// Diagnostic build only: cycles spent per phase by thread 0 of block 0.
+__device__ unsigned long long g_phase_cycles[16];
+#define KDA_PHASE(i)                                                        \
+    do {                                                                    \
+        if (blockIdx.x == 0 && threadIdx.x == 0) {                          \
+            const long long t_ = clock64();                                 \
+            g_phase_cycles[i] += (unsigned long long)(t_ - phase_t_);       \
+            phase_t_ = t_;                                                  \
+        }                                                                   \
+    } while (0)
+#else
+#define KDA_PHASE(i) do {} while (0)
+#endif
 
 // Make this thread's shared-memory and TMEM writes visible to the tensor core,
 // then synchronise the block.
@@ -470,17 +620,25 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     const uint32_t sKB = smem_u32(sm + kKB), sTT = smem_u32(sm + kTT), sPP = smem_u32(sm + kPP),
                    sWT = smem_u32(sm + kWT);
     bool ok = true;
+#ifdef KDA_PHASE_TIMING
+    long long phase_t_ = clock64();
+#endif
 
+    float braw_next = (tid < C && bos + tid < eos) ? bf2f(beta[(bos + tid) * H + h]) : 0.f;
     for (int c = 0; c < nchunks && ok; ++c) {
         const int st = c & 1;
         uint8_t* stage = sm + st * kStageBytes;
         const uint32_t sQK = sQKbase + st * kStageBytes + kQK, sV = sQKbase + st * kStageBytes + kV;
         const int64_t t0 = bos + (int64_t)c * C;
         const int L = (int)((eos - t0) < C ? (eos - t0) : C);
-        float braw = 0.f;
-        if (tid < L) braw = bf2f(beta[(t0 + tid) * H + h]);
+        const float braw = braw_next;                 // beta of this chunk, loaded one chunk ahead
+        if (c + 1 < nchunks) {
+            const int64_t tn = t0 + C + tid;
+            braw_next = (tid < C && tn < eos) ? bf2f(beta[tn * H + h]) : 0.f;
+        }
 
         ok = wait_all(&full_bar[st], full_ph[st]);
+        KDA_PHASE(0);
         if (!ok) break;
         full_ph[st] ^= 1u;
         pending[st] = false;
@@ -495,11 +653,14 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
                 reload_pending = false;
             }
             const int r1 = next_run(reinterpret_cast<const float*>(stage + kA), r0, L);
+            KDA_PHASE(1);
             if (tid < C) beta_s[tid] = (tid >= r0 && tid < r1) ? braw : 0.f;
             build_operands(sm, st * kStageBytes, r0, r1, gam);
             __syncthreads();
+            KDA_PHASE(2);
             decay_state(tb, gam);
             publish_to_mma();
+            KDA_PHASE(3);
 
             if (tid == 0) {
                 mma_gram(tb, sQK, sKB);
@@ -510,11 +671,14 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mma_ph ^= 1u;
             mma_pending = false;
             tc_fence_after();
+            KDA_PHASE(4);
             read_gram(tb, stage, sm, beta_s);
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid < 64) solve_T(stage, sm, beta_s);
+            KDA_PHASE(5);
+            solve_T(stage, sm, beta_s);
             publish_to_mma();
+            KDA_PHASE(6);
 
             if (tid == 0) {
                 mma_wu(tb, sQK, sV, sTT);
@@ -525,8 +689,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mma_ph ^= 1u;
             mma_pending = false;
             tc_fence_after();
+            KDA_PHASE(7);
             read_w(tb, sm);
             publish_to_mma();
+            KDA_PHASE(8);
 
             if (tid == 0) {
                 mma_delta_out(tb, sWT, sQK);
@@ -537,8 +703,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mma_ph ^= 1u;
             mma_pending = false;
             tc_fence_after();
+            KDA_PHASE(9);
             pack_delta(tb);
             publish_to_mma();
+            KDA_PHASE(10);
 
             if (tid == 0) {
                 mma_state_out(tb, sKB, sPP);
@@ -549,11 +717,13 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mma_ph ^= 1u;
             mma_pending = false;
             tc_fence_after();
-            store_out(tb, out, t0, H, h, r0, r1);
+            KDA_PHASE(11);
+            store_out(tb, sm, out, t0, H, h, r0, r1);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncthreads();
             tc_fence_after();
+            KDA_PHASE(12);
             r0 = r1;
         }
         if (ok && c + 2 < nchunks) {
@@ -606,6 +776,18 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 }
 
 }  // namespace
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_phase_cycles(unsigned long long* host16, int reset) {
+    if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 16 * sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    if (reset) {
+        unsigned long long z[16] = {};
+        if (cudaMemcpyToSymbol(g_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
+    }
+    return 0;
+}
+#endif
 
 bool chunk_tc_supported(const PrefillArgs& a) {
     return a.dtype == DType::BF16 && a.dk == D && a.dv == D && a.total_tokens > 0 &&
