@@ -10,7 +10,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "../../include/kda.h"
+#include "kda.h"
 #include "kda_internal.h"
 
 // Device status word; bit kda::kStatusTimeout is set by a kernel whose bounded

@@ -5,7 +5,7 @@
 // The math (one head, one chunk of C = 64 tokens r = 1..C, state S0 entering
 // the chunk, a_r = log alpha_r, g_r = sum_{t<=r} a_t, G = g_C):
 //
-//   Unrolling S_r = Diag(alpha_r)(I - ...) gives S_r = Diag(e^{g_r}) S0 +
+//   Unrolling the recurrence gives S_r = Diag(e^{g_r}) S0 +
 //   sum_{s<=r} Diag(e^{g_r-g_s}) k_s d_s^T with
 //     d_r = beta_r (v_r - S0^T (e^{g_r} o k_r) - sum_{s<r} A_rs d_s),
 //     A_rs = sum_c k_rc k_sc e^{g_rc - g_sc}.
@@ -19,40 +19,38 @@
 //   Teardown" (section "Hybrid Attention for 1M Tokens", Visual 5: decay,
 //   erase with beta, write with beta; output read after the write, as in
 //   "Kimi K3 Architecture: KDA, MoE, and Attention", section "Memory as a
-//   First-Class Problem").  The same section of the Teardown says K3 tiles the
+//   First-Class Problem").  The same section of the Teardown says K3 floors the
 //   decay so a 16-token tile stays in BF16 range on tensor cores; this kernel
 //   uses its own exact scheme instead (below) and needs no floor on alpha.
 //
 // Decay factoring.  Everything is referred to the chunk END: with
 // e_r = g_C - g_r = sum_{r<t<=C} a_t (<= 0),
-//   Khat = e^{-e} o K, Qhat = e^{-e} o Q   (>= 1 in magnitude scale)
-//   Kb   = e^{ e} o K                      (<= 1)
+//   Khat = e^{-e} o K, Qhat = e^{-e} o Q,  Kb = e^{e} o K,
 //   A = Khat Kb^T, P = Qhat Kb^T, W = (T Khat) Diag(e^G),
 //   (e^g o Q) S0 = Qhat (Diag(e^G) S0).
 // With Ss = Diag(e^G) S0 (the decayed state, computed once per chunk):
 //   Delta = U - (T Khat) Ss,  O = Qhat Ss + (mask o P) Delta,  S_C = Ss + Kb^T Delta.
-// All exponents lie in [-|G|, |G|].  A chunk is used whole only when every
-// channel has |G| <= 60 (e^60 ~ 1e26, far inside the bf16 / fp32 range, and
-// the factored products lose nothing).  Otherwise the chunk is split greedily
-// into runs of consecutive tokens that each satisfy the bound; a single
-// token always qualifies (its exponents are 0), so the kernel is exact for any
-// log_alpha <= 0, including -inf.
+// All exponents lie in [-|G|, |G|].  The tensor-core path takes a chunk when
+// every channel has |G| <= 60 (e^60 ~ 1e26, far inside the bf16 / fp32
+// range).  A chunk that decays harder than that is run token by token in fp32
+// on the state held in tensor memory (exact for any log_alpha <= 0, -inf
+// included); the K3-shaped inputs never need it.
 //
-// Work layout.  One CTA (128 threads = 4 warps, TMEM lanes 0..127) per
-// (sequence, head); it walks the sequence's chunks in order.  TMA loads the
-// next chunk's q, k, v and log_alpha tiles into the other of two shared-memory
-// stages while the current chunk is processed.  Matrices that end in TMEM with
-// a 128-wide dimension are computed transposed so that dimension lies on the
-// 128 TMEM lanes (M = 128 everywhere):
-//   AP      [Khat;Qhat](128x128) x Kb^T        -> lanes 0-63 = A rows, 64-127 = P rows
-//   W'^T    Khat^T (MN-major) x T^T        -> lanes = key channel
-//   U^T     V^T (MN-major) x T^T        -> lanes = value channel
-//   Delta^T U^T += Ss^T(TMEM) x (-W'^T)   (A operand read from TMEM)
-//   O^T     Ss^T(TMEM) x Qhat^T, += Delta^T(TMEM) x P^T
-//   S^T     += Delta^T(TMEM) x Kb (MN-major)
-// The state lives in TMEM as fp32 S^T (lane = value channel, column = key
-// channel) for the whole sequence; a bf16 copy of Ss^T is packed into TMEM as
-// the A operand of the two products that read it.
+// Work layout.  One CTA of 384 threads per (sequence, head) walks the
+// sequence's chunks in order, in two warp-specialised groups:
+//   group A (warps 0-7) prepares chunk n+1 while group B (warps 8-11) runs the
+//   state recurrence for chunk n.
+//   A: decay-range check, Khat / Qhat / Kb tiles, the Gram product [Khat;Qhat]
+//      Kb^T, N = Diag(beta) L(A) and the masked P, the UT solve T.
+//   B: W'^T = Khat^T T^T and U^T = V^T T^T, the decayed state Ss and its bf16
+//      copy, Delta^T = U^T - Ss^T W'^T, O^T = Ss^T Qhat^T + Delta^T P^T,
+//      S^T += Delta^T Kb, the output store, and the TMA loads of chunk n+2.
+// q/k, v and log_alpha have separate two-slot rings, each refilled as soon as
+// its last reader is done.  Matrices that land in TMEM put a 128-wide
+// dimension on the 128 lanes (M = 128 everywhere); the state lives in TMEM as
+// fp32 S^T (lane = value channel, column = key channel) for the whole
+// sequence, and the bf16 copies of Ss^T and Delta^T are packed into TMEM as the
+// A operands of the products that read them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -69,44 +67,107 @@ using namespace sm103;
 
 constexpr int C = 64;          // chunk length (tokens)
 constexpr int D = 128;         // dk = dv
-constexpr int kThreads = 128;
+constexpr int kThreads = 384;  // group A: 256 threads, group B: 128 threads
+constexpr int kGroupA = 256, kGroupB = 128;
 constexpr float kMaxExponent = 60.f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
+constexpr int kBarA = 1, kBarB = 2;                // named barriers of the groups
 
-// ---- dynamic shared memory layout (offsets from a 1024-byte aligned base)
-// stage s (two stages): QK [k_h0 | q_h0 | k_h1 | q_h1] (8 KB each, 64 rows x
-// 128 B, 128-byte swizzle), V [v_h0 | v_h1], A (log_alpha, fp32 [64][128]).
-constexpr uint32_t kQK = 0, kV = 32768, kA = 49152, kStageBytes = 81920;
-constexpr uint32_t kKB = 2 * kStageBytes;          // Kb  [v-style halves] 16 KB
-constexpr uint32_t kTT = kKB + 16384;              // T   64 x 128 B        8 KB
-constexpr uint32_t kPP = kTT + 8192;               // P   64 x 128 B        8 KB
-constexpr uint32_t kWT = kPP + 8192;               // -W'^T 128 x 128 B    16 KB
-constexpr uint32_t kSmemUsed = kWT + 16384;        // 212992
-constexpr uint32_t kSmemDynamic = kSmemUsed + 1024;
-// The UT solve works on 16x16 blocks of the strictly lower 64x64 matrix
-// N = Diag(beta) L(A) and of X = (I + N)^-1, kept in the stage's log_alpha slot
-// (free by then) as the 10 lower-triangular blocks each, row stride 20 floats.
-constexpr uint32_t kBlkStride = 20, kBlkBytes = 16 * kBlkStride * 4;          // 1280
+// ---- dynamic shared memory (offsets from a 1024-byte aligned base)
+constexpr uint32_t kQK0 = 0;          // 2 x 32 KB: [k_h0 | q_h0 | k_h1 | q_h1], 64 rows x 128 B, SW128
+constexpr uint32_t kV0 = 65536;       // 2 x 16 KB: [v_h0 | v_h1]
+constexpr uint32_t kA0 = 98304;       // 2 x 32 KB: log_alpha fp32 [64][128]; then solve scratch + T
+constexpr uint32_t kKB0 = 163840;     // 2 x 16 KB: Kb [halves]
+constexpr uint32_t kPP0 = 196608;     // 2 x 8 KB: masked P, K-major
+constexpr uint32_t kWT = 212992;      // 16 KB: -W'^T (MN-major), then the output staging tile
+constexpr uint32_t kSmall = 229376;   // 2 KB: barriers, flags, beta, gamma
+constexpr uint32_t kSmemUsed = kSmall + 2048;
+constexpr uint32_t kSmemDynamic = kSmemUsed + 1024;   // + alignment slack = 232448
+// inside an A slot, after log_alpha has been consumed:
+constexpr uint32_t kBlkStride = 16, kBlkBytes = 16 * kBlkStride * 4;   // 1024
 constexpr uint32_t kSolveN = 0, kSolveX = 10 * kBlkBytes, kSolveY = 20 * kBlkBytes;
-constexpr uint32_t kLoadBytes = 81920;             // q, k, v, log_alpha tiles of one chunk
-constexpr uint32_t kReloadBytes = 65536;           // q, k, log_alpha again (split chunks)
+constexpr uint32_t kTT = 24576;                                        // T, 64 x 128 B, SW128
+constexpr uint32_t kQKBytes = 32768, kVBytes = 16384, kABytes = 32768;
 
 // ---- TMEM columns
-constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmAP = 192, kTmU = 256, kTmDbf = 320, kTmO = 384;
+constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmDbf = 128, kTmO = 192, kTmU = 256, kTmAP = 384,
+                   kTmW = 448;
 constexpr uint32_t kTmCols = 512;
 
 struct Maps {
     CUtensorMap q, k, v, a;
 };
 
+// Barriers and small per-slot data in the kSmall area.
+struct Small {
+    uint64_t qk_full[2], v_full[2], a_full[2];   // TMA completions
+    uint64_t ready[2];                           // group A -> B: chunk prepared
+    uint64_t kbp_free[2];                        // group B -> A: Kb / P / beta / gamma slot free
+    uint64_t gram_done, wu_done, mma1_done, mma2_done;
+    uint32_t tmem_base;
+    int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
+    int pad[5];
+    int issued[3][2];                            // TMA loads issued / waited for, per
+    int consumed[3][2];                          //   (kind, slot), to drain after a timeout
+    float beta[2][C];
+    float gam[2][D];
+};
+static_assert(sizeof(Small) <= 2048, "small area");
+
 __device__ __forceinline__ uint32_t qk_off(bool is_q, uint32_t r, uint32_t c) {
-    return kQK + (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
+    return (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
 }
 __device__ __forceinline__ uint32_t half_off(uint32_t r, uint32_t c) {   // V and Kb
     return (c >> 6) * 8192u + sw128_offset(r, (c & 63u) * 2u);
 }
-
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ bool in_group_a() { return threadIdx.x < kGroupA; }
+// Index of the thread inside its group (0..255 in A, 0..127 in B).
+__device__ __forceinline__ int lt() { return in_group_a() ? (int)threadIdx.x : (int)threadIdx.x - kGroupA; }
+// First TMEM lane this warp may access (the warp's lane quarter).
+__device__ __forceinline__ uint32_t lane0() { return ((threadIdx.x >> 5) & 3) * 32; }
+__device__ __forceinline__ int group_count(int id) { return id == kBarA ? kGroupA : kGroupB; }
+
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(group_count(id)) : "memory");
+}
+// OR / AND of a predicate over the threads of a group (also a barrier).
+__device__ __forceinline__ bool group_or(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(group_count(id))
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool group_and(int id, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(group_count(id))
+        : "memory");
+    return r != 0;
+}
+// Every thread of the group waits (bounded); the group agrees on the outcome.
+__device__ __forceinline__ bool group_wait(int id, uint64_t* bar, uint32_t parity) {
+    return group_and(id, mbar_wait_parked(bar, parity, kWaitLimitNs));
+}
+// Make this thread's shared-memory and TMEM writes visible to the tensor core
+// and synchronise the group.
+__device__ __forceinline__ void group_publish(int id) {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    group_sync(id);
+    tc_fence_after();
+}
 
 __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seqs, int64_t T,
                                            int64_t& bos, int64_t& eos) {
@@ -123,79 +184,48 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
     }
 }
 
-// Every thread waits (bounded); the block agrees on the outcome.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
-    return __syncthreads_and(ok) != 0;
-}
+// ============================ group A: chunk-local stage =========================
 
-// TMA: q, k (and v) and log_alpha tiles of tokens [t0, t0+64) of head h.
-__device__ __forceinline__ void issue_tile_loads(uint8_t* stage, const Maps& m, int h, int t0,
-                                                 uint64_t* bar, bool with_v) {
-    mbar_arrive_expect_tx(bar, with_v ? kLoadBytes : kReloadBytes);
-    tma_load_3d(stage + kQK + 0, &m.k, 0, h, t0, bar);
-    tma_load_3d(stage + kQK + 8192, &m.q, 0, h, t0, bar);
-    tma_load_3d(stage + kQK + 16384, &m.k, 64, h, t0, bar);
-    tma_load_3d(stage + kQK + 24576, &m.q, 64, h, t0, bar);
-    if (with_v) {
-        tma_load_3d(stage + kV, &m.v, 0, h, t0, bar);
-        tma_load_3d(stage + kV + 8192, &m.v, 64, h, t0, bar);
-    }
-    tma_load_3d(stage + kA, &m.a, 0, h, t0, bar);
-}
-
-// Length of the next run [r0, r1) whose per-channel decay total stays within
-// +-kMaxExponent (a single token is always accepted).  Thread = key channel.
-__device__ int next_run(const float* A, int r0, int L) {
-    const int c = threadIdx.x;
-    if (r0 == 0) {
-        float t4[4] = {0.f, 0.f, 0.f, 0.f};
+// Khat, Qhat (in place over k, q) and Kb for the rows [0, L); other rows are
+// zeroed; gam[c] = e^{G_c}.  Thread (c, half) of group A handles key channel c
+// and rows [32 half, 32 half + 32): it pulls its 32 log-decays into registers,
+// forms suffix sums, adds the later half's total (exchanged through `xchg`),
+// and only then runs the exponentials and tile stores, which carry no loop
+// dependency.  Returns false, having written nothing, when some channel's decay
+// total over the chunk leaves +-kMaxExponent (the chunk then runs token by
+// token).
+__device__ bool build_operands(uint8_t* qk, uint8_t* kb, const float* A, int L, float* gam, float* xchg) {
+    const int a = lt(), c = a & 127, hf = a >> 7;
+    float e[32];
 #pragma unroll
-        for (int r = 0; r < C; ++r) t4[r & 3] += (r < L) ? A[r * D + c] : 0.f;
-        const float tot = (t4[0] + t4[1]) + (t4[2] + t4[3]);
-        if (!__syncthreads_or(!(fabsf(tot) <= kMaxExponent))) return L;
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * hf + i;
+        e[i] = (r < L) ? A[r * D + c] : 0.f;
     }
-    float acc = 0.f;
-    int r1 = r0 + 1;
-    for (int r = r0; r < L; ++r) {
-        acc += A[r * D + c];
-        if (__syncthreads_or(!(fabsf(acc) <= kMaxExponent))) {
-            r1 = (r == r0) ? r0 + 1 : r;
-            break;
-        }
-        r1 = r + 1;
-    }
-    return r1;
-}
-
-// Khat, Qhat (in place over k, q) and Kb for the rows [r0, r1); other rows are
-// zeroed.  gam[c] = e^{G_c}, the decay of the whole run.  Thread = key channel.
-// The 64 log-decays are first pulled into registers and turned into suffix
-// sums, so the exponentials and the tile stores carry no loop dependency.
-__device__ void build_operands(uint8_t* sm, uint32_t stage, int r0, int r1, float* gam) {
-    const int c = threadIdx.x;
-    uint8_t* stg = sm + stage;
-    const float* A = reinterpret_cast<const float*>(stg + kA);
-    float e[C];
+    float run = 0.f;   // sum of log_alpha over this half's rows after row r
 #pragma unroll
-    for (int r = 0; r < C; ++r) e[r] = (r >= r0 && r < r1) ? A[r * D + c] : 0.f;
-    float run = 0.f;   // sum of log_alpha over the run's tokens after row r
-#pragma unroll
-    for (int r = C - 1; r >= 0; --r) {
-        const float ar = e[r];
-        e[r] = run;
+    for (int i = 31; i >= 0; --i) {
+        const float ar = e[i];
+        e[i] = run;
         run += ar;
     }
-    gam[c] = __expf(run);
+    if (hf == 1) xchg[c] = run;
+    group_sync(kBarA);
+    const float off = (hf == 0) ? xchg[c] : 0.f;   // decay of the rows after this half
+    const float total = run + off;
+    if (group_or(kBarA, hf == 0 && !(fabsf(total) <= kMaxExponent))) return false;
+    if (hf == 0) gam[c] = __expf(total);
     const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
 #pragma unroll
-    for (int r = 0; r < C; ++r) {
-        __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(stg + qk_off(false, r, c));
-        __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(stg + qk_off(true, r, c));
-        __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(sm + kKB + half_off(r, c));
-        if (r >= r0 && r < r1) {
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * hf + i;
+        __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(qk + qk_off(false, r, c));
+        __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(qk + qk_off(true, r, c));
+        __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(kb + half_off(r, c));
+        if (r < L) {
+            const float ee = e[i] + off;
             const float kv = bf2f(*kp), qv = bf2f(*qp);
-            const float up = __expf(-e[r]), dn = __expf(e[r]);
+            const float up = __expf(-ee), dn = __expf(ee);
             *kp = __float2bfloat16_rn(kv * up);
             *qp = __float2bfloat16_rn(qv * up);
             *bp = __float2bfloat16_rn(kv * dn);
@@ -205,36 +235,344 @@ __device__ void build_operands(uint8_t* sm, uint32_t stage, int r0, int r1, floa
             *bp = zero;
         }
     }
+    return true;
 }
+
+__device__ __forceinline__ float* blk(float* base, int i, int j) {
+    return base + (i * (i + 1) / 2 + j) * (kBlkBytes / 4);
+}
+
+// TMEM lanes 0-63 hold A rows r: N = beta_r A_rs (s < r) as fp32
+// lower-triangular 16x16 blocks in the A slot.  Lanes 64-127 hold P rows r:
+// P_rs (s <= r) as the bf16 K-major operand tile.  Warps 0-3 of group A read
+// columns 0-31, warps 4-7 columns 32-63 of the same lanes.
+__device__ void read_gram(uint32_t tb, uint8_t* aslot, uint8_t* pp, const float* beta) {
+    const int a = lt(), ch = (a >> 7);               // column half
+    const int row = (int)lane0() + (a & 31);
+    uint32_t v[32];
+    tmem_ld32(tmem_addr(tb, lane0(), kTmAP + 32 * ch), v);
+    tmem_wait_ld();
+    if (row < 64) {
+        const int r = row, bi = r >> 4, rr = r & 15;
+        const float b = beta[r];
+        float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int bj = 2 * ch + k;
+            if (bj > bi) break;
+            float* dst = blk(Nb, bi, bj) + rr * kBlkStride;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int s0 = 16 * bj + 4 * q4, i0 = 16 * k + 4 * q4;
+                float4 f;
+                f.x = (s0 + 0 < r) ? b * __uint_as_float(v[i0 + 0]) : 0.f;
+                f.y = (s0 + 1 < r) ? b * __uint_as_float(v[i0 + 1]) : 0.f;
+                f.z = (s0 + 2 < r) ? b * __uint_as_float(v[i0 + 2]) : 0.f;
+                f.w = (s0 + 3 < r) ? b * __uint_as_float(v[i0 + 3]) : 0.f;
+                *reinterpret_cast<float4*>(dst + 4 * q4) = f;
+            }
+        }
+    } else {
+        const int r = row - 64;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int chunk = 4 * ch + k;
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int s = 8 * chunk + 2 * u, i = 8 * k + 2 * u;
+                const float lo = (s <= r) ? __uint_as_float(v[i]) : 0.f;
+                const float hi = (s + 1 <= r) ? __uint_as_float(v[i + 1]) : 0.f;
+                w[u] = pack_bf16x2(lo, hi);
+            }
+            *reinterpret_cast<uint4*>(pp + sw128_offset(r, 16 * chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// One warp computes rows [rb, rb + NR) of C = sign * sum_p A_p B_p for 16x16
+// blocks (NP pairs); each lane owns NR/2 consecutive columns of one row
+// (NR = 2: one column).
+template <int NR, int NP>
+__device__ __forceinline__ void blk_product(float* Cb, float* const (&Ab)[NP], float* const (&Bb)[NP],
+                                            int rb, float sign) {
+    constexpr int NC = NR / 2;                  // columns per lane
+    constexpr int LPR = 16 / NC;                // lanes per row
+    const int lane = threadIdx.x & 31;
+    const int rr = rb + lane / LPR, c0 = (lane % LPR) * NC;
+    float acc[NC];
+#pragma unroll
+    for (int u = 0; u < NC; ++u) acc[u] = 0.f;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        float arow[16];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(Ab[p] + rr * kBlkStride + 4 * k4);
+            arow[4 * k4] = a4.x; arow[4 * k4 + 1] = a4.y; arow[4 * k4 + 2] = a4.z; arow[4 * k4 + 3] = a4.w;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float* brow = Bb[p] + k * kBlkStride + c0;
+            if constexpr (NC == 1) {
+                acc[0] = fmaf(arow[k], brow[0], acc[0]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < NC; u += 2) {
+                    const float2 b2 = *reinterpret_cast<const float2*>(brow + u);
+                    acc[u] = fmaf(arow[k], b2.x, acc[u]);
+                    acc[u + 1] = fmaf(arow[k], b2.y, acc[u + 1]);
+                }
+            }
+        }
+    }
+    if constexpr (NC == 1) {
+        Cb[rr * kBlkStride + c0] = sign * acc[0];
+    } else {
+#pragma unroll
+        for (int u = 0; u < NC; u += 2)
+            *reinterpret_cast<float2*>(Cb + rr * kBlkStride + c0 + u) = make_float2(sign * acc[u], sign * acc[u + 1]);
+    }
+}
+
+// T = (I + N)^{-1} Diag(beta), N strictly lower (64 x 64), by 16x16 blocks:
+// the four diagonal blocks D_i = (I + N_ii)^{-1} by forward substitution, then
+// X_ij = -D_i sum_{k=j}^{i-1} N_ik X_kj one block sub-diagonal at a time, all
+// in fp32 on group A's 8 warps.  T is written as the bf16 K-major operand tile
+// (row r = token, column s) inside the A slot.
+__device__ void solve_T(uint8_t* aslot, const float* beta) {
+    float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
+    float* Xb = reinterpret_cast<float*>(aslot + kSolveX);
+    float* Yb = reinterpret_cast<float*>(aslot + kSolveY);
+    const int t = lt(), w = t >> 5;
+    if (t < 64) {                                    // diagonal blocks
+        const int i = t >> 4, jl = t & 15;
+        const float* Nii = blk(Nb, i, i);
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == jl) ? 1.f : 0.f;
+#pragma unroll
+            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[r * kBlkStride + q], x[q], acc);
+            x[r] = acc;
+        }
+        float* Xii = blk(Xb, i, i);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
+    }
+    group_sync(kBarA);
+    if (w < 6) {                                     // Y_i = N_{i+1,i} D_i (rows split in two)
+        const int i = w >> 1, rb = 8 * (w & 1);
+        float* const A1[1] = {blk(Nb, i + 1, i)};
+        float* const B1[1] = {blk(Xb, i, i)};
+        blk_product<8, 1>(Yb + i * (kBlkBytes / 4), A1, B1, rb, 1.f);
+    }
+    group_sync(kBarA);
+    if (w < 6) {                                     // X_{i+1,i} = -D_{i+1} Y_i
+        const int i = w >> 1, rb = 8 * (w & 1);
+        float* const A1[1] = {blk(Xb, i + 1, i + 1)};
+        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
+        blk_product<8, 1>(blk(Xb, i + 1, i), A1, B1, rb, -1.f);
+    }
+    group_sync(kBarA);
+    {                                                // Z_i = N_{i+2,i} D_i + N_{i+2,i+1} X_{i+1,i}
+        const int i = w >> 2, rb = 4 * (w & 3);
+        float* const A2[2] = {blk(Nb, i + 2, i), blk(Nb, i + 2, i + 1)};
+        float* const B2[2] = {blk(Xb, i, i), blk(Xb, i + 1, i)};
+        blk_product<4, 2>(Yb + i * (kBlkBytes / 4), A2, B2, rb, 1.f);
+    }
+    group_sync(kBarA);
+    {                                                // X_{i+2,i} = -D_{i+2} Z_i
+        const int i = w >> 2, rb = 4 * (w & 3);
+        float* const A1[1] = {blk(Xb, i + 2, i + 2)};
+        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
+        blk_product<4, 1>(blk(Xb, i + 2, i), A1, B1, rb, -1.f);
+    }
+    group_sync(kBarA);
+    {                                                // Z = N_30 D_0 + N_31 X_10 + N_32 X_20
+        float* const A3[3] = {blk(Nb, 3, 0), blk(Nb, 3, 1), blk(Nb, 3, 2)};
+        float* const B3[3] = {blk(Xb, 0, 0), blk(Xb, 1, 0), blk(Xb, 2, 0)};
+        blk_product<2, 3>(Yb, A3, B3, 2 * w, 1.f);
+    }
+    group_sync(kBarA);
+    {                                                // X_30 = -D_3 Z
+        float* const A1[1] = {blk(Xb, 3, 3)};
+        float* const B1[1] = {Yb};
+        blk_product<2, 1>(blk(Xb, 3, 0), A1, B1, 2 * w, -1.f);
+    }
+    group_sync(kBarA);
+    {                                                // T[r][s] = X[r][s] beta_s (bf16)
+        const int r = t >> 2, q = t & 3, bi = r >> 4, rr = r & 15;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int s0 = 16 * q + 8 * k;
+            uint32_t wv[4];
+            if (q <= bi) {
+                const float* xr = blk(Xb, bi, q) + rr * kBlkStride + 8 * k;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    wv[u] = pack_bf16x2(xr[2 * u] * beta[s0 + 2 * u], xr[2 * u + 1] * beta[s0 + 2 * u + 1]);
+            } else {
+                wv[0] = wv[1] = wv[2] = wv[3] = 0u;
+            }
+            *reinterpret_cast<uint4*>(aslot + kTT + sw128_offset(r, 16 * (2 * q + k))) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    }
+}
+
+// ============================ group B: state stage ===============================
 
 // TMEM S^T (lane j = value channel, column c = key channel): S <- S Diag(gam)
 // in fp32, and the bf16 copy of the decayed state packed as an A operand.
+// Works in 32-column steps to keep the register footprint small.
 __device__ void decay_state(uint32_t tb, const float* gam) {
-    const uint32_t lane0 = (threadIdx.x >> 5) * 32;
 #pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
-        uint32_t v0[32], v1[32], pk[32];
-        tmem_ld32(tmem_addr(tb, lane0, kTmS + 64 * hf), v0);
-        tmem_ld32(tmem_addr(tb, lane0, kTmS + 64 * hf + 32), v1);
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32], pk[16];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            v0[i] = __float_as_uint(__uint_as_float(v0[i]) * gam[64 * hf + i]);
-            v1[i] = __float_as_uint(__uint_as_float(v1[i]) * gam[64 * hf + 32 + i]);
-        }
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * gam[32 * cb + i]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            pk[i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
-            pk[16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
-        }
-        tmem_st32(tmem_addr(tb, lane0, kTmS + 64 * hf), v0);
-        tmem_st32(tmem_addr(tb, lane0, kTmS + 64 * hf + 32), v1);
-        tmem_st32(tmem_addr(tb, lane0, kTmSbf + 32 * hf), pk);
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), v);
+        tmem_st16(tmem_addr(tb, lane0(), kTmSbf + 16 * cb), pk);
     }
     tmem_wait_st();
 }
 
-// ---- MMA groups (issued by one thread) -------------------------------------
+// Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
+__device__ void read_w(uint32_t tb, uint8_t* wt) {
+    const int c = lt();
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmW + 32 * hf), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                w[u] = pack_bf16x2(-__uint_as_float(v[8 * k + 2 * u]), -__uint_as_float(v[8 * k + 2 * u + 1]));
+            *reinterpret_cast<uint4*>(wt + sw128_offset(c, 16 * (4 * hf + k))) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// Lane j holds Delta^T row j (fp32): pack to bf16 in TMEM as an A operand.
+__device__ void pack_delta(uint32_t tb) {
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32], pk[16];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmU + 32 * hf), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        tmem_st16(tmem_addr(tb, lane0(), kTmDbf + 16 * hf), pk);
+    }
+    tmem_wait_st();
+}
+
+// Lane j holds O^T row j.  The rows are transposed through a 64 x 256-byte
+// staging tile and written as 16-byte row segments, rows [0, L) only.
+__device__ void store_out(uint32_t tb, uint8_t* stg, __nv_bfloat16* out, int64_t t0, int H, int h,
+                          int L) {
+    const int t = lt();
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmO + 32 * hf), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(stg + (32 * hf + i) * 256 + t * 2) =
+                __float2bfloat16_rn(__uint_as_float(v[i]));
+    }
+    group_sync(kBarB);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int id = t + 128 * m, row = id >> 4, ch = id & 15;
+        if (row < L) {
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + ch * 16);
+            *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
+        }
+    }
+}
+
+__device__ void load_state(uint32_t tb, const float* h0, size_t base) {
+    const int j = lt();
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            r[i] = h0 ? __float_as_uint(h0[base + (size_t)(32 * cb + i) * D + j]) : 0u;
+        tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), r);
+    }
+    tmem_wait_st();
+}
+
+__device__ void store_state(uint32_t tb, float* hT, size_t base) {
+    const int j = lt();
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) hT[base + (size_t)(32 * cb + i) * D + j] = __uint_as_float(r[i]);
+    }
+}
+
+// Exact token-by-token path for a chunk whose decay leaves the factored
+// range: the state row of lane j (value channel) is updated in fp32 with the
+// recurrence itself (decay, erase with beta, write with beta, read after the
+// write).  log_alpha in the A slot is first turned into alpha in place.
+__device__ __noinline__ void token_chunk(uint32_t tb, float* A, const uint8_t* qk, const uint8_t* vv,
+                            const float* beta, __nv_bfloat16* out, int64_t t0, int H, int h, int L) {
+    const int j = lt();
+    for (int r = 0; r < L; ++r) A[r * D + j] = expf(A[r * D + j]);
+    group_sync(kBarB);
+    float s[D];
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[32 * cb + i] = __uint_as_float(u[i]);
+    }
+    for (int r = 0; r < L; ++r) {
+        const float* al = A + r * D;
+        float rk = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; ++c) {
+            s[c] *= al[c];
+            rk = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), rk);
+        }
+        const float vj = bf2f(*reinterpret_cast<const __nv_bfloat16*>(vv + half_off(r, j)));
+        const float d = beta[r] * (vj - rk);
+        float y = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; ++c) {
+            s[c] = fmaf(bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), d, s[c]);
+            y = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(true, r, c))), y);
+        }
+        out[((t0 + r) * H + h) * D + j] = __float2bfloat16_rn(y);
+    }
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+        uint32_t u[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(s[32 * cb + i]);
+        tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+    }
+    tmem_wait_st();
+}
+
+// ---- MMA groups (each issued by one thread) --------------------------------------
 // AP = [Khat; Qhat] x Kb^T : M = 128, N = 64, K = 128 (both K-major).
 __device__ __forceinline__ void mma_gram(uint32_t tb, uint32_t sQK, uint32_t sKB) {
     constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
@@ -246,14 +584,14 @@ __device__ __forceinline__ void mma_gram(uint32_t tb, uint32_t sQK, uint32_t sKB
     }
 }
 
-// W'^T = Khat^T T^T -> AP columns; U^T = V^T T^T -> U columns.  M = 128, N = 64,
+// W'^T = Khat^T T^T -> W columns; U^T = V^T T^T -> U columns.  M = 128, N = 64,
 // K = 64 tokens; A operands MN-major (channel halves LBO apart), B = T K-major.
 __device__ __forceinline__ void mma_wu(uint32_t tb, uint32_t sQK, uint32_t sV, uint32_t sTT) {
     constexpr uint32_t id = idesc_bf16_f32(128, 64, true, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 4; ++ks) {
         const uint64_t b = smem_desc(sTT + ks * 32, 16, 1024, kSwizzle128B);
-        mma_ss(tb + kTmAP, smem_desc(sQK + ks * 2048, 16384, 1024, kSwizzle128B), b, id, ks > 0);
+        mma_ss(tb + kTmW, smem_desc(sQK + ks * 2048, 16384, 1024, kSwizzle128B), b, id, ks > 0);
         mma_ss(tb + kTmU, smem_desc(sV + ks * 2048, 8192, 1024, kSwizzle128B), b, id, ks > 0);
     }
 }
@@ -287,284 +625,223 @@ __device__ __forceinline__ void mma_state_out(uint32_t tb, uint32_t sKB, uint32_
         mma_ts(tb + kTmO, tb + kTmDbf + ks * 8, smem_desc(sPP + ks * 32, 16, 1024, kSwizzle128B), idp, 1);
 }
 
-// ---- TMEM readouts (thread = TMEM lane) --------------------------------------
-__device__ __forceinline__ void ld64(uint32_t tb, uint32_t col, uint32_t (&v)[64]) {
-    const uint32_t lane0 = (threadIdx.x >> 5) * 32;
-    uint32_t* lo = v;
-    tmem_ld32(tmem_addr(tb, lane0, col), *reinterpret_cast<uint32_t(*)[32]>(lo));
-    tmem_ld32(tmem_addr(tb, lane0, col + 32), *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
-    tmem_wait_ld();
-}
-
-// Lanes 0-63 hold A rows r: N[r][s] = beta_r A_rs (s < r) -> fp32 matrix in the
-// stage's log_alpha slot.  Lanes 64-127 hold P rows r: P_rs (s <= r) -> bf16,
-// K-major operand tile PP.
-__device__ void read_gram(uint32_t tb, uint8_t* stage, uint8_t* sm, const float* beta_s) {
-    uint32_t v[64];
-    ld64(tb, kTmAP, v);
-    const int tid = threadIdx.x;
-    if (tid < 64) {
-        const int r = tid, bi = r >> 4, rr = r & 15;
-        const float b = beta_s[r];
-        float* Nbase = reinterpret_cast<float*>(stage + kA + kSolveN);
-#pragma unroll
-        for (int bj = 0; bj < 4; ++bj) {
-            if (bj > bi) break;
-            float* dst = Nbase + (bi * (bi + 1) / 2 + bj) * (kBlkBytes / 4) + rr * kBlkStride;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int s0 = 16 * bj + 4 * q4;
-                float4 f;
-                f.x = (s0 + 0 < r) ? b * __uint_as_float(v[s0 + 0]) : 0.f;
-                f.y = (s0 + 1 < r) ? b * __uint_as_float(v[s0 + 1]) : 0.f;
-                f.z = (s0 + 2 < r) ? b * __uint_as_float(v[s0 + 2]) : 0.f;
-                f.w = (s0 + 3 < r) ? b * __uint_as_float(v[s0 + 3]) : 0.f;
-                *reinterpret_cast<float4*>(dst + 4 * q4) = f;
-            }
-        }
-    } else {
-        const int r = tid - 64;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = 8 * ch + 2 * u;
-                const float lo = (s <= r) ? __uint_as_float(v[s]) : 0.f;
-                const float hi = (s + 1 <= r) ? __uint_as_float(v[s + 1]) : 0.f;
-                w[u] = pack_bf16x2(lo, hi);
-            }
-            *reinterpret_cast<uint4*>(sm + kPP + sw128_offset(r, 16 * ch)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-        }
-    }
-}
-
-__device__ __forceinline__ float* blk(float* base, int i, int j) {
-    return base + (i * (i + 1) / 2 + j) * (kBlkBytes / 4);
-}
-
-// One warp computes rows [rb, rb + NR) of C = sign * sum_p A_p B_p for 16x16
-// blocks (NP pairs); each lane owns NR/2 consecutive columns of one row.
-template <int NR, int NP>
-__device__ __forceinline__ void blk_product(float* Cb, float* const (&Ab)[NP], float* const (&Bb)[NP],
-                                            int rb, float sign) {
-    constexpr int NC = NR / 2;                  // columns per lane
-    constexpr int LPR = 16 / NC;                // lanes per row
-    const int lane = threadIdx.x & 31;
-    const int rr = rb + lane / LPR, c0 = (lane % LPR) * NC;
-    float acc[NC];
-#pragma unroll
-    for (int u = 0; u < NC; ++u) acc[u] = 0.f;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        float arow[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(Ab[p] + rr * kBlkStride + 4 * k4);
-            arow[4 * k4] = a4.x; arow[4 * k4 + 1] = a4.y; arow[4 * k4 + 2] = a4.z; arow[4 * k4 + 3] = a4.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float* brow = Bb[p] + k * kBlkStride + c0;
-#pragma unroll
-            for (int u = 0; u < NC; u += 2) {
-                const float2 b2 = *reinterpret_cast<const float2*>(brow + u);
-                acc[u] = fmaf(arow[k], b2.x, acc[u]);
-                acc[u + 1] = fmaf(arow[k], b2.y, acc[u + 1]);
-            }
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < NC; u += 2)
-        *reinterpret_cast<float2*>(Cb + rr * kBlkStride + c0 + u) = make_float2(sign * acc[u], sign * acc[u + 1]);
-}
-
-// T = (I + N)^{-1} Diag(beta), N strictly lower (64 x 64), by 16x16 blocks:
-// the four diagonal blocks D_i = (I + N_ii)^{-1} by forward substitution, then
-// X_ij = -D_i sum_{k=j}^{i-1} N_ik X_kj one block sub-diagonal at a time.
-// All 128 threads take part; fp32 throughout.  T goes to the bf16 K-major
-// operand tile TT (row r = token, column s).
-__device__ void solve_T(uint8_t* stage, uint8_t* sm, const float* beta_s) {
-    float* Nb = reinterpret_cast<float*>(stage + kA + kSolveN);
-    float* Xb = reinterpret_cast<float*>(stage + kA + kSolveX);
-    float* Yb = reinterpret_cast<float*>(stage + kA + kSolveY);
-    const int tid = threadIdx.x, w = tid >> 5;
-    if (tid < 64) {                                  // diagonal blocks
-        const int i = tid >> 4, jl = tid & 15;
-        const float* Nii = blk(Nb, i, i);
-        float x[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == jl) ? 1.f : 0.f;
-#pragma unroll
-            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[r * kBlkStride + q], x[q], acc);
-            x[r] = acc;
-        }
-        float* Xii = blk(Xb, i, i);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
-    }
-    __syncthreads();
-    // first sub-diagonal: Y_i = N_{i+1,i} D_i, X_{i+1,i} = -D_{i+1} Y_i
-    if (w < 3) {
-        float* const A1[1] = {blk(Nb, w + 1, w)};
-        float* const B1[1] = {blk(Xb, w, w)};
-        blk_product<16, 1>(Yb + w * (kBlkBytes / 4), A1, B1, 0, 1.f);
-    }
-    __syncthreads();
-    if (w < 3) {
-        float* const A1[1] = {blk(Xb, w + 1, w + 1)};
-        float* const B1[1] = {Yb + w * (kBlkBytes / 4)};
-        blk_product<16, 1>(blk(Xb, w + 1, w), A1, B1, 0, -1.f);
-    }
-    __syncthreads();
-    // second sub-diagonal: Z_i = N_{i+2,i} D_i + N_{i+2,i+1} X_{i+1,i}; X_{i+2,i} = -D_{i+2} Z_i
-    {
-        const int i = w >> 1, rb = (w & 1) * 8;
-        float* const A2[2] = {blk(Nb, i + 2, i), blk(Nb, i + 2, i + 1)};
-        float* const B2[2] = {blk(Xb, i, i), blk(Xb, i + 1, i)};
-        blk_product<8, 2>(Yb + i * (kBlkBytes / 4), A2, B2, rb, 1.f);
-    }
-    __syncthreads();
-    {
-        const int i = w >> 1, rb = (w & 1) * 8;
-        float* const A1[1] = {blk(Xb, i + 2, i + 2)};
-        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
-        blk_product<8, 1>(blk(Xb, i + 2, i), A1, B1, rb, -1.f);
-    }
-    __syncthreads();
-    // third sub-diagonal: Z = N_30 D_0 + N_31 X_10 + N_32 X_20; X_30 = -D_3 Z
-    {
-        float* const A3[3] = {blk(Nb, 3, 0), blk(Nb, 3, 1), blk(Nb, 3, 2)};
-        float* const B3[3] = {blk(Xb, 0, 0), blk(Xb, 1, 0), blk(Xb, 2, 0)};
-        blk_product<4, 3>(Yb, A3, B3, 4 * w, 1.f);
-    }
-    __syncthreads();
-    {
-        float* const A1[1] = {blk(Xb, 3, 3)};
-        float* const B1[1] = {Yb};
-        blk_product<4, 1>(blk(Xb, 3, 0), A1, B1, 4 * w, -1.f);
-    }
-    __syncthreads();
-    // T[r][s] = X[r][s] beta_s, bf16, row r: thread (r, half) writes 32 columns
-    {
-        const int r = tid >> 1, hf = tid & 1, bi = r >> 4, rr = r & 15;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            const int s0 = 32 * hf + 8 * ch, bj = s0 >> 4;
-            uint32_t wv[4];
-            if (bj <= bi) {
-                const float* xr = blk(Xb, bi, bj) + rr * kBlkStride + (s0 & 15);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    wv[u] = pack_bf16x2(xr[2 * u] * beta_s[s0 + 2 * u], xr[2 * u + 1] * beta_s[s0 + 2 * u + 1]);
-            } else {
-                wv[0] = wv[1] = wv[2] = wv[3] = 0u;
-            }
-            *reinterpret_cast<uint4*>(sm + kTT + sw128_offset(r, 16 * (4 * hf + ch))) =
-                make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-    }
-}
-
-// Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
-__device__ void read_w(uint32_t tb, uint8_t* sm) {
-    uint32_t v[64];
-    ld64(tb, kTmAP, v);
-    const int c = threadIdx.x;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            w[u] = pack_bf16x2(-__uint_as_float(v[8 * ch + 2 * u]), -__uint_as_float(v[8 * ch + 2 * u + 1]));
-        *reinterpret_cast<uint4*>(sm + kWT + sw128_offset(c, 16 * ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
-// Lane j holds Delta^T row j (fp32): pack to bf16 in TMEM as an A operand.
-__device__ void pack_delta(uint32_t tb) {
-    uint32_t v[64], pk[32];
-    ld64(tb, kTmU, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-    tmem_st32(tmem_addr(tb, (threadIdx.x >> 5) * 32, kTmDbf), pk);
-    tmem_wait_st();
-}
-
-// Lane j holds O^T row j.  The rows are transposed through a 64 x 256-byte
-// staging tile (the -W'^T slot, dead after the Delta product) and written as
-// 16-byte row segments, rows [r0, r1) only.
-__device__ void store_out(uint32_t tb, uint8_t* sm, __nv_bfloat16* out, int64_t t0, int H, int h,
-                          int r0, int r1) {
-    uint32_t v[64];
-    ld64(tb, kTmO, v);
-    const int tid = threadIdx.x;
-    uint8_t* stg = sm + kWT;
-#pragma unroll
-    for (int r = 0; r < 64; ++r)
-        *reinterpret_cast<__nv_bfloat16*>(stg + r * 256 + tid * 2) = __float2bfloat16_rn(__uint_as_float(v[r]));
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const int id = tid + kThreads * m, row = id >> 4, ch = id & 15;
-        if (row >= r0 && row < r1) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + ch * 16);
-            *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
-        }
-    }
-}
-
-__device__ void load_state(uint32_t tb, const float* h0, size_t base) {
-    const int j = threadIdx.x;
-    const uint32_t lane0 = (threadIdx.x >> 5) * 32;
-#pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            r[i] = h0 ? __float_as_uint(h0[base + (size_t)(32 * cb + i) * D + j]) : 0u;
-        tmem_st32(tmem_addr(tb, lane0, kTmS + 32 * cb), r);
-    }
-    tmem_wait_st();
-}
-
-__device__ void store_state(uint32_t tb, float* hT, size_t base) {
-    const int j = threadIdx.x;
-    const uint32_t lane0 = (threadIdx.x >> 5) * 32;
-#pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tmem_ld32(tmem_addr(tb, lane0, kTmS + 32 * cb), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) hT[base + (size_t)(32 * cb + i) * D + j] = __uint_as_float(r[i]);
-    }
-}
-
 #ifdef KDA_PHASE_TIMING
-// Diagnostic build only: cycles spent per phase by thread 0 of block 0.
+// Diagnostic build only: cycles per phase of block 0, group A in slots 0-7
+// (thread 0), group B in slots 8-15 (thread 128).
 __device__ unsigned long long g_phase_cycles[16];
-#define KDA_PHASE(i)                                                        \
-    do {                                                                    \
-        if (blockIdx.x == 0 && threadIdx.x == 0) {                          \
-            const long long t_ = clock64();                                 \
-            g_phase_cycles[i] += (unsigned long long)(t_ - phase_t_);       \
-            phase_t_ = t_;                                                  \
-        }                                                                   \
+#define KDA_PHASE(i)                                                                  \
+    do {                                                                              \
+        if (blockIdx.x == 0 && lt() == 0) {                                           \
+            const long long t_ = clock64();                                           \
+            g_phase_cycles[i] += (unsigned long long)(t_ - phase_t_);                 \
+            phase_t_ = t_;                                                            \
+        }                                                                             \
     } while (0)
+#define KDA_PHASE_INIT long long phase_t_ = clock64()
 #else
 #define KDA_PHASE(i) do {} while (0)
+#define KDA_PHASE_INIT do {} while (0)
 #endif
 
-// Make this thread's shared-memory and TMEM writes visible to the tensor core,
-// then synchronise the block.
-__device__ __forceinline__ void publish_to_mma() {
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+// ============================ TMA ring refills ===================================
+__device__ __forceinline__ void load_qk(uint8_t* dst, const Maps& m, int h, int t0, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, kQKBytes);
+    tma_load_3d(dst + 0, &m.k, 0, h, t0, bar);
+    tma_load_3d(dst + 8192, &m.q, 0, h, t0, bar);
+    tma_load_3d(dst + 16384, &m.k, 64, h, t0, bar);
+    tma_load_3d(dst + 24576, &m.q, 64, h, t0, bar);
+}
+__device__ __forceinline__ void load_v(uint8_t* dst, const Maps& m, int h, int t0, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, kVBytes);
+    tma_load_3d(dst, &m.v, 0, h, t0, bar);
+    tma_load_3d(dst + 8192, &m.v, 64, h, t0, bar);
+}
+__device__ __forceinline__ void load_a(uint8_t* dst, const Maps& m, int h, int t0, uint64_t* bar) {
+    mbar_arrive_expect_tx(bar, kABytes);
+    tma_load_3d(dst, &m.a, 0, h, t0, bar);
+}
+
+struct Ctx {
+    uint8_t* sm;
+    Small* sw;
+    uint32_t tb;
+    int64_t bos, eos;
+    int nchunks, H, h;
+};
+
+enum { kLdQK = 0, kLdV = 1, kLdA = 2 };
+
+// ============================ group A loop =======================================
+__device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __restrict__ beta) {
+    Small& sw = *x.sw;
+    const int t = lt();
+    uint32_t gram_ph = 0;
+    bool ok = true, gram_pending = false;
+    float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
+    KDA_PHASE_INIT;
+    for (int n = 0; n < x.nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        const int64_t t0 = x.bos + (int64_t)n * C;
+        const int L = (int)((x.eos - t0) < C ? (x.eos - t0) : C);
+        const float braw = braw_next;                    // loaded one chunk ahead
+        if (n + 1 < x.nchunks) {
+            const int64_t tn = t0 + C + t;
+            braw_next = (t < C && tn < x.eos) ? bf2f(beta[tn * x.H + x.h]) : 0.f;
+        }
+        uint8_t* aslot = x.sm + kA0 + s * kABytes;
+        uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
+        uint8_t* kb = x.sm + kKB0 + s * 16384;
+        uint8_t* pp = x.sm + kPP0 + s * 8192;
+
+        if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
+        KDA_PHASE(0);
+        if (t == 0) ++sw.consumed[kLdA][s];
+        KDA_PHASE(1);
+        if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
+        KDA_PHASE(2);
+        if (t < C) sw.beta[s][t] = (t < L) ? braw : 0.f;
+        if (!(ok = group_wait(kBarA, &sw.qk_full[s], ph))) break;
+        KDA_PHASE(3);
+        if (t == 0) ++sw.consumed[kLdQK][s];
+        const bool fast = build_operands(qk, kb, reinterpret_cast<const float*>(aslot), L, sw.gam[s],
+                                         reinterpret_cast<float*>(pp));
+        if (!fast) {                                     // token-by-token chunk
+            group_sync(kBarA);
+            if (t == 0) {
+                sw.mode[s] = 1;
+                mbar_arrive(&sw.ready[s]);
+            }
+            continue;
+        }
+        group_publish(kBarA);
+        KDA_PHASE(4);
+        if (t == 0) {
+            mma_gram(x.tb, smem_u32(qk), smem_u32(kb));
+            mma_commit(&sw.gram_done);
+        }
+        gram_pending = true;
+        if (!(ok = group_wait(kBarA, &sw.gram_done, gram_ph))) break;
+        gram_ph ^= 1u;
+        gram_pending = false;
+        KDA_PHASE(5);
+        tc_fence_after();
+        read_gram(x.tb, aslot, pp, sw.beta[s]);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        group_sync(kBarA);
+        KDA_PHASE(6);
+        solve_T(aslot, sw.beta[s]);
+        fence_proxy_async_smem();
+        group_sync(kBarA);
+        KDA_PHASE(7);
+        if (t == 0) {
+            sw.mode[s] = 0;
+            mbar_arrive(&sw.ready[s]);
+        }
+    }
+    if (gram_pending) mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);   // let it land
+    return ok;
+}
+
+// ============================ group B loop =======================================
+__device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bfloat16* __restrict__ out,
+                            const float* __restrict__ h0, float* __restrict__ hT, size_t sbase) {
+    Small& sw = *x.sw;
+    const int t = lt();
+    const bool leader = (t == 0);
+    uint32_t wu_ph = 0, m1_ph = 0, m2_ph = 0;
+    bool mma_pending = false;
+    uint64_t* pending_bar = nullptr;
+    uint32_t pending_ph = 0;
+    auto issue_chunk = [&](int c, int s, bool a, bool v, bool q) {
+        const int tc = (int)(x.bos + (int64_t)c * C);
+        if (a) { load_a(x.sm + kA0 + s * kABytes, maps, x.h, tc, &sw.a_full[s]); ++sw.issued[kLdA][s]; }
+        if (v) { load_v(x.sm + kV0 + s * kVBytes, maps, x.h, tc, &sw.v_full[s]); ++sw.issued[kLdV][s]; }
+        if (q) { load_qk(x.sm + kQK0 + s * kQKBytes, maps, x.h, tc, &sw.qk_full[s]); ++sw.issued[kLdQK][s]; }
+    };
+    if (leader)
+        for (int c = 0; c < 2 && c < x.nchunks; ++c) issue_chunk(c, c, true, true, true);
+    load_state(x.tb, h0, sbase);
+    const uint32_t sWT = smem_u32(x.sm + kWT);
+    bool ok = true;
+    KDA_PHASE_INIT;
+    for (int n = 0; n < x.nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        const int64_t t0 = x.bos + (int64_t)n * C;
+        const int L = (int)((x.eos - t0) < C ? (x.eos - t0) : C);
+        const bool refill = (n + 2 < x.nchunks);
+        uint8_t* aslot = x.sm + kA0 + s * kABytes;
+        uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
+        uint8_t* vs = x.sm + kV0 + s * kVBytes;
+        const uint32_t sQK = smem_u32(qk), sV = smem_u32(vs), sA = smem_u32(aslot),
+                       sKB = smem_u32(x.sm + kKB0 + s * 16384), sPP = smem_u32(x.sm + kPP0 + s * 8192);
+
+        if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
+        if (!(ok = group_wait(kBarB, &sw.v_full[s], ph))) break;
+        if (leader) ++sw.consumed[kLdV][s];
+        KDA_PHASE(8);
+        tc_fence_after();
+        if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
+            token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], out, t0, x.H, x.h, L);
+            tc_fence_before();
+            group_sync(kBarB);
+            if (leader) {
+                if (refill) issue_chunk(n + 2, s, true, true, true);
+                mbar_arrive(&sw.kbp_free[s]);
+            }
+            continue;
+        }
+        if (leader) {
+            mma_wu(x.tb, sQK, sV, sA + kTT);
+            mma_commit(&sw.wu_done);
+        }
+        mma_pending = true; pending_bar = &sw.wu_done; pending_ph = wu_ph;
+        decay_state(x.tb, sw.gam[s]);
+        KDA_PHASE(9);
+        if (!(ok = group_wait(kBarB, &sw.wu_done, wu_ph))) break;
+        wu_ph ^= 1u; mma_pending = false;
+        tc_fence_after();
+        if (leader && refill) issue_chunk(n + 2, s, true, true, false);
+        read_w(x.tb, x.sm + kWT);
+        group_publish(kBarB);
+        KDA_PHASE(10);
+        if (leader) {
+            mma_delta_out(x.tb, sWT, sQK);
+            mma_commit(&sw.mma1_done);
+        }
+        mma_pending = true; pending_bar = &sw.mma1_done; pending_ph = m1_ph;
+        if (!(ok = group_wait(kBarB, &sw.mma1_done, m1_ph))) break;
+        m1_ph ^= 1u; mma_pending = false;
+        KDA_PHASE(11);
+        tc_fence_after();
+        if (leader && refill) issue_chunk(n + 2, s, false, false, true);
+        pack_delta(x.tb);
+        group_publish(kBarB);
+        KDA_PHASE(12);
+        if (leader) {
+            mma_state_out(x.tb, sKB, sPP);
+            mma_commit(&sw.mma2_done);
+            mma_commit(&sw.kbp_free[s]);
+        }
+        mma_pending = true; pending_bar = &sw.mma2_done; pending_ph = m2_ph;
+        if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
+        m2_ph ^= 1u; mma_pending = false;
+        KDA_PHASE(13);
+        tc_fence_after();
+        store_out(x.tb, x.sm + kWT, out, t0, x.H, x.h, L);
+        tc_fence_before();
+        group_sync(kBarB);
+        tc_fence_after();
+        KDA_PHASE(14);
+    }
+    if (ok) {
+        if (hT) store_state(x.tb, hT, sbase);
+    } else if (mma_pending) {
+        mbar_wait_bounded(pending_bar, pending_ph, kWaitLimitNs);
+    }
+    return ok;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -575,181 +852,65 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t full_bar[2], mma_bar, reload_bar;
-    __shared__ uint32_t tmem_base;
-    __shared__ float beta_s[C], gam[D];
-
+    Small* sw = reinterpret_cast<Small*>(sm + kSmall);
     const int tid = threadIdx.x;
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
-    int64_t bos, eos;
-    seq_bounds(cu, n, num_seqs, T, bos, eos);
-    const int nchunks = (int)((eos - bos + C - 1) / C);
-    const size_t sbase = ((size_t)n * H + h) * D * D;
+    Ctx x;
+    x.sm = sm;
+    x.sw = sw;
+    x.H = H;
+    x.h = blockIdx.x % H;
+    const int n = blockIdx.x / H;
+    seq_bounds(cu, n, num_seqs, T, x.bos, x.eos);
+    x.nchunks = (int)((x.eos - x.bos + C - 1) / C);
+    const size_t sbase = ((size_t)n * H + x.h) * D * D;
 
     if (tid == 0) {
-        mbar_init(&full_bar[0], 1);
-        mbar_init(&full_bar[1], 1);
-        mbar_init(&mma_bar, 1);
-        mbar_init(&reload_bar, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sw->qk_full[s], 1);
+            mbar_init(&sw->v_full[s], 1);
+            mbar_init(&sw->a_full[s], 1);
+            mbar_init(&sw->ready[s], 1);
+            mbar_init(&sw->kbp_free[s], 1);
+        }
+        mbar_init(&sw->gram_done, 1);
+        mbar_init(&sw->wu_done, 1);
+        mbar_init(&sw->mma1_done, 1);
+        mbar_init(&sw->mma2_done, 1);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
         tma_prefetch_desc(&maps.a);
+        for (int k = 0; k < 3; ++k)
+            for (int s = 0; s < 2; ++s) sw->issued[k][s] = sw->consumed[k][s] = 0;
     }
     if ((tid >> 5) == 0) {
-        tmem_alloc(&tmem_base, kTmCols);
+        tmem_alloc(&sw->tmem_base, kTmCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tb = tmem_base;
+    x.tb = sw->tmem_base;
 
-    bool pending[2] = {false, false};
-    if (tid == 0) {
-        for (int c = 0; c < 2 && c < nchunks; ++c)
-            issue_tile_loads(sm + c * kStageBytes, maps, h, (int)(bos + (int64_t)c * C), &full_bar[c], true);
-    }
-    for (int c = 0; c < 2 && c < nchunks; ++c) pending[c] = true;
-    load_state(tb, h0, sbase);
+    const bool ok = in_group_a() ? run_group_a(x, beta) : run_group_b(x, maps, out, h0, hT, sbase);
+    if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
 
-    uint32_t full_ph[2] = {0u, 0u}, mma_ph = 0u, reload_ph = 0u;
-    bool mma_pending = false, reload_pending = false;
-    const uint32_t sQKbase = smem_u32(sm);
-    const uint32_t sKB = smem_u32(sm + kKB), sTT = smem_u32(sm + kTT), sPP = smem_u32(sm + kPP),
-                   sWT = smem_u32(sm + kWT);
-    bool ok = true;
-#ifdef KDA_PHASE_TIMING
-    long long phase_t_ = clock64();
-#endif
-
-    float braw_next = (tid < C && bos + tid < eos) ? bf2f(beta[(bos + tid) * H + h]) : 0.f;
-    for (int c = 0; c < nchunks && ok; ++c) {
-        const int st = c & 1;
-        uint8_t* stage = sm + st * kStageBytes;
-        const uint32_t sQK = sQKbase + st * kStageBytes + kQK, sV = sQKbase + st * kStageBytes + kV;
-        const int64_t t0 = bos + (int64_t)c * C;
-        const int L = (int)((eos - t0) < C ? (eos - t0) : C);
-        const float braw = braw_next;                 // beta of this chunk, loaded one chunk ahead
-        if (c + 1 < nchunks) {
-            const int64_t tn = t0 + C + tid;
-            braw_next = (tid < C && tn < eos) ? bf2f(beta[tn * H + h]) : 0.f;
-        }
-
-        ok = wait_all(&full_bar[st], full_ph[st]);
-        KDA_PHASE(0);
-        if (!ok) break;
-        full_ph[st] ^= 1u;
-        pending[st] = false;
-
-        for (int r0 = 0; r0 < L && ok;) {
-            if (r0 > 0) {   // split chunk: restore the raw q, k, log_alpha tiles
-                if (tid == 0) issue_tile_loads(stage, maps, h, (int)t0, &reload_bar, false);
-                reload_pending = true;
-                ok = wait_all(&reload_bar, reload_ph);
-                if (!ok) break;
-                reload_ph ^= 1u;
-                reload_pending = false;
-            }
-            const int r1 = next_run(reinterpret_cast<const float*>(stage + kA), r0, L);
-            KDA_PHASE(1);
-            if (tid < C) beta_s[tid] = (tid >= r0 && tid < r1) ? braw : 0.f;
-            build_operands(sm, st * kStageBytes, r0, r1, gam);
-            __syncthreads();
-            KDA_PHASE(2);
-            decay_state(tb, gam);
-            publish_to_mma();
-            KDA_PHASE(3);
-
-            if (tid == 0) {
-                mma_gram(tb, sQK, sKB);
-                mma_commit(&mma_bar);
-            }
-            mma_pending = true;
-            if (!(ok = wait_all(&mma_bar, mma_ph))) break;
-            mma_ph ^= 1u;
-            mma_pending = false;
-            tc_fence_after();
-            KDA_PHASE(4);
-            read_gram(tb, stage, sm, beta_s);
-            fence_proxy_async_smem();
-            __syncthreads();
-            KDA_PHASE(5);
-            solve_T(stage, sm, beta_s);
-            publish_to_mma();
-            KDA_PHASE(6);
-
-            if (tid == 0) {
-                mma_wu(tb, sQK, sV, sTT);
-                mma_commit(&mma_bar);
-            }
-            mma_pending = true;
-            if (!(ok = wait_all(&mma_bar, mma_ph))) break;
-            mma_ph ^= 1u;
-            mma_pending = false;
-            tc_fence_after();
-            KDA_PHASE(7);
-            read_w(tb, sm);
-            publish_to_mma();
-            KDA_PHASE(8);
-
-            if (tid == 0) {
-                mma_delta_out(tb, sWT, sQK);
-                mma_commit(&mma_bar);
-            }
-            mma_pending = true;
-            if (!(ok = wait_all(&mma_bar, mma_ph))) break;
-            mma_ph ^= 1u;
-            mma_pending = false;
-            tc_fence_after();
-            KDA_PHASE(9);
-            pack_delta(tb);
-            publish_to_mma();
-            KDA_PHASE(10);
-
-            if (tid == 0) {
-                mma_state_out(tb, sKB, sPP);
-                mma_commit(&mma_bar);
-            }
-            mma_pending = true;
-            if (!(ok = wait_all(&mma_bar, mma_ph))) break;
-            mma_ph ^= 1u;
-            mma_pending = false;
-            tc_fence_after();
-            KDA_PHASE(11);
-            store_out(tb, sm, out, t0, H, h, r0, r1);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            KDA_PHASE(12);
-            r0 = r1;
-        }
-        if (ok && c + 2 < nchunks) {
-            if (tid == 0)
-                issue_tile_loads(stage, maps, h, (int)(t0 + 2 * C), &full_bar[st], true);
-            pending[st] = true;
-        }
-    }
-
-    if (ok) {
-        if (hT) store_state(tb, hT, sbase);
-    } else {
-        if (tid == 0) atomicOr(status, kStatusTimeout);
-        // let in-flight copies land before the block exits (bounded)
-        for (int s = 0; s < 2; ++s)
-            if (pending[s]) mbar_wait_bounded(&full_bar[s], full_ph[s], kWaitLimitNs);
-        if (mma_pending) mbar_wait_bounded(&mma_bar, mma_ph, kWaitLimitNs);
-        if (reload_pending) mbar_wait_bounded(&reload_bar, reload_ph, kWaitLimitNs);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if ((tid >> 5) == 0) tmem_dealloc(tb, kTmCols);
+    if (tid == 0) {   // let any copy still in flight land before the block exits (bounded)
+        uint64_t* bars[3] = {sw->qk_full, sw->v_full, sw->a_full};
+        for (int k = 0; k < 3; ++k)
+            for (int s = 0; s < 2; ++s)
+                if (sw->issued[k][s] > sw->consumed[k][s])
+                    mbar_wait_bounded(&bars[k][s], (uint32_t)(sw->consumed[k][s] & 1), kWaitLimitNs);
+    }
+    __syncthreads();
+    if ((tid >> 5) == 0) tmem_dealloc(x.tb, kTmCols);
 }
 
-// ---- host side ------------------------------------------------------------------
+// ============================ host side ==========================================
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
