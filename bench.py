@@ -138,27 +138,34 @@ def stored_traffic(kernel_digest):
 
 
 def oracle_sample(budget_s, threads=0):
-    """Time the fp64 oracle on a bounded sample of the prefill workload (one
-    8192-token sequence, as many heads as fit the time budget)."""
+    """Time the fp64 oracle on a bounded sample of the prefill workload: as many of
+    its B sequences (all H heads each) as fit the time budget on the host cores."""
     import numpy as np
     from linear_attention_06_gb300 import workloads
     from oracle import kda_oracle
     cores = os.cpu_count() or 1
     used = kda_oracle.max_threads() if threads == 0 else threads
-    w = workloads.make_inputs(T, H, D, D, seed=1, num_seqs=1)       # same recipe, one sequence
-    arr = [np.ascontiguousarray(x.float().numpy().astype(np.float64))
-           for x in (w.q, w.k, w.v, w.log_alpha, w.beta)]
 
-    def run(heads):
-        sl = [a[:, :heads].copy() for a in arr]
+    def inputs(nseq):
+        w = workloads.make_inputs(nseq * T, H, D, D, seed=1, num_seqs=nseq)   # same recipe
+        return [np.ascontiguousarray(x.float().numpy().astype(np.float64))
+                for x in (w.q, w.k, w.v, w.log_alpha, w.beta)]
+
+    one = inputs(1)
+    t0 = time.perf_counter()
+    kda_oracle.prefill(*[a[:, :1].copy() for a in one], None, cu_seqlens=[0, T], num_threads=1)
+    t1 = time.perf_counter() - t0                  # one (sequence, head) pair on one thread
+    pairs = budget_s / max(t1, 1e-6) * max(1, min(used, B * H))
+    nseq = int(max(1, min(B, pairs // H)))
+    arr = one if nseq == 1 else inputs(nseq)
+    cu = [i * T for i in range(nseq + 1)]
+
+    def run():
         t0 = time.perf_counter()
-        kda_oracle.prefill(*sl, None, cu_seqlens=[0, T], num_threads=used)
+        kda_oracle.prefill(*arr, None, cu_seqlens=cu, num_threads=used)
         return time.perf_counter() - t0
 
-    t1 = run(1)                                    # one (sequence, head) pair = one thread's work
-    per_thread = max(1, int(budget_s / max(t1, 1e-6)))
-    heads = max(1, min(H, per_thread * max(1, used)))
-    return run, heads, cores, used
+    return run, nseq, cores, used
 
 
 class Ranks:
@@ -197,12 +204,12 @@ def run_reference(args):
     if rank != 0:
         return
     budget = max(1.0, args.ref_step_budget)
-    run, heads, cores, used = oracle_sample(budget)
+    run, nseq, cores, used = oracle_sample(budget)
     for _ in range(args.warmup):
-        run(heads)
-    t = sum(run(heads) for _ in range(args.steps)) / args.steps
-    value = heads * T / t / H                      # token-heads/s over H heads = tokens/s
-    sample = f"fp64 oracle, 1 sequence x {heads} of {H} heads x {T} tokens per step"
+        run()
+    t = sum(run() for _ in range(args.steps)) / args.steps
+    value = nseq * T / t                           # tokens (all H heads each) per second
+    sample = f"fp64 oracle, {nseq} of {B} sequences x {H} heads x {T} tokens per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -338,11 +345,11 @@ def run_ours(args):
         "e2e": e2e, "gpu_launches": prefill_launches, "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        run, heads, cores, used = oracle_sample(args.cpu_budget)
-        t = run(heads)
-        line["cpu_baseline"] = {"value": heads * T / t / H, "unit": UNIT, "cores": used,
+        run, nseq, cores, used = oracle_sample(args.cpu_budget)
+        t = run()
+        line["cpu_baseline"] = {"value": nseq * T / t, "unit": UNIT, "cores": used,
                                 "kind": "oracle",
-                                "sample": f"fp64 oracle on 1 sequence x {heads} of {H} heads x {T} tokens "
+                                "sample": f"fp64 oracle on {nseq} of {B} sequences x {H} heads x {T} tokens "
                                           f"({t:.1f} s, {cores} host cores)"}
     print(json.dumps(line), flush=True)
     ranks.close()

@@ -90,8 +90,10 @@ constexpr uint32_t kTT = 24576;                                        // T, 64 
 constexpr uint32_t kQKBytes = 32768, kVBytes = 16384, kABytes = 32768;
 
 // ---- TMEM columns
-constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmDbf = 128, kTmO = 192, kTmU = 256, kTmAP = 384,
-                   kTmW = 448;
+constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmDbf = 128, kTmO = 192;
+// two slots (chunk parity) each for U / Delta and for the Gram result, which W' later overwrites
+__device__ __forceinline__ uint32_t tm_u(int s) { return 256u + 64u * s; }
+__device__ __forceinline__ uint32_t tm_apw(int s) { return 384u + 64u * s; }
 constexpr uint32_t kTmCols = 512;
 
 struct Maps {
@@ -101,9 +103,9 @@ struct Maps {
 // Barriers and small per-slot data in the kSmall area.
 struct Small {
     uint64_t qk_full[2], v_full[2], a_full[2];   // TMA completions
-    uint64_t ready[2];                           // group A -> B: chunk prepared
+    uint64_t ready[2];                           // group A -> B: chunk prepared and W', U computed (2 arrivals)
     uint64_t kbp_free[2];                        // group B -> A: Kb / P / beta / gamma slot free
-    uint64_t gram_done, wu_done, mma1_done, mma2_done;
+    uint64_t gram_done, mma1_done, mma2_done;
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
     int pad[5];
@@ -186,15 +188,11 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
 
 // ============================ group A: chunk-local stage =========================
 
-// Khat, Qhat (in place over k, q) and Kb for the rows [0, L); other rows are
-// zeroed; gam[c] = e^{G_c}.  Thread (c, half) of group A handles key channel c
-// and rows [32 half, 32 half + 32): it pulls its 32 log-decays into registers,
-// forms suffix sums, adds the later half's total (exchanged through `xchg`),
-// and only then runs the exponentials and tile stores, which carry no loop
-// dependency.  Returns false, having written nothing, when some channel's decay
-// total over the chunk leaves +-kMaxExponent (the chunk then runs token by
-// token).
-__device__ bool build_operands(uint8_t* qk, uint8_t* kb, const float* A, int L, float* gam, float* xchg) {
+// Pass 1 (thread = key channel c and row half): suffix sums of log_alpha, written back in place
+// over the A slot as e[r][c] = sum_{r<t<L} a[t][c]; returns false when a channel's chunk total
+// leaves +-kMaxExponent.  gam[c] = e^{G_c}.  Pass 2 (thread = 16-byte chunk of 8 channels of one
+// row): Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector accesses.
+__device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float* gam, float* xchg) {
     const int a = lt(), c = a & 127, hf = a >> 7;
     float e[32];
 #pragma unroll
@@ -202,7 +200,7 @@ __device__ bool build_operands(uint8_t* qk, uint8_t* kb, const float* A, int L, 
         const int r = 32 * hf + i;
         e[i] = (r < L) ? A[r * D + c] : 0.f;
     }
-    float run = 0.f;   // sum of log_alpha over this half's rows after row r
+    float run = 0.f;
 #pragma unroll
     for (int i = 31; i >= 0; --i) {
         const float ar = e[i];
@@ -211,32 +209,48 @@ __device__ bool build_operands(uint8_t* qk, uint8_t* kb, const float* A, int L, 
     }
     if (hf == 1) xchg[c] = run;
     group_sync(kBarA);
-    const float off = (hf == 0) ? xchg[c] : 0.f;   // decay of the rows after this half
+    const float off = (hf == 0) ? xchg[c] : 0.f;
     const float total = run + off;
     if (group_or(kBarA, hf == 0 && !(fabsf(total) <= kMaxExponent))) return false;
     if (hf == 0) gam[c] = __expf(total);
-    const __nv_bfloat16 zero = __float2bfloat16_rn(0.f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = 32 * hf + i;
-        __nv_bfloat16* kp = reinterpret_cast<__nv_bfloat16*>(qk + qk_off(false, r, c));
-        __nv_bfloat16* qp = reinterpret_cast<__nv_bfloat16*>(qk + qk_off(true, r, c));
-        __nv_bfloat16* bp = reinterpret_cast<__nv_bfloat16*>(kb + half_off(r, c));
+    for (int i = 0; i < 32; ++i) A[(32 * hf + i) * D + c] = e[i] + off;
+    group_sync(kBarA);
+    // pass 2: 64 rows x 16 chunks = 1024 units, 4 per thread
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int u = a + 256 * m, r = u >> 4, j = u & 15;
+        const uint32_t ko = qk_off(false, r, 8 * j), qo = qk_off(true, r, 8 * j), bo = half_off(r, 8 * j);
+        uint4 kh = make_uint4(0u, 0u, 0u, 0u), qh = kh, kbv = kh;
         if (r < L) {
-            const float ee = e[i] + off;
-            const float kv = bf2f(*kp), qv = bf2f(*qp);
-            const float up = __expf(-ee), dn = __expf(ee);
-            *kp = __float2bfloat16_rn(kv * up);
-            *qp = __float2bfloat16_rn(qv * up);
-            *bp = __float2bfloat16_rn(kv * dn);
-        } else {
-            *kp = zero;
-            *qp = zero;
-            *bp = zero;
+            const uint4 kr = *reinterpret_cast<const uint4*>(qk + ko);
+            const uint4 qr = *reinterpret_cast<const uint4*>(qk + qo);
+            const float4 e0 = *reinterpret_cast<const float4*>(A + r * D + 8 * j);
+            const float4 e1 = *reinterpret_cast<const float4*>(A + r * D + 8 * j + 4);
+            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qw[4] = {qr.x, qr.y, qr.z, qr.w};
+            uint32_t o1[4], o2[4], o3[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float k0 = __uint_as_float(kw[p] << 16), k1 = __uint_as_float(kw[p] & 0xffff0000u);
+                const float q0 = __uint_as_float(qw[p] << 16), q1 = __uint_as_float(qw[p] & 0xffff0000u);
+                const float u0 = __expf(-ev[2 * p]), u1 = __expf(-ev[2 * p + 1]);
+                const float d0 = __expf(ev[2 * p]), d1 = __expf(ev[2 * p + 1]);
+                o1[p] = pack_bf16x2(k0 * u0, k1 * u1);
+                o2[p] = pack_bf16x2(q0 * u0, q1 * u1);
+                o3[p] = pack_bf16x2(k0 * d0, k1 * d1);
+            }
+            kh = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            qh = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+            kbv = make_uint4(o3[0], o3[1], o3[2], o3[3]);
         }
+        *reinterpret_cast<uint4*>(qk + ko) = kh;
+        *reinterpret_cast<uint4*>(qk + qo) = qh;
+        *reinterpret_cast<uint4*>(kb + bo) = kbv;
     }
     return true;
 }
+
 
 __device__ __forceinline__ float* blk(float* base, int i, int j) {
     return base + (i * (i + 1) / 2 + j) * (kBlkBytes / 4);
@@ -246,11 +260,11 @@ __device__ __forceinline__ float* blk(float* base, int i, int j) {
 // lower-triangular 16x16 blocks in the A slot.  Lanes 64-127 hold P rows r:
 // P_rs (s <= r) as the bf16 K-major operand tile.  Warps 0-3 of group A read
 // columns 0-31, warps 4-7 columns 32-63 of the same lanes.
-__device__ void read_gram(uint32_t tb, uint8_t* aslot, uint8_t* pp, const float* beta) {
+__device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp, const float* beta) {
     const int a = lt(), ch = (a >> 7);               // column half
     const int row = (int)lane0() + (a & 31);
     uint32_t v[32];
-    tmem_ld32(tmem_addr(tb, lane0(), kTmAP + 32 * ch), v);
+    tmem_ld32(tmem_addr(tb, lane0(), col + 32 * ch), v);
     tmem_wait_ld();
     if (row < 64) {
         const int r = row, bi = r >> 4, rr = r & 15;
@@ -290,62 +304,58 @@ __device__ void read_gram(uint32_t tb, uint8_t* aslot, uint8_t* pp, const float*
     }
 }
 
-// One warp computes rows [rb, rb + NR) of C = sign * sum_p A_p B_p for 16x16
-// blocks (NP pairs); each lane owns NR/2 consecutive columns of one row
-// (NR = 2: one column).
-template <int NR, int NP>
-__device__ __forceinline__ void blk_product(float* Cb, float* const (&Ab)[NP], float* const (&Bb)[NP],
-                                            int rb, float sign) {
-    constexpr int NC = NR / 2;                  // columns per lane
-    constexpr int LPR = 16 / NC;                // lanes per row
-    const int lane = threadIdx.x & 31;
-    const int rr = rb + lane / LPR, c0 = (lane % LPR) * NC;
-    float acc[NC];
-#pragma unroll
-    for (int u = 0; u < NC; ++u) acc[u] = 0.f;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        float arow[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(Ab[p] + rr * kBlkStride + 4 * k4);
-            arow[4 * k4] = a4.x; arow[4 * k4 + 1] = a4.y; arow[4 * k4 + 2] = a4.z; arow[4 * k4 + 3] = a4.w;
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float* brow = Bb[p] + k * kBlkStride + c0;
-            if constexpr (NC == 1) {
-                acc[0] = fmaf(arow[k], brow[0], acc[0]);
-            } else {
-#pragma unroll
-                for (int u = 0; u < NC; u += 2) {
-                    const float2 b2 = *reinterpret_cast<const float2*>(brow + u);
-                    acc[u] = fmaf(arow[k], b2.x, acc[u]);
-                    acc[u + 1] = fmaf(arow[k], b2.y, acc[u + 1]);
-                }
-            }
-        }
-    }
-    if constexpr (NC == 1) {
-        Cb[rr * kBlkStride + c0] = sign * acc[0];
-    } else {
-#pragma unroll
-        for (int u = 0; u < NC; u += 2)
-            *reinterpret_cast<float2*>(Cb + rr * kBlkStride + c0 + u) = make_float2(sign * acc[u], sign * acc[u + 1]);
-    }
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 
-// T = (I + N)^{-1} Diag(beta), N strictly lower (64 x 64), by 16x16 blocks:
-// the four diagonal blocks D_i = (I + N_ii)^{-1} by forward substitution, then
-// X_ij = -D_i sum_{k=j}^{i-1} N_ik X_kj one block sub-diagonal at a time, all
-// in fp32 on group A's 8 warps.  T is written as the bf16 K-major operand tile
-// (row r = token, column s) inside the A slot.
+// d += a(16x8, row-major fragment) * b(8x8, column fragment), TF32 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// One warp: columns [8 nt, 8 nt + 8) of C = sign * sum_p A_p B_p for 16x16 blocks (row stride
+// kBlkStride floats).
+template <int NP>
+__device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP], const float* const (&Bb)[NP],
+                                        int nt, float sign) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const float* A = Ab[p] + 8 * ks;
+            const float* B = Bb[p] + (8 * ks) * kBlkStride + 8 * nt;
+            const uint32_t af[4] = {to_tf32(A[g * kBlkStride + t]), to_tf32(A[(g + 8) * kBlkStride + t]),
+                                    to_tf32(A[g * kBlkStride + t + 4]), to_tf32(A[(g + 8) * kBlkStride + t + 4])};
+            const uint32_t bf[2] = {to_tf32(B[t * kBlkStride + g]), to_tf32(B[(t + 4) * kBlkStride + g])};
+            mma_tf32(d, af, bf);
+        }
+    }
+    float* C = Cb + 8 * nt;
+    C[g * kBlkStride + 2 * t] = sign * d[0];
+    C[g * kBlkStride + 2 * t + 1] = sign * d[1];
+    C[(g + 8) * kBlkStride + 2 * t] = sign * d[2];
+    C[(g + 8) * kBlkStride + 2 * t + 1] = sign * d[3];
+}
+
+// T = (I + N)^{-1} Diag(beta) with N strictly lower 64x64 (10 lower 16x16 blocks in the A slot):
+// D_i = (I + N_ii)^{-1} by fp32 forward substitution; then the 32x32 halves
+// X_10 = -D_1 N_10 D_0, X_32 = -D_3 N_32 D_2; then the lower-left 32x32 quarter
+// -C^{-1} (B A^{-1}) with A^{-1}, C^{-1} the inverted halves and B = N[32:64, 0:32], using TF32
+// tensor-core block products with fp32 accumulation.  8 warps, 4 group barriers.
 __device__ void solve_T(uint8_t* aslot, const float* beta) {
     float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
     float* Xb = reinterpret_cast<float*>(aslot + kSolveX);
-    float* Yb = reinterpret_cast<float*>(aslot + kSolveY);
+    float* Yb = reinterpret_cast<float*>(aslot + kSolveY);   // 4 blocks
     const int t = lt(), w = t >> 5;
-    if (t < 64) {                                    // diagonal blocks
+    if (t < 64) {
         const int i = t >> 4, jl = t & 15;
         const float* Nii = blk(Nb, i, i);
         float x[16];
@@ -361,44 +371,55 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
         for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
     }
     group_sync(kBarA);
-    if (w < 6) {                                     // Y_i = N_{i+1,i} D_i (rows split in two)
-        const int i = w >> 1, rb = 8 * (w & 1);
-        float* const A1[1] = {blk(Nb, i + 1, i)};
-        float* const B1[1] = {blk(Xb, i, i)};
-        blk_product<8, 1>(Yb + i * (kBlkBytes / 4), A1, B1, rb, 1.f);
+    // halves: warps 0-1 -> X_10 (n-tile w), warps 2-3 -> X_32 (n-tile w-2); Y via the block's own
+    // Y slot, the chain stays inside the warp
+    if (w < 4) {
+        const int hb = w >> 1, nt = w & 1;                   // hb 0: blocks (1,0); hb 1: blocks (3,2)
+        const int i0 = 2 * hb;                               // diagonal index of the upper block
+        float* Ys = Yb + hb * (kBlkBytes / 4);
+        {
+            const float* A1[1] = {blk(Nb, i0 + 1, i0)};
+            const float* B1[1] = {blk(Xb, i0, i0)};
+            blk_mma<1>(Ys, A1, B1, nt, 1.f);
+        }
+        __syncwarp();
+        // the second product needs both column tiles of Y; tile nt only depends on Y tile nt
+        {
+            const float* A1[1] = {blk(Xb, i0 + 1, i0 + 1)};
+            const float* B1[1] = {Ys};
+            blk_mma<1>(blk(Xb, i0 + 1, i0), A1, B1, nt, -1.f);
+        }
     }
     group_sync(kBarA);
-    if (w < 6) {                                     // X_{i+1,i} = -D_{i+1} Y_i
-        const int i = w >> 1, rb = 8 * (w & 1);
-        float* const A1[1] = {blk(Xb, i + 1, i + 1)};
-        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
-        blk_product<8, 1>(blk(Xb, i + 1, i), A1, B1, rb, -1.f);
+    // Y = B A^{-1}: Y_20 = N_20 D_0 + N_21 X_10, Y_21 = N_21 D_1, Y_30 = N_30 D_0 + N_31 X_10, Y_31 = N_31 D_1
+    {
+        const int ob = w >> 1, nt = w & 1;                   // ob: 0 Y20, 1 Y21, 2 Y30, 3 Y31
+        const int ri = 2 + (ob >> 1), cj = ob & 1;
+        float* Ys = Yb + ob * (kBlkBytes / 4);
+        if (cj == 0) {
+            const float* A2[2] = {blk(Nb, ri, 0), blk(Nb, ri, 1)};
+            const float* B2[2] = {blk(Xb, 0, 0), blk(Xb, 1, 0)};
+            blk_mma<2>(Ys, A2, B2, nt, 1.f);
+        } else {
+            const float* A1[1] = {blk(Nb, ri, 1)};
+            const float* B1[1] = {blk(Xb, 1, 1)};
+            blk_mma<1>(Ys, A1, B1, nt, 1.f);
+        }
     }
     group_sync(kBarA);
-    {                                                // Z_i = N_{i+2,i} D_i + N_{i+2,i+1} X_{i+1,i}
-        const int i = w >> 2, rb = 4 * (w & 3);
-        float* const A2[2] = {blk(Nb, i + 2, i), blk(Nb, i + 2, i + 1)};
-        float* const B2[2] = {blk(Xb, i, i), blk(Xb, i + 1, i)};
-        blk_product<4, 2>(Yb + i * (kBlkBytes / 4), A2, B2, rb, 1.f);
-    }
-    group_sync(kBarA);
-    {                                                // X_{i+2,i} = -D_{i+2} Z_i
-        const int i = w >> 2, rb = 4 * (w & 3);
-        float* const A1[1] = {blk(Xb, i + 2, i + 2)};
-        float* const B1[1] = {Yb + i * (kBlkBytes / 4)};
-        blk_product<4, 1>(blk(Xb, i + 2, i), A1, B1, rb, -1.f);
-    }
-    group_sync(kBarA);
-    {                                                // Z = N_30 D_0 + N_31 X_10 + N_32 X_20
-        float* const A3[3] = {blk(Nb, 3, 0), blk(Nb, 3, 1), blk(Nb, 3, 2)};
-        float* const B3[3] = {blk(Xb, 0, 0), blk(Xb, 1, 0), blk(Xb, 2, 0)};
-        blk_product<2, 3>(Yb, A3, B3, 2 * w, 1.f);
-    }
-    group_sync(kBarA);
-    {                                                // X_30 = -D_3 Z
-        float* const A1[1] = {blk(Xb, 3, 3)};
-        float* const B1[1] = {Yb};
-        blk_product<2, 1>(blk(Xb, 3, 0), A1, B1, 2 * w, -1.f);
+    // X_lower = -C^{-1} Y: X_20 = -D_2 Y_20, X_21 = -D_2 Y_21, X_30 = -(X_32 Y_20 + D_3 Y_30), X_31 = -(X_32 Y_21 + D_3 Y_31)
+    {
+        const int ob = w >> 1, nt = w & 1;
+        const int ri = 2 + (ob >> 1), cj = ob & 1;
+        if (ri == 2) {
+            const float* A1[1] = {blk(Xb, 2, 2)};
+            const float* B1[1] = {Yb + cj * (kBlkBytes / 4)};
+            blk_mma<1>(blk(Xb, 2, cj), A1, B1, nt, -1.f);
+        } else {
+            const float* A2[2] = {blk(Xb, 3, 2), blk(Xb, 3, 3)};
+            const float* B2[2] = {Yb + cj * (kBlkBytes / 4), Yb + (2 + cj) * (kBlkBytes / 4)};
+            blk_mma<2>(blk(Xb, 3, cj), A2, B2, nt, -1.f);
+        }
     }
     group_sync(kBarA);
     {                                                // T[r][s] = X[r][s] beta_s (bf16)
@@ -443,12 +464,12 @@ __device__ void decay_state(uint32_t tb, const float* gam) {
 }
 
 // Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
-__device__ void read_w(uint32_t tb, uint8_t* wt) {
+__device__ void read_w(uint32_t tb, uint32_t col, uint8_t* wt) {
     const int c = lt();
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[32];
-        tmem_ld32(tmem_addr(tb, lane0(), kTmW + 32 * hf), v);
+        tmem_ld32(tmem_addr(tb, lane0(), col + 32 * hf), v);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -462,11 +483,11 @@ __device__ void read_w(uint32_t tb, uint8_t* wt) {
 }
 
 // Lane j holds Delta^T row j (fp32): pack to bf16 in TMEM as an A operand.
-__device__ void pack_delta(uint32_t tb) {
+__device__ void pack_delta(uint32_t tb, uint32_t col) {
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[32], pk[16];
-        tmem_ld32(tmem_addr(tb, lane0(), kTmU + 32 * hf), v);
+        tmem_ld32(tmem_addr(tb, lane0(), col + 32 * hf), v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
@@ -574,35 +595,36 @@ __device__ __noinline__ void token_chunk(uint32_t tb, float* A, const uint8_t* q
 
 // ---- MMA groups (each issued by one thread) --------------------------------------
 // AP = [Khat; Qhat] x Kb^T : M = 128, N = 64, K = 128 (both K-major).
-__device__ __forceinline__ void mma_gram(uint32_t tb, uint32_t sQK, uint32_t sKB) {
+__device__ __forceinline__ void mma_gram(uint32_t tb, uint32_t dcol, uint32_t sQK, uint32_t sKB) {
     constexpr uint32_t id = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 8; ++ks) {
         const uint64_t a = smem_desc(sQK + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128B);
         const uint64_t b = smem_desc(sKB + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-        mma_ss(tb + kTmAP, a, b, id, ks > 0);
+        mma_ss(tb + dcol, a, b, id, ks > 0);
     }
 }
 
 // W'^T = Khat^T T^T -> W columns; U^T = V^T T^T -> U columns.  M = 128, N = 64,
 // K = 64 tokens; A operands MN-major (channel halves LBO apart), B = T K-major.
-__device__ __forceinline__ void mma_wu(uint32_t tb, uint32_t sQK, uint32_t sV, uint32_t sTT) {
+__device__ __forceinline__ void mma_wu(uint32_t tb, uint32_t wcol, uint32_t ucol, uint32_t sQK, uint32_t sV,
+                                       uint32_t sTT) {
     constexpr uint32_t id = idesc_bf16_f32(128, 64, true, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 4; ++ks) {
         const uint64_t b = smem_desc(sTT + ks * 32, 16, 1024, kSwizzle128B);
-        mma_ss(tb + kTmW, smem_desc(sQK + ks * 2048, 16384, 1024, kSwizzle128B), b, id, ks > 0);
-        mma_ss(tb + kTmU, smem_desc(sV + ks * 2048, 8192, 1024, kSwizzle128B), b, id, ks > 0);
+        mma_ss(tb + wcol, smem_desc(sQK + ks * 2048, 16384, 1024, kSwizzle128B), b, id, ks > 0);
+        mma_ss(tb + ucol, smem_desc(sV + ks * 2048, 8192, 1024, kSwizzle128B), b, id, ks > 0);
     }
 }
 
 // Delta^T = U^T + Ss^T (-W'^T)  and  O^T = Ss^T Qhat^T : A = Ss^T from TMEM, K = 128.
-__device__ __forceinline__ void mma_delta_out(uint32_t tb, uint32_t sWT, uint32_t sQK) {
+__device__ __forceinline__ void mma_delta_out(uint32_t tb, uint32_t ucol, uint32_t sWT, uint32_t sQK) {
     constexpr uint32_t idw = idesc_bf16_f32(128, 64, false, true);
     constexpr uint32_t idq = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 8; ++ks)
-        mma_ts(tb + kTmU, tb + kTmSbf + ks * 8, smem_desc(sWT + ks * 2048, 16384, 1024, kSwizzle128B),
+        mma_ts(tb + ucol, tb + kTmSbf + ks * 8, smem_desc(sWT + ks * 2048, 16384, 1024, kSwizzle128B),
                idw, 1);
 #pragma unroll
     for (uint32_t ks = 0; ks < 8; ++ks)
@@ -704,12 +726,14 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         if (!(ok = group_wait(kBarA, &sw.qk_full[s], ph))) break;
         KDA_PHASE(3);
         if (t == 0) ++sw.consumed[kLdQK][s];
-        const bool fast = build_operands(qk, kb, reinterpret_cast<const float*>(aslot), L, sw.gam[s],
+        const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s],
                                          reinterpret_cast<float*>(pp));
         if (!fast) {                                     // token-by-token chunk
-            group_sync(kBarA);
+            if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
             if (t == 0) {
+                ++sw.consumed[kLdV][s];
                 sw.mode[s] = 1;
+                mbar_arrive(&sw.ready[s]);
                 mbar_arrive(&sw.ready[s]);
             }
             continue;
@@ -717,7 +741,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         group_publish(kBarA);
         KDA_PHASE(4);
         if (t == 0) {
-            mma_gram(x.tb, smem_u32(qk), smem_u32(kb));
+            mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
             mma_commit(&sw.gram_done);
         }
         gram_pending = true;
@@ -726,21 +750,32 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         gram_pending = false;
         KDA_PHASE(5);
         tc_fence_after();
-        read_gram(x.tb, aslot, pp, sw.beta[s]);
+        read_gram(x.tb, tm_apw(s), aslot, pp, sw.beta[s]);
         fence_proxy_async_smem();
         tc_fence_before();
         group_sync(kBarA);
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s]);
-        fence_proxy_async_smem();
-        group_sync(kBarA);
+        if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
+        if (t == 0) ++sw.consumed[kLdV][s];
+        group_publish(kBarA);
         KDA_PHASE(7);
-        if (t == 0) {
+        if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival
             sw.mode[s] = 0;
             mbar_arrive(&sw.ready[s]);
+            mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
+                   smem_u32(aslot + kTT));
+            mma_commit(&sw.ready[s]);
         }
     }
-    if (gram_pending) mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);   // let it land
+    if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
+        if (gram_pending) {
+            mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);
+            gram_ph ^= 1u;
+        }
+        mma_commit(&sw.gram_done);
+        mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);
+    }
     return ok;
 }
 
@@ -750,7 +785,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
     Small& sw = *x.sw;
     const int t = lt();
     const bool leader = (t == 0);
-    uint32_t wu_ph = 0, m1_ph = 0, m2_ph = 0;
+    uint32_t m1_ph = 0, m2_ph = 0;
     bool mma_pending = false;
     uint64_t* pending_bar = nullptr;
     uint32_t pending_ph = 0;
@@ -779,8 +814,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
                        sKB = smem_u32(x.sm + kKB0 + s * 16384), sPP = smem_u32(x.sm + kPP0 + s * 8192);
 
         if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
-        if (!(ok = group_wait(kBarB, &sw.v_full[s], ph))) break;
-        if (leader) ++sw.consumed[kLdV][s];
         KDA_PHASE(8);
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
@@ -793,22 +826,14 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             }
             continue;
         }
-        if (leader) {
-            mma_wu(x.tb, sQK, sV, sA + kTT);
-            mma_commit(&sw.wu_done);
-        }
-        mma_pending = true; pending_bar = &sw.wu_done; pending_ph = wu_ph;
+        if (leader && refill) issue_chunk(n + 2, s, true, true, false);   // W', U done: A, V slots free
         decay_state(x.tb, sw.gam[s]);
         KDA_PHASE(9);
-        if (!(ok = group_wait(kBarB, &sw.wu_done, wu_ph))) break;
-        wu_ph ^= 1u; mma_pending = false;
-        tc_fence_after();
-        if (leader && refill) issue_chunk(n + 2, s, true, true, false);
-        read_w(x.tb, x.sm + kWT);
+        read_w(x.tb, tm_apw(s), x.sm + kWT);
         group_publish(kBarB);
         KDA_PHASE(10);
         if (leader) {
-            mma_delta_out(x.tb, sWT, sQK);
+            mma_delta_out(x.tb, tm_u(s), sWT, sQK);
             mma_commit(&sw.mma1_done);
         }
         mma_pending = true; pending_bar = &sw.mma1_done; pending_ph = m1_ph;
@@ -817,7 +842,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         KDA_PHASE(11);
         tc_fence_after();
         if (leader && refill) issue_chunk(n + 2, s, false, false, true);
-        pack_delta(x.tb);
+        pack_delta(x.tb, tm_u(s));
         group_publish(kBarB);
         KDA_PHASE(12);
         if (leader) {
@@ -869,11 +894,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mbar_init(&sw->qk_full[s], 1);
             mbar_init(&sw->v_full[s], 1);
             mbar_init(&sw->a_full[s], 1);
-            mbar_init(&sw->ready[s], 1);
+            mbar_init(&sw->ready[s], 2);
             mbar_init(&sw->kbp_free[s], 1);
         }
         mbar_init(&sw->gram_done, 1);
-        mbar_init(&sw->wu_done, 1);
         mbar_init(&sw->mma1_done, 1);
         mbar_init(&sw->mma2_done, 1);
         fence_mbar_init();
