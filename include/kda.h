@@ -103,13 +103,57 @@ kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k,
                        void* out, float* final_state, kda_stream_t stream);
 
 /*
- * kda_decode_step -- one token for each of N independent sequences.
+ * kda_prefill_checkpointed -- kda_prefill that also saves the state at chosen
+ * points of each sequence, for the prefix-cache checkpoints that "Kimi K3
+ * architecture: KDA, MLA and MoE" (section "Serving K3 means managing two
+ * cache lifecycles") describes: KDA states kept only at reusable prefix
+ * boundaries, from which a later request resumes prefill.
  *
- * shape->total_tokens must equal shape->num_seqs.  q, k, log_alpha are
- * [N, H, dk], v and out [N, H, dv], beta [N, H]; state_inout [N, H, dk, dv]
- * fp32 is read once and overwritten in place with S_t.  out receives
- * o_t = S_t^T q_t.  Same error rules as kda_prefill; state_inout must not be
- * NULL.
+ * All other arguments and layouts are those of kda_prefill.
+ * ckpt_cu:     DEVICE int32 [N+1]; checkpoints ckpt_cu[n] .. ckpt_cu[n+1]-1
+ *              belong to sequence n (ckpt_cu[0] = 0, non-decreasing).
+ * ckpt_pos:    DEVICE int32 [ckpt_cu[N]]; for each checkpoint, the number of
+ *              tokens of its sequence after which the state is saved: strictly
+ *              increasing within a sequence, each a multiple of 64 or equal to
+ *              the sequence length.  A position that breaks these rules is not
+ *              written (kda_check_checkpoints validates a host copy).
+ * ckpt_states: [ckpt_cu[N], H, dk, dv] fp32, caller-owned; checkpoint c of a
+ *              sequence and head h lands at ckpt_states[c, h].
+ * The saved state equals the final state of a kda_prefill over the same
+ * prefix.  Errors: those of kda_prefill, plus KDA_ERR_INVALID_ARG for a NULL
+ * checkpoint pointer and KDA_ERR_UNSUPPORTED for a misaligned one (ckpt_states
+ * 16 bytes, the tables 4 bytes).
+ */
+kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const void* k,
+                                    const void* v, const float* log_alpha, const void* beta,
+                                    const float* initial_state, const int32_t* cu_seqlens,
+                                    void* out, float* final_state, const int32_t* ckpt_cu,
+                                    const int32_t* ckpt_pos, float* ckpt_states,
+                                    kda_stream_t stream);
+
+/*
+ * kda_check_checkpoints -- validate HOST copies of a cu_seqlens table and of a
+ * checkpoint table against the rules of kda_prefill_checkpointed.  Returns
+ * KDA_OK or KDA_ERR_INVALID_ARG.  No CUDA call.
+ */
+kda_status kda_check_checkpoints(const int32_t* host_cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, const int32_t* host_ckpt_cu,
+                                 const int32_t* host_ckpt_pos);
+
+/*
+ * kda_decode_step -- a decode step of T tokens (1 <= T <= 16) for each of N
+ * independent sequences, each starting from the state in state_inout.
+ *
+ * shape->num_seqs = N and shape->total_tokens = N * T.  q, k, log_alpha are
+ * [N*T, H, dk], v and out [N*T, H, dv], beta [N*T, H]; rows n*T .. n*T+T-1 are
+ * the tokens of sequence n in order (T = 1 is the ordinary one-token step).
+ * state_inout [N, H, dk, dv] fp32 is read once and overwritten in place with
+ * the state after the sequence's last token; out receives o_t = S_t^T q_t for
+ * every token.  The state crosses HBM once in each direction whatever T is.
+ * Errors: as kda_prefill; in addition KDA_ERR_INVALID_ARG if state_inout is
+ * NULL or total_tokens is not a positive multiple of num_seqs (num_seqs = 0
+ * with total_tokens = 0 is a no-op), KDA_ERR_UNSUPPORTED if T > 16 (use
+ * kda_prefill with initial_state for longer runs).
  */
 kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
                            const void* v, const float* log_alpha,

@@ -48,6 +48,10 @@ def lib():
         L.kda_prefill.restype = ctypes.c_int
         L.kda_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kda_decode_step.restype = ctypes.c_int
+        L.kda_prefill_checkpointed.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.kda_prefill_checkpointed.restype = ctypes.c_int
+        L.kda_check_checkpoints.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, vp, vp]
+        L.kda_check_checkpoints.restype = ctypes.c_int
         L.kda_check_cu_seqlens.argtypes = [vp, ctypes.c_int32, ctypes.c_int64]
         L.kda_check_cu_seqlens.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
@@ -138,14 +142,65 @@ def kda_prefill(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None, o
     return out, final_state
 
 
-def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):
-    """One decode step: q, k, log_alpha [N, H, dk]; v [N, H, dv]; beta [N, H];
-    state [N, H, dk, dv] fp32 updated in place.  Returns out [N, H, dv]."""
-    N, H, dk = q.shape
+def kda_prefill_checkpointed(q, k, v, log_alpha, beta, ckpt_pos, initial_state=None,
+                             cu_seqlens=None, out=None, final_state=None, num_seqs=None,
+                             stream=None):
+    """kda_prefill that also returns the state after chosen token counts.
+
+    ckpt_pos: list (one entry per sequence) of host lists of positions; each is a
+    token count from the sequence start, a multiple of 64 or the sequence length.
+    The tables are validated on the host, copied to the device, and the saved
+    states returned as [total_checkpoints, H, dk, dv] fp32 with the checkpoints
+    of sequence 0 first.  Returns (out, final_state, checkpoint_states).
+    """
+    T, H, dk = q.shape
     dv = v.shape[2]
+    if cu_seqlens is None:
+        n = 1 if num_seqs is None else int(num_seqs)
+        host_cu = torch.arange(n + 1, dtype=torch.int32) * (T // n)
+    elif isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda:
+        host_cu = cu_seqlens.cpu().to(torch.int32)
+    else:
+        host_cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+    n = host_cu.numel() - 1
+    if len(ckpt_pos) != n:
+        raise ValueError("ckpt_pos needs one list per sequence")
+    counts = [len(p) for p in ckpt_pos]
+    ck_cu = torch.tensor([0] + list(torch.tensor(counts).cumsum(0).tolist()) if n else [0], dtype=torch.int32)
+    ck_pos = torch.tensor([int(x) for p in ckpt_pos for x in p] or [0], dtype=torch.int32)
+    st = lib().kda_check_checkpoints(ctypes.c_void_p(host_cu.contiguous().data_ptr()), n, T,
+                                     ctypes.c_void_p(ck_cu.data_ptr()), ctypes.c_void_p(ck_pos.data_ptr()))
+    _check("kda_check_checkpoints", st)
+    dev = q.device
+    d_cu = host_cu.to(dev)
+    d_ck_cu, d_ck_pos = ck_cu.to(dev), ck_pos.to(dev)
+    total = int(ck_cu[-1])
+    ck_states = torch.empty((max(total, 1), H, dk, dv), dtype=torch.float32, device=dev)
     if out is None:
-        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    shape = KdaShape(N, N, H, dk, dv, _dtype_code(q))
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+    if final_state is True:
+        final_state = torch.empty((n, H, dk, dv), dtype=torch.float32, device=dev)
+    shape = KdaShape(n, T, H, dk, dv, _dtype_code(q))
+    st = lib().kda_prefill_checkpointed(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                        _ptr(beta), _ptr(initial_state), _ptr(d_cu), _ptr(out),
+                                        _ptr(final_state), _ptr(d_ck_cu), _ptr(d_ck_pos),
+                                        _ptr(ck_states), _stream(stream))
+    _check("kda_prefill_checkpointed", st)
+    return out, final_state, ck_states[:total]
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):
+    """Decode step of T tokens per sequence (see ``include/kda.h``).
+
+    state: [N, H, dk, dv] fp32, updated in place.  q, k, log_alpha: [N*T, H, dk];
+    v: [N*T, H, dv]; beta: [N*T, H]; rows n*T .. n*T+T-1 belong to sequence n
+    (T = 1 is the one-token step).  Returns out [N*T, H, dv]."""
+    rows, H, dk = q.shape
+    dv = v.shape[2]
+    N = state.shape[0]
+    if out is None:
+        out = torch.empty((rows, H, dv), dtype=q.dtype, device=q.device)
+    shape = KdaShape(N, rows, H, dk, dv, _dtype_code(q))
     st = lib().kda_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                _ptr(beta), _ptr(state), _ptr(out), _stream(stream))
     _check("kda_decode_step", st)

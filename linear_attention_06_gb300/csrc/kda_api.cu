@@ -83,10 +83,14 @@ kda_status kda_check_cu_seqlens(const int32_t* cu, int32_t num_seqs, int64_t tot
     return KDA_OK;
 }
 
-kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k, const void* v,
-                       const float* log_alpha, const void* beta, const float* initial_state,
-                       const int32_t* cu_seqlens, void* out, float* final_state,
-                       kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+kda_status prefill_impl(const kda_shape* shape, const void* q, const void* k, const void* v,
+                        const float* log_alpha, const void* beta, const float* initial_state,
+                        const int32_t* cu_seqlens, void* out, float* final_state,
+                        const int32_t* ckpt_cu, const int32_t* ckpt_pos, float* ckpt_states,
+                        kda_stream_t stream) {
     kda_status st = check_shape(shape);
     if (st != KDA_OK) return st;
     if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
@@ -106,7 +110,8 @@ kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k, con
     if (!status) return KDA_ERR_CUDA;
     kda::PrefillArgs a{q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
                        shape->total_tokens, shape->num_seqs, shape->H, shape->dk, shape->dv,
-                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, status};
+                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, status,
+                       ckpt_cu, ckpt_pos, ckpt_states};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const char* force = getenv("KDA_PREFILL_IMPL");
     const bool want_recurrent = force && strcmp(force, "recurrent") == 0;
@@ -117,19 +122,62 @@ kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k, con
         e = kda::launch_recurrent_prefill(a, s);
     return finish(e, s);
 }
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill(const kda_shape* shape, const void* q, const void* k, const void* v,
+                       const float* log_alpha, const void* beta, const float* initial_state,
+                       const int32_t* cu_seqlens, void* out, float* final_state,
+                       kda_stream_t stream) {
+    return prefill_impl(shape, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                        nullptr, nullptr, nullptr, stream);
+}
+
+kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const void* k,
+                                    const void* v, const float* log_alpha, const void* beta,
+                                    const float* initial_state, const int32_t* cu_seqlens,
+                                    void* out, float* final_state, const int32_t* ckpt_cu,
+                                    const int32_t* ckpt_pos, float* ckpt_states,
+                                    kda_stream_t stream) {
+    if (!ckpt_cu || !ckpt_pos || !ckpt_states) return KDA_ERR_INVALID_ARG;
+    if (!aligned(ckpt_cu, 4) || !aligned(ckpt_pos, 4) || !aligned(ckpt_states, 16))
+        return KDA_ERR_UNSUPPORTED;
+    return prefill_impl(shape, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                        ckpt_cu, ckpt_pos, ckpt_states, stream);
+}
+
+kda_status kda_check_checkpoints(const int32_t* cu, int32_t num_seqs, int64_t total_tokens,
+                                 const int32_t* ckpt_cu, const int32_t* ckpt_pos) {
+    if (kda_check_cu_seqlens(cu, num_seqs, total_tokens) != KDA_OK) return KDA_ERR_INVALID_ARG;
+    if (!ckpt_cu || (ckpt_cu[num_seqs] > 0 && !ckpt_pos) || ckpt_cu[0] != 0) return KDA_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        if (ckpt_cu[n + 1] < ckpt_cu[n]) return KDA_ERR_INVALID_ARG;
+        const int64_t len = (int64_t)cu[n + 1] - cu[n];
+        int64_t prev = 0;
+        for (int32_t c = ckpt_cu[n]; c < ckpt_cu[n + 1]; ++c) {
+            const int64_t p = ckpt_pos[c];
+            if (p <= prev || p > len || (p % 64 != 0 && p != len)) return KDA_ERR_INVALID_ARG;
+            prev = p;
+        }
+    }
+    return KDA_OK;
+}
 
 kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k, const void* v,
                            const float* log_alpha, const void* beta, float* state_inout,
                            void* out, kda_stream_t stream) {
     kda_status st = check_shape(shape);
     if (st != KDA_OK) return st;
-    if (shape->total_tokens != shape->num_seqs) return KDA_ERR_INVALID_ARG;
-    if (shape->num_seqs == 0) return KDA_OK;
+    if (shape->num_seqs == 0) return shape->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens <= 0 || shape->total_tokens % shape->num_seqs != 0) return KDA_ERR_INVALID_ARG;
+    const int64_t tps = shape->total_tokens / shape->num_seqs;
+    if (tps > kda::kMaxDecodeTokens) return KDA_ERR_UNSUPPORTED;
     if (!state_inout) return KDA_ERR_INVALID_ARG;
     st = check_tensor_ptrs(shape, q, k, v, log_alpha, beta, out);
     if (st != KDA_OK) return st;
     if (!aligned(state_inout, 16)) return KDA_ERR_UNSUPPORTED;
-    kda::DecodeArgs a{q, k, v, log_alpha, beta, state_inout, out, shape->num_seqs, shape->H,
+    kda::DecodeArgs a{q, k, v, log_alpha, beta, state_inout, out, shape->num_seqs, (int32_t)tps, shape->H,
                       shape->dk, shape->dv,
                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

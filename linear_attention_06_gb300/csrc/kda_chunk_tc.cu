@@ -90,8 +90,9 @@ constexpr uint32_t kTT = 24576;                                        // T, 64 
 constexpr uint32_t kQKBytes = 32768, kVBytes = 16384, kABytes = 32768;
 
 // ---- TMEM columns
-constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmDbf = 128, kTmO = 192;
-// two slots (chunk parity) each for U / Delta and for the Gram result, which W' later overwrites
+constexpr uint32_t kTmS = 0, kTmSbf = 128, kTmDbf = 192;
+// two slots (chunk parity) each for U / Delta / then the chunk's output O, and for the Gram result,
+// which W' later overwrites
 __device__ __forceinline__ uint32_t tm_u(int s) { return 256u + 64u * s; }
 __device__ __forceinline__ uint32_t tm_apw(int s) { return 384u + 64u * s; }
 constexpr uint32_t kTmCols = 512;
@@ -106,6 +107,8 @@ struct Small {
     uint64_t ready[2];                           // group A -> B: chunk prepared and W', U computed (2 arrivals)
     uint64_t kbp_free[2];                        // group B -> A: Kb / P / beta / gamma slot free
     uint64_t gram_done, mma1_done, mma2_done;
+    uint64_t wu_done[2];                         // W', U of the chunk in a slot finished (group A refills)
+    uint64_t u_free[2];                          // group B read the output held in a U slot
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
     int pad[5];
@@ -496,20 +499,27 @@ __device__ void pack_delta(uint32_t tb, uint32_t col) {
     tmem_wait_st();
 }
 
-// Lane j holds O^T row j.  The rows are transposed through a 64 x 256-byte
-// staging tile and written as 16-byte row segments, rows [0, L) only.
-__device__ void store_out(uint32_t tb, uint8_t* stg, __nv_bfloat16* out, int64_t t0, int H, int h,
-                          int L) {
-    const int t = lt();
-#pragma unroll 1
+// Lane j holds O^T row j: read it out of TMEM, packed to bf16 pairs of rows.
+__device__ __forceinline__ void o_to_regs(uint32_t tb, uint32_t col, uint32_t (&opk)[32]) {
+#pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[32];
-        tmem_ld32(tmem_addr(tb, lane0(), kTmO + 32 * hf), v);
+        tmem_ld32(tmem_addr(tb, lane0(), col + 32 * hf), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<__nv_bfloat16*>(stg + (32 * hf + i) * 256 + t * 2) =
-                __float2bfloat16_rn(__uint_as_float(v[i]));
+        for (int i = 0; i < 16; ++i) opk[16 * hf + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    }
+}
+
+// Transpose the held output rows through a 64 x 256-byte staging tile and write
+// them as 16-byte row segments, rows [0, L) only.
+__device__ void o_store(const uint32_t (&opk)[32], uint8_t* stg, __nv_bfloat16* out, int64_t t0, int H,
+                        int h, int L) {
+    const int t = lt();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        *reinterpret_cast<uint16_t*>(stg + (2 * i) * 256 + t * 2) = (uint16_t)(opk[i] & 0xffffu);
+        *reinterpret_cast<uint16_t*>(stg + (2 * i + 1) * 256 + t * 2) = (uint16_t)(opk[i] >> 16);
     }
     group_sync(kBarB);
 #pragma unroll
@@ -520,6 +530,7 @@ __device__ void store_out(uint32_t tb, uint8_t* stg, __nv_bfloat16* out, int64_t
             *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
         }
     }
+    group_sync(kBarB);
 }
 
 __device__ void load_state(uint32_t tb, const float* h0, size_t base) {
@@ -618,33 +629,33 @@ __device__ __forceinline__ void mma_wu(uint32_t tb, uint32_t wcol, uint32_t ucol
     }
 }
 
-// Delta^T = U^T + Ss^T (-W'^T)  and  O^T = Ss^T Qhat^T : A = Ss^T from TMEM, K = 128.
-__device__ __forceinline__ void mma_delta_out(uint32_t tb, uint32_t ucol, uint32_t sWT, uint32_t sQK) {
+// Delta^T = U^T + Ss^T (-W'^T) in the U slot: A = Ss^T from TMEM, K = 128.
+__device__ __forceinline__ void mma_delta(uint32_t tb, uint32_t ucol, uint32_t sWT) {
     constexpr uint32_t idw = idesc_bf16_f32(128, 64, false, true);
-    constexpr uint32_t idq = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 8; ++ks)
         mma_ts(tb + ucol, tb + kTmSbf + ks * 8, smem_desc(sWT + ks * 2048, 16384, 1024, kSwizzle128B),
                idw, 1);
-#pragma unroll
-    for (uint32_t ks = 0; ks < 8; ++ks)
-        mma_ts(tb + kTmO, tb + kTmSbf + ks * 8,
-               smem_desc(sQK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128B), idq,
-               ks > 0);
 }
 
-// S^T += Delta^T Kb (N = 128, Kb MN-major) and O^T += Delta^T P^T (N = 64):
-// A = Delta^T from TMEM, K = 64 tokens.
-__device__ __forceinline__ void mma_state_out(uint32_t tb, uint32_t sKB, uint32_t sPP) {
+// S^T += Delta^T Kb (N = 128, Kb MN-major); then the chunk output, in the U slot
+// (Delta is already packed): O^T = Ss^T Qhat^T + Delta^T P^T.
+__device__ __forceinline__ void mma_state_out(uint32_t tb, uint32_t ocol, uint32_t sKB, uint32_t sQK,
+                                              uint32_t sPP) {
     constexpr uint32_t ids = idesc_bf16_f32(128, 128, false, true);
-    constexpr uint32_t idp = idesc_bf16_f32(128, 64, false, false);
+    constexpr uint32_t idq = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
     for (uint32_t ks = 0; ks < 4; ++ks)
         mma_ts(tb + kTmS, tb + kTmDbf + ks * 8, smem_desc(sKB + ks * 2048, 8192, 1024, kSwizzle128B),
                ids, 1);
 #pragma unroll
+    for (uint32_t ks = 0; ks < 8; ++ks)
+        mma_ts(tb + ocol, tb + kTmSbf + ks * 8,
+               smem_desc(sQK + 8192 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128B), idq,
+               ks > 0);
+#pragma unroll
     for (uint32_t ks = 0; ks < 4; ++ks)
-        mma_ts(tb + kTmO, tb + kTmDbf + ks * 8, smem_desc(sPP + ks * 32, 16, 1024, kSwizzle128B), idp, 1);
+        mma_ts(tb + ocol, tb + kTmDbf + ks * 8, smem_desc(sPP + ks * 32, 16, 1024, kSwizzle128B), idq, 1);
 }
 
 #ifdef KDA_PHASE_TIMING
@@ -688,17 +699,54 @@ struct Ctx {
     Small* sw;
     uint32_t tb;
     int64_t bos, eos;
-    int nchunks, H, h;
+    int nchunks, H, h, seq;
+};
+
+// Optional checkpoints of one sequence: the state after ck_pos[c] tokens goes to
+// ck_states[c]; a position that is not a chunk end (a multiple of 64 or the
+// sequence end) is skipped.
+struct Ckpt {
+    const int32_t* pos;
+    float* states;
+    int c, end;
+    __device__ void init(const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states, int seq) {
+        pos = ck_pos;
+        states = ck_states;
+        c = end = 0;
+        if (ck_states) {
+            c = ck_cu[seq];
+            end = ck_cu[seq + 1];
+        }
+    }
+    // called by the whole group after the chunk that ends `done` tokens into the sequence
+    __device__ void after_chunk(uint32_t tb, int64_t done, bool seq_end, int H, int h) {
+        while (c < end) {
+            const int64_t p = pos[c];
+            if (p > done) break;
+            if (p == done && (done % C == 0 || seq_end))
+                store_state(tb, states, ((size_t)c * H + h) * D * D);
+            ++c;
+        }
+    }
 };
 
 enum { kLdQK = 0, kLdV = 1, kLdA = 2 };
 
+// TMA refill of slot s with the tiles of chunk c (issued by one thread).
+__device__ __forceinline__ void refill(const Ctx& x, const Maps& maps, int c, int s, bool a, bool v, bool q) {
+    Small& sw = *x.sw;
+    const int tc = (int)(x.bos + (int64_t)c * C);
+    if (a) { load_a(x.sm + kA0 + s * kABytes, maps, x.h, tc, &sw.a_full[s]); ++sw.issued[kLdA][s]; }
+    if (v) { load_v(x.sm + kV0 + s * kVBytes, maps, x.h, tc, &sw.v_full[s]); ++sw.issued[kLdV][s]; }
+    if (q) { load_qk(x.sm + kQK0 + s * kQKBytes, maps, x.h, tc, &sw.qk_full[s]); ++sw.issued[kLdQK][s]; }
+}
+
 // ============================ group A loop =======================================
-__device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __restrict__ beta) {
+__device__ __noinline__ bool run_group_a(const Ctx& x, const Maps& maps, const __nv_bfloat16* __restrict__ beta) {
     Small& sw = *x.sw;
     const int t = lt();
-    uint32_t gram_ph = 0;
-    bool ok = true, gram_pending = false;
+    uint32_t gram_ph = 0, wu_ph[2] = {0u, 0u}, u_ph[2] = {0u, 0u};
+    bool ok = true, gram_pending = false, prev_fast = false;
     float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
     for (int n = 0; n < x.nchunks; ++n) {
@@ -718,6 +766,15 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
 
         if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
         KDA_PHASE(0);
+        // log_alpha and v of chunk n+1 go into the other slot once the W', U products of
+        // chunk n-1 (which read that slot) are done; a token-by-token chunk n-1 is refilled by B
+        if (t == 0 && n >= 1 && prev_fast && n + 1 < x.nchunks) {
+            const int so = s ^ 1;
+            if (mbar_wait_bounded(&sw.wu_done[so], wu_ph[so], kWaitLimitNs)) {
+                wu_ph[so] ^= 1u;
+                refill(x, maps, n + 1, so, true, true, false);
+            }
+        }
         if (t == 0) ++sw.consumed[kLdA][s];
         KDA_PHASE(1);
         if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
@@ -728,6 +785,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         if (t == 0) ++sw.consumed[kLdQK][s];
         const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s],
                                          reinterpret_cast<float*>(pp));
+        prev_fast = fast;
         if (!fast) {                                     // token-by-token chunk
             if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
             if (t == 0) {
@@ -758,6 +816,9 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         solve_T(aslot, sw.beta[s]);
         if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
+        // the U slot still holds chunk n-2's output until group B has read it
+        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], u_ph[s]))) break;
+        if (n >= 2) u_ph[s] ^= 1u;
         group_publish(kBarA);
         KDA_PHASE(7);
         if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival
@@ -766,6 +827,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
             mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
                    smem_u32(aslot + kTT));
             mma_commit(&sw.ready[s]);
+            mma_commit(&sw.wu_done[s]);
         }
     }
     if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
@@ -779,24 +841,36 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
     return ok;
 }
 
+// Store the output a chunk left in its U slot (through the staging tile), then
+// release that U slot to group A.
+__device__ __forceinline__ void flush_prev(const Ctx& x, __nv_bfloat16* out, int prev_s, int64_t prev_t0,
+                                           int prev_L, bool leader) {
+    uint32_t opk[32];
+    o_to_regs(x.tb, tm_u(prev_s), opk);
+    tc_fence_before();
+    o_store(opk, x.sm + kWT, out, prev_t0, x.H, x.h, prev_L);
+    if (leader) mbar_arrive(&x.sw->u_free[prev_s]);
+}
+
 // ============================ group B loop =======================================
 __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bfloat16* __restrict__ out,
-                            const float* __restrict__ h0, float* __restrict__ hT, size_t sbase) {
+                            const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
+                            const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
     Small& sw = *x.sw;
+    Ckpt ck;
+    ck.init(ck_cu, ck_pos, ck_states, x.seq);
     const int t = lt();
     const bool leader = (t == 0);
     uint32_t m1_ph = 0, m2_ph = 0;
     bool mma_pending = false;
     uint64_t* pending_bar = nullptr;
     uint32_t pending_ph = 0;
-    auto issue_chunk = [&](int c, int s, bool a, bool v, bool q) {
-        const int tc = (int)(x.bos + (int64_t)c * C);
-        if (a) { load_a(x.sm + kA0 + s * kABytes, maps, x.h, tc, &sw.a_full[s]); ++sw.issued[kLdA][s]; }
-        if (v) { load_v(x.sm + kV0 + s * kVBytes, maps, x.h, tc, &sw.v_full[s]); ++sw.issued[kLdV][s]; }
-        if (q) { load_qk(x.sm + kQK0 + s * kQKBytes, maps, x.h, tc, &sw.qk_full[s]); ++sw.issued[kLdQK][s]; }
-    };
+    // the previous chunk's output waits in its U slot until the next Delta product is in flight
+    bool have_prev = false;
+    int prev_s = 0, prev_L = 0;
+    int64_t prev_t0 = 0;
     if (leader)
-        for (int c = 0; c < 2 && c < x.nchunks; ++c) issue_chunk(c, c, true, true, true);
+        for (int c = 0; c < 2 && c < x.nchunks; ++c) refill(x, maps, c, c, true, true, true);
     load_state(x.tb, h0, sbase);
     const uint32_t sWT = smem_u32(x.sm + kWT);
     bool ok = true;
@@ -806,34 +880,40 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         const uint32_t ph = (n >> 1) & 1;
         const int64_t t0 = x.bos + (int64_t)n * C;
         const int L = (int)((x.eos - t0) < C ? (x.eos - t0) : C);
-        const bool refill = (n + 2 < x.nchunks);
+        const bool more = (n + 2 < x.nchunks);
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* vs = x.sm + kV0 + s * kVBytes;
-        const uint32_t sQK = smem_u32(qk), sV = smem_u32(vs), sA = smem_u32(aslot),
-                       sKB = smem_u32(x.sm + kKB0 + s * 16384), sPP = smem_u32(x.sm + kPP0 + s * 8192);
+        const uint32_t sQK = smem_u32(qk), sKB = smem_u32(x.sm + kKB0 + s * 16384),
+                       sPP = smem_u32(x.sm + kPP0 + s * 8192);
 
         if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
         KDA_PHASE(8);
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
+            if (have_prev) {
+                flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
+                have_prev = false;
+            }
             token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], out, t0, x.H, x.h, L);
             tc_fence_before();
             group_sync(kBarB);
+            tc_fence_after();
+            ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
             if (leader) {
-                if (refill) issue_chunk(n + 2, s, true, true, true);
+                if (more) refill(x, maps, n + 2, s, true, true, true);
                 mbar_arrive(&sw.kbp_free[s]);
+                mbar_arrive(&sw.u_free[s]);              // this chunk left no output in its U slot
             }
             continue;
         }
-        if (leader && refill) issue_chunk(n + 2, s, true, true, false);   // W', U done: A, V slots free
         decay_state(x.tb, sw.gam[s]);
         KDA_PHASE(9);
         read_w(x.tb, tm_apw(s), x.sm + kWT);
         group_publish(kBarB);
         KDA_PHASE(10);
         if (leader) {
-            mma_delta_out(x.tb, tm_u(s), sWT, sQK);
+            mma_delta(x.tb, tm_u(s), sWT);
             mma_commit(&sw.mma1_done);
         }
         mma_pending = true; pending_bar = &sw.mma1_done; pending_ph = m1_ph;
@@ -841,27 +921,33 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         m1_ph ^= 1u; mma_pending = false;
         KDA_PHASE(11);
         tc_fence_after();
-        if (leader && refill) issue_chunk(n + 2, s, false, false, true);
         pack_delta(x.tb, tm_u(s));
         group_publish(kBarB);
         KDA_PHASE(12);
         if (leader) {
-            mma_state_out(x.tb, sKB, sPP);
+            mma_state_out(x.tb, tm_u(s), sKB, sQK, sPP);
             mma_commit(&sw.mma2_done);
             mma_commit(&sw.kbp_free[s]);
         }
         mma_pending = true; pending_bar = &sw.mma2_done; pending_ph = m2_ph;
+        if (have_prev) {                                 // previous output, under this chunk's MMAs
+            flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
+            have_prev = false;
+        }
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
         m2_ph ^= 1u; mma_pending = false;
         KDA_PHASE(13);
         tc_fence_after();
-        store_out(x.tb, x.sm + kWT, out, t0, x.H, x.h, L);
+        if (leader && more) refill(x, maps, n + 2, s, false, false, true);   // Qhat consumed
+        ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
+        have_prev = true; prev_s = s; prev_L = L; prev_t0 = t0;
         tc_fence_before();
         group_sync(kBarB);
         tc_fence_after();
         KDA_PHASE(14);
     }
     if (ok) {
+        if (have_prev) flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
         if (hT) store_state(x.tb, hT, sbase);
     } else if (mma_pending) {
         mbar_wait_bounded(pending_bar, pending_ph, kWaitLimitNs);
@@ -873,7 +959,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
                 const float* __restrict__ h0, const int32_t* __restrict__ cu,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ hT, int64_t T, int num_seqs,
-                int H, unsigned int* status) {
+                int H, unsigned int* status, const int32_t* __restrict__ ck_cu,
+                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -885,6 +972,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     x.H = H;
     x.h = blockIdx.x % H;
     const int n = blockIdx.x / H;
+    x.seq = n;
     seq_bounds(cu, n, num_seqs, T, x.bos, x.eos);
     x.nchunks = (int)((x.eos - x.bos + C - 1) / C);
     const size_t sbase = ((size_t)n * H + x.h) * D * D;
@@ -900,6 +988,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         mbar_init(&sw->gram_done, 1);
         mbar_init(&sw->mma1_done, 1);
         mbar_init(&sw->mma2_done, 1);
+        mbar_init(&sw->wu_done[0], 1);
+        mbar_init(&sw->wu_done[1], 1);
+        mbar_init(&sw->u_free[0], 1);
+        mbar_init(&sw->u_free[1], 1);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
@@ -917,7 +1009,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     tc_fence_after();
     x.tb = sw->tmem_base;
 
-    const bool ok = in_group_a() ? run_group_a(x, beta) : run_group_b(x, maps, out, h0, hT, sbase);
+    const bool ok = in_group_a() ? run_group_a(x, maps, beta) : run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
     if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
 
     tc_fence_before();
@@ -1000,7 +1092,8 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
     const unsigned blocks = (unsigned)((int64_t)a.num_seqs * a.H);
     chunk_tc_kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
         maps, static_cast<const __nv_bfloat16*>(a.beta), a.initial_state, a.cu_seqlens,
-        static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.status);
+        static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.status,
+        a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
     return cudaGetLastError();
 }
 

@@ -12,6 +12,10 @@
 //   S  = S' + k delta^T                        written back in place
 //   o  = S^T q = y + (k . q) delta             read after write
 //
+// Several tokens per sequence (tokens_per_seq = T, at most 16) run through the
+// same block one after another with the state held in registers, so a short
+// multi-token step costs the same state traffic as a single token.
+//
 // Layout of the work: one block of 256 threads per (sequence, head).  A row of
 // S (dv fp32) is covered by dv/4 threads with 16-byte loads, so each warp
 // instruction moves whole 512-byte rows; each thread keeps its rows in
@@ -38,13 +42,14 @@ template <int DK, int DV, typename Tin>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ log_alpha, const Tin* __restrict__ beta,
-              float* __restrict__ S, Tin* __restrict__ out) {
+              float* __restrict__ S, Tin* __restrict__ out, int H, int T) {
     constexpr int LANES = DV / 4;          // threads per row (float4 each)
     constexpr int RG = kThreads / LANES;   // row groups
     constexpr int RPT = DK / RG;           // rows per thread
     static_assert(RPT * RG == DK, "row split");
 
     const size_t p = blockIdx.x;           // (sequence, head) pair
+    const size_t n = p / H, h = p % H;
     const int c4 = threadIdx.x % LANES;
     const int g = threadIdx.x / LANES;
     float4* Sp = reinterpret_cast<float4*>(S + p * DK * DV);
@@ -58,56 +63,63 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     __shared__ float red_r[RG][DV], red_y[RG][DV];
     __shared__ float kq_s;
     __shared__ float beta_s;
-    for (int i = threadIdx.x; i < DK; i += kThreads) {
-        ks[i] = to_f32(k[p * DK + i]);
-        qs[i] = to_f32(q[p * DK + i]);
-        al[i] = expf(log_alpha[p * DK + i]);
-    }
-    for (int j = threadIdx.x; j < DV; j += kThreads) vs[j] = to_f32(v[p * DV + j]);
-    if (threadIdx.x == 0) beta_s = to_f32(beta[p]);
-    __syncthreads();
+    // The T tokens of this sequence are rows n*T .. n*T+T-1; the state stays in
+    // registers between them and crosses HBM once in each direction.
+    for (int tok = 0; tok < T; ++tok) {
+        const size_t row = (n * (size_t)T + tok) * H + h;
+        for (int i = threadIdx.x; i < DK; i += kThreads) {
+            ks[i] = to_f32(k[row * DK + i]);
+            qs[i] = to_f32(q[row * DK + i]);
+            al[i] = expf(log_alpha[row * DK + i]);
+        }
+        for (int j = threadIdx.x; j < DV; j += kThreads) vs[j] = to_f32(v[row * DV + j]);
+        if (threadIdx.x == 0) beta_s = to_f32(beta[row]);
+        __syncthreads();
 
-    if (threadIdx.x < 32) {               // k . q on warp 0
-        float acc = 0.f;
-        for (int i = threadIdx.x; i < DK; i += 32) acc = fmaf(ks[i], qs[i], acc);
+        if (threadIdx.x < 32) {               // k . q on warp 0
+            float acc = 0.f;
+            for (int i = threadIdx.x; i < DK; i += 32) acc = fmaf(ks[i], qs[i], acc);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (threadIdx.x == 0) kq_s = acc;
-    }
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (threadIdx.x == 0) kq_s = acc;
+        }
 
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f), y = r;
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f), y = r;
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-        const int i = g + RG * m;
-        const float a = al[i], ki = ks[i], qi = qs[i];
-        s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
-        r.x = fmaf(s[m].x, ki, r.x); r.y = fmaf(s[m].y, ki, r.y);
-        r.z = fmaf(s[m].z, ki, r.z); r.w = fmaf(s[m].w, ki, r.w);
-        y.x = fmaf(s[m].x, qi, y.x); y.y = fmaf(s[m].y, qi, y.y);
-        y.z = fmaf(s[m].z, qi, y.z); y.w = fmaf(s[m].w, qi, y.w);
-    }
-    *reinterpret_cast<float4*>(&red_r[g][4 * c4]) = r;
-    *reinterpret_cast<float4*>(&red_y[g][4 * c4]) = y;
-    __syncthreads();
+        for (int m = 0; m < RPT; ++m) {
+            const int i = g + RG * m;
+            const float a = al[i], ki = ks[i], qi = qs[i];
+            s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
+            r.x = fmaf(s[m].x, ki, r.x); r.y = fmaf(s[m].y, ki, r.y);
+            r.z = fmaf(s[m].z, ki, r.z); r.w = fmaf(s[m].w, ki, r.w);
+            y.x = fmaf(s[m].x, qi, y.x); y.y = fmaf(s[m].y, qi, y.y);
+            y.z = fmaf(s[m].z, qi, y.z); y.w = fmaf(s[m].w, qi, y.w);
+        }
+        *reinterpret_cast<float4*>(&red_r[g][4 * c4]) = r;
+        *reinterpret_cast<float4*>(&red_y[g][4 * c4]) = y;
+        __syncthreads();
 
-    for (int j = threadIdx.x; j < DV; j += kThreads) {
-        float rj = 0.f, yj = 0.f;
+        for (int j = threadIdx.x; j < DV; j += kThreads) {
+            float rj = 0.f, yj = 0.f;
 #pragma unroll
-        for (int gg = 0; gg < RG; ++gg) { rj += red_r[gg][j]; yj += red_y[gg][j]; }
-        const float d = beta_s * (vs[j] - rj);
-        dl[j] = d;
-        store_as(&out[p * DV + j], fmaf(kq_s, d, yj));
-    }
-    __syncthreads();
+            for (int gg = 0; gg < RG; ++gg) { rj += red_r[gg][j]; yj += red_y[gg][j]; }
+            const float d = beta_s * (vs[j] - rj);
+            dl[j] = d;
+            store_as(&out[row * DV + j], fmaf(kq_s, d, yj));
+        }
+        __syncthreads();
 
-    const float4 d4 = *reinterpret_cast<const float4*>(&dl[4 * c4]);
+        const float4 d4 = *reinterpret_cast<const float4*>(&dl[4 * c4]);
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-        const float ki = ks[g + RG * m];
-        s[m].x = fmaf(ki, d4.x, s[m].x); s[m].y = fmaf(ki, d4.y, s[m].y);
-        s[m].z = fmaf(ki, d4.z, s[m].z); s[m].w = fmaf(ki, d4.w, s[m].w);
-        __stcs(Sp + (size_t)(g + RG * m) * LANES + c4, s[m]);
+        for (int m = 0; m < RPT; ++m) {
+            const float ki = ks[g + RG * m];
+            s[m].x = fmaf(ki, d4.x, s[m].x); s[m].y = fmaf(ki, d4.y, s[m].y);
+            s[m].z = fmaf(ki, d4.z, s[m].z); s[m].w = fmaf(ki, d4.w, s[m].w);
+        }
+        __syncthreads();   // the vectors of this token are dead before the next token's load
     }
+#pragma unroll
+    for (int m = 0; m < RPT; ++m) __stcs(Sp + (size_t)(g + RG * m) * LANES + c4, s[m]);
 }
 
 template <int DK, int DV>
@@ -117,12 +129,13 @@ cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
         decode_kernel<DK, DV, float><<<blocks, kThreads, 0, st>>>(
             static_cast<const float*>(a.q), static_cast<const float*>(a.k),
             static_cast<const float*>(a.v), a.log_alpha, static_cast<const float*>(a.beta),
-            a.state, static_cast<float*>(a.out));
+            a.state, static_cast<float*>(a.out), a.H, a.tokens_per_seq);
     } else {
         decode_kernel<DK, DV, __nv_bfloat16><<<blocks, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
             static_cast<const __nv_bfloat16*>(a.v), a.log_alpha,
-            static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out));
+            static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out), a.H,
+            a.tokens_per_seq);
     }
     return cudaGetLastError();
 }

@@ -25,6 +25,12 @@ struct PrefillArgs {
     int32_t H, dk, dv;
     DType dtype;
     unsigned int* status;         // device status word (timeouts)
+    // optional state checkpoints (all null when not requested): checkpoints
+    // ckpt_cu[n] .. ckpt_cu[n+1]-1 of sequence n are saved after ckpt_pos[c]
+    // tokens of that sequence into ckpt_states[c] ([H, dk, dv] fp32 each)
+    const int32_t* ckpt_cu = nullptr;
+    const int32_t* ckpt_pos = nullptr;
+    float* ckpt_states = nullptr;
 };
 
 struct DecodeArgs {
@@ -36,6 +42,7 @@ struct DecodeArgs {
     float* state;
     void* out;
     int32_t num_seqs;
+    int32_t tokens_per_seq;       // T >= 1: rows n*T .. n*T+T-1 belong to sequence n
     int32_t H, dk, dv;
     DType dtype;
 };
@@ -45,8 +52,11 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // Chunkwise tensor-core prefill: bf16, dk = dv = 128.
 bool chunk_tc_supported(const PrefillArgs& a);
 cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s);
-// One decode step.
+// One decode step of T tokens per sequence (state in place).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Longest run of tokens per sequence that kda_decode_step accepts.
+constexpr int kMaxDecodeTokens = 16;
 
 // Bits of the device status word.
 constexpr unsigned int kStatusTimeout = 1u;

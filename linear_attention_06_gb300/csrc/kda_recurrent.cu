@@ -53,7 +53,9 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                          const Tin* __restrict__ v, const float* __restrict__ log_alpha,
                          const Tin* __restrict__ beta, const float* __restrict__ h0,
                          const int32_t* __restrict__ cu, Tin* __restrict__ out,
-                         float* __restrict__ hT, int64_t T, int num_seqs, int H, int dv) {
+                         float* __restrict__ hT, int64_t T, int num_seqs, int H, int dv,
+                         const int32_t* __restrict__ ck_cu, const int32_t* __restrict__ ck_pos,
+                         float* __restrict__ ck_states) {
     const int tiles = dv / kCols;
     const int n = blockIdx.x / tiles;
     const int j = (blockIdx.x % tiles) * kCols + threadIdx.x;
@@ -84,6 +86,14 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
     if (bos < eos) stage(bos, 0);
     __syncthreads();
 
+    // checkpoints of this sequence: the state after ck_pos[ck] tokens goes to ck_states[ck]
+    int ck = 0, ck_end = 0;
+    int64_t ck_next = -1;
+    if (ck_states) {
+        ck = ck_cu[n];
+        ck_end = ck_cu[n + 1];
+        ck_next = (ck < ck_end) ? ck_pos[ck] : -1;
+    }
     int buf = 0;
     for (int64_t t = bos; t < eos; ++t) {
         // prefetch the next token's vectors into registers
@@ -133,6 +143,18 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
             s[i + 3] = fmaf(k4.w, delta, s[i + 3]);
         }
         store_as(&out[th * dv + j], fmaf(kqs, delta, yj));   // read after write
+        if (ck_next > 0) {
+            const int64_t done = t - bos + 1;
+            while (ck < ck_end && ck_next <= done) {   // positions not on a chunk end are skipped
+                if (ck_next == done && (done % 64 == 0 || t + 1 == eos)) {
+                    const size_t cb = ((size_t)ck * H + h) * DK * dv + j;
+#pragma unroll
+                    for (int i = 0; i < DK; ++i) ck_states[cb + (size_t)i * dv] = s[i];
+                }
+                ++ck;
+                ck_next = (ck < ck_end) ? ck_pos[ck] : -1;
+            }
+        }
 
         if (more) {
             const int nb = buf ^ 1;
@@ -160,7 +182,8 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
     recurrent_prefill_kernel<DK, Tin><<<grid, kCols, 0, st>>>(
         static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
         a.log_alpha, static_cast<const Tin*>(a.beta), a.initial_state, a.cu_seqlens,
-        static_cast<Tin*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.dv);
+        static_cast<Tin*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.dv, a.ckpt_cu,
+        a.ckpt_pos, a.ckpt_states);
     return cudaGetLastError();
 }
 

@@ -114,3 +114,31 @@ def test_valid_call_without_gpu_reports_cuda_error(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert prefill(L, shape()) == _lib.KDA_ERR_CUDA
+
+
+def test_decode_multi_token_argument_rules(L):
+    E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
+    assert decode(L, shape(n=4, T=4 * 17)) == E_UNS         # more than 16 tokens per sequence
+    assert decode(L, shape(n=4, T=0)) == E_ARG
+    assert decode(L, shape(n=4, T=10)) == E_ARG              # not a multiple of num_seqs
+
+
+def test_check_checkpoints_host_rules(L):
+    import numpy as np
+    def chk(cu, ck_cu, ck_pos):
+        cu = np.asarray(cu, dtype=np.int32); a = np.asarray(ck_cu, dtype=np.int32)
+        b = np.asarray(ck_pos or [0], dtype=np.int32)
+        return L.kda_check_checkpoints(cu.ctypes.data, len(cu) - 1, int(cu[-1]), a.ctypes.data, b.ctypes.data)
+    assert chk([0, 200, 264], [0, 3, 4], [64, 128, 200, 64]) == 0
+    assert chk([0, 200], [0, 1], [100]) == _lib.KDA_ERR_INVALID_ARG       # not a chunk end
+    assert chk([0, 200], [0, 2], [128, 64]) == _lib.KDA_ERR_INVALID_ARG   # not increasing
+    assert chk([0, 200], [0, 1], [256]) == _lib.KDA_ERR_INVALID_ARG       # past the end
+    assert chk([0, 200], [0, 0], []) == 0
+
+
+def test_prefill_checkpointed_rejects_null_tables(L):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    sh = shape()
+    args = [ctypes.byref(sh)] + [p(FAKE)] * 5 + [None, None, p(FAKE), None]
+    assert L.kda_prefill_checkpointed(*args, None, p(FAKE), p(FAKE), None) == _lib.KDA_ERR_INVALID_ARG
+    assert L.kda_prefill_checkpointed(*args, p(FAKE), p(FAKE), p(FAKE + 8), None) == _lib.KDA_ERR_UNSUPPORTED

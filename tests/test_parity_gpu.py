@@ -199,3 +199,85 @@ def test_recurrent_and_chunk_paths_agree(monkeypatch):
 
 def test_device_status_is_clean():
     assert kda.kda_device_status() == 0
+
+
+# ---- multi-token decode (T tokens per sequence through the decode path) -------------
+@pytest.mark.parametrize("T", [2, 5, 16])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_multi_token_matches_oracle(T, dtype):
+    n = 24
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, 4, 128, 128, dtype=dtype, seed=30 + T, cu_seqlens=cu,
+                              state_std=0.05).to(DEV)
+    S = w.initial_state.clone()
+    out = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(w)
+    assert rel_l2(np64(out), ro) < TOL[dtype] and rel_l2(np64(S), rf) < TOL[dtype]
+
+
+def test_decode_multi_token_equals_repeated_single_steps():
+    n, T, H = 16, 7, 4
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, H, 128, 128, seed=40, cu_seqlens=cu, state_std=0.05).to(DEV)
+    S_multi = w.initial_state.clone()
+    out_multi = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S_multi)
+    S_step = w.initial_state.clone()
+    rows = torch.arange(n, device=DEV) * T
+    for t in range(T):
+        r = rows + t
+        o_t = kda.kda_decode_step(w.q[r].contiguous(), w.k[r].contiguous(), w.v[r].contiguous(),
+                                  w.log_alpha[r].contiguous(), w.beta[r].contiguous(), S_step)
+        assert torch.equal(o_t, out_multi[r])
+    torch.cuda.synchronize()
+    assert torch.equal(S_step, S_multi)
+
+
+# ---- checkpoint emission during prefill ---------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_checkpoints_equal_prefix_final_states(dtype):
+    lens = [200, 64, 300, 30]
+    cu = workloads.cu_from_lengths(lens)
+    ck = [[64, 128, 200], [64], [192, 256, 300], [30]]
+    w = workloads.make_inputs(cu[-1], 3, 128, 128, dtype=dtype, seed=50, cu_seqlens=cu,
+                              state_std=0.05).to(DEV)
+    out, fin, cks = kda.kda_prefill_checkpointed(w.q, w.k, w.v, w.log_alpha, w.beta, ck,
+                                                 w.initial_state, cu, final_state=True)
+    ref_out, ref_fin = gpu_prefill(w)
+    assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    c = 0
+    for n, positions in enumerate(ck):
+        for p in positions:
+            s, e = cu[n], cu[n] + p
+            _, f = kda.kda_prefill(w.q[s:e], w.k[s:e], w.v[s:e], w.log_alpha[s:e], w.beta[s:e],
+                                   w.initial_state[n:n + 1].contiguous(), None, final_state=True)
+            torch.cuda.synchronize()
+            assert torch.equal(cks[c], f[0]), (n, p)
+            c += 1
+
+
+def test_checkpoint_positions_off_chunk_ends_are_not_written():
+    import ctypes
+    from linear_attention_06_gb300 import _lib
+    lens = [256]
+    w = workloads.make_inputs(256, 2, 128, 128, seed=51, cu_seqlens=[0, 256]).to(DEV)
+    with pytest.raises(kda.KdaError):           # the host validator rejects 100
+        kda.kda_prefill_checkpointed(w.q, w.k, w.v, w.log_alpha, w.beta, [[64, 100]], None, [0, 256])
+    # straight through the C ABI, the device skips the bad position and writes the good one
+    d_cu = torch.tensor([0, 256], dtype=torch.int32, device=DEV)
+    ck_cu = torch.tensor([0, 2], dtype=torch.int32, device=DEV)
+    ck_pos = torch.tensor([100, 128], dtype=torch.int32, device=DEV)
+    cks = torch.full((2, 2, 128, 128), float("nan"), device=DEV)
+    out = torch.empty_like(w.v)
+    shape = _lib.KdaShape(1, 256, 2, 128, 128, _lib.KDA_BF16)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = _lib.lib().kda_prefill_checkpointed(ctypes.byref(shape), p(w.q), p(w.k), p(w.v), p(w.log_alpha),
+                                             p(w.beta), None, p(d_cu), p(out), None, p(ck_cu), p(ck_pos),
+                                             p(cks), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0
+    assert torch.isnan(cks[0]).all()
+    _, f = kda.kda_prefill(w.q[:128], w.k[:128], w.v[:128], w.log_alpha[:128], w.beta[:128], None, None,
+                           final_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(cks[1], f[0])
