@@ -67,8 +67,8 @@ using namespace sm103;
 
 constexpr int C = 64;          // chunk length (tokens)
 constexpr int D = 128;         // dk = dv
-constexpr int kThreads = 384;  // group A: 256 threads, group B: 128 threads
-constexpr int kGroupA = 256, kGroupB = 128;
+constexpr int kThreads = 416;  // group A: 256 threads, group B: 128 threads, one producer warp
+constexpr int kGroupA = 256, kGroupB = 128, kProducer = kGroupA + kGroupB;
 constexpr float kMaxExponent = 60.f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
 constexpr int kBarA = 1, kBarB = 2;                // named barriers of the groups
@@ -107,7 +107,8 @@ struct Small {
     uint64_t ready[2];                           // group A -> B: chunk prepared and W', U computed (2 arrivals)
     uint64_t kbp_free[2];                        // group B -> A: Kb / P / beta / gamma slot free
     uint64_t gram_done, mma1_done, mma2_done;
-    uint64_t wu_done[2];                         // W', U of the chunk in a slot finished (group A refills)
+    uint64_t av_free[2];                         // log_alpha / v slot free (W', U done, or token path)
+    uint64_t qk_free[2];                         // q / k slot free (output product done, or token path)
     uint64_t u_free[2];                          // group B read the output held in a U slot
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
@@ -128,7 +129,9 @@ __device__ __forceinline__ uint32_t half_off(uint32_t r, uint32_t c) {   // V an
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ bool in_group_a() { return threadIdx.x < kGroupA; }
 // Index of the thread inside its group (0..255 in A, 0..127 in B).
-__device__ __forceinline__ int lt() { return in_group_a() ? (int)threadIdx.x : (int)threadIdx.x - kGroupA; }
+__device__ __forceinline__ int lt() {
+    return in_group_a() ? (int)threadIdx.x : (int)threadIdx.x - (threadIdx.x < kProducer ? kGroupA : kProducer);
+}
 // First TMEM lane this warp may access (the warp's lane quarter).
 __device__ __forceinline__ uint32_t lane0() { return ((threadIdx.x >> 5) & 3) * 32; }
 __device__ __forceinline__ int group_count(int id) { return id == kBarA ? kGroupA : kGroupB; }
@@ -511,22 +514,31 @@ __device__ __forceinline__ void o_to_regs(uint32_t tb, uint32_t col, uint32_t (&
     }
 }
 
-// Transpose the held output rows through a 64 x 256-byte staging tile and write
-// them as 16-byte row segments, rows [0, L) only.
+// Transpose the held output rows (lane = column, words = row pairs) through a
+// 64 x 256-byte staging tile and write them as 16-byte row segments, rows
+// [0, L) only.  Neighbouring lanes swap halves so every staging store is a
+// 4-byte column pair; odd rows have their 16-byte chunks shifted by four so the
+// two rows a warp writes at once fall in different banks.
 __device__ void o_store(const uint32_t (&opk)[32], uint8_t* stg, __nv_bfloat16* out, int64_t t0, int H,
                         int h, int L) {
     const int t = lt();
+    const bool odd = t & 1;
+    const int col = t & ~1;                          // first column of the lane pair
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        *reinterpret_cast<uint16_t*>(stg + (2 * i) * 256 + t * 2) = (uint16_t)(opk[i] & 0xffffu);
-        *reinterpret_cast<uint16_t*>(stg + (2 * i + 1) * 256 + t * 2) = (uint16_t)(opk[i] >> 16);
+        const uint32_t mine = opk[i];                // rows 2i (low half) and 2i+1 (high half)
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
+        const uint32_t word = odd ? (got | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
+        const int r = 2 * i + (odd ? 1 : 0);
+        const int chunk = (col >> 3) ^ ((r & 1) << 2);
+        *reinterpret_cast<uint32_t*>(stg + r * 256 + chunk * 16 + (col * 2 & 15)) = word;
     }
     group_sync(kBarB);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         const int id = t + 128 * m, row = id >> 4, ch = id & 15;
         if (row < L) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + ch * 16);
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + (ch ^ ((row & 1) << 2)) * 16);
             *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
         }
     }
@@ -742,11 +754,11 @@ __device__ __forceinline__ void refill(const Ctx& x, const Maps& maps, int c, in
 }
 
 // ============================ group A loop =======================================
-__device__ __noinline__ bool run_group_a(const Ctx& x, const Maps& maps, const __nv_bfloat16* __restrict__ beta) {
+__device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __restrict__ beta) {
     Small& sw = *x.sw;
     const int t = lt();
-    uint32_t gram_ph = 0, wu_ph[2] = {0u, 0u}, u_ph[2] = {0u, 0u};
-    bool ok = true, gram_pending = false, prev_fast = false;
+    uint32_t gram_ph = 0, u_ph[2] = {0u, 0u};
+    bool ok = true, gram_pending = false;
     float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
     for (int n = 0; n < x.nchunks; ++n) {
@@ -766,15 +778,6 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const Maps& maps, const _
 
         if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
         KDA_PHASE(0);
-        // log_alpha and v of chunk n+1 go into the other slot once the W', U products of
-        // chunk n-1 (which read that slot) are done; a token-by-token chunk n-1 is refilled by B
-        if (t == 0 && n >= 1 && prev_fast && n + 1 < x.nchunks) {
-            const int so = s ^ 1;
-            if (mbar_wait_bounded(&sw.wu_done[so], wu_ph[so], kWaitLimitNs)) {
-                wu_ph[so] ^= 1u;
-                refill(x, maps, n + 1, so, true, true, false);
-            }
-        }
         if (t == 0) ++sw.consumed[kLdA][s];
         KDA_PHASE(1);
         if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
@@ -785,7 +788,6 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const Maps& maps, const _
         if (t == 0) ++sw.consumed[kLdQK][s];
         const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s],
                                          reinterpret_cast<float*>(pp));
-        prev_fast = fast;
         if (!fast) {                                     // token-by-token chunk
             if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
             if (t == 0) {
@@ -827,7 +829,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const Maps& maps, const _
             mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
                    smem_u32(aslot + kTT));
             mma_commit(&sw.ready[s]);
-            mma_commit(&sw.wu_done[s]);
+            mma_commit(&sw.av_free[s]);
         }
     }
     if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
@@ -852,8 +854,24 @@ __device__ __forceinline__ void flush_prev(const Ctx& x, __nv_bfloat16* out, int
     if (leader) mbar_arrive(&x.sw->u_free[prev_s]);
 }
 
+// ============================ producer warp ======================================
+// One thread issues every TMA load: chunks 0 and 1 up front, then chunk n into
+// slot n % 2 as soon as that slot's last reader for chunk n-2 is done.
+__device__ __noinline__ void run_producer(const Ctx& x, const Maps& maps) {
+    Small& sw = *x.sw;
+    for (int c = 0; c < 2 && c < x.nchunks; ++c) refill(x, maps, c, c, true, true, true);
+    for (int n = 2; n < x.nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph = ((n - 2) >> 1) & 1;
+        if (!mbar_wait_parked(&sw.av_free[s], ph, kWaitLimitNs)) return;
+        refill(x, maps, n, s, true, true, false);
+        if (!mbar_wait_parked(&sw.qk_free[s], ph, kWaitLimitNs)) return;
+        refill(x, maps, n, s, false, false, true);
+    }
+}
+
 // ============================ group B loop =======================================
-__device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bfloat16* __restrict__ out,
+__device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict__ out,
                             const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
                             const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
     Small& sw = *x.sw;
@@ -869,8 +887,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
     bool have_prev = false;
     int prev_s = 0, prev_L = 0;
     int64_t prev_t0 = 0;
-    if (leader)
-        for (int c = 0; c < 2 && c < x.nchunks; ++c) refill(x, maps, c, c, true, true, true);
     load_state(x.tb, h0, sbase);
     const uint32_t sWT = smem_u32(x.sm + kWT);
     bool ok = true;
@@ -880,7 +896,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         const uint32_t ph = (n >> 1) & 1;
         const int64_t t0 = x.bos + (int64_t)n * C;
         const int L = (int)((x.eos - t0) < C ? (x.eos - t0) : C);
-        const bool more = (n + 2 < x.nchunks);
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* vs = x.sm + kV0 + s * kVBytes;
@@ -901,9 +916,10 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             tc_fence_after();
             ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
             if (leader) {
-                if (more) refill(x, maps, n + 2, s, true, true, true);
                 mbar_arrive(&sw.kbp_free[s]);
                 mbar_arrive(&sw.u_free[s]);              // this chunk left no output in its U slot
+                mbar_arrive(&sw.av_free[s]);
+                mbar_arrive(&sw.qk_free[s]);
             }
             continue;
         }
@@ -928,6 +944,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             mma_state_out(x.tb, tm_u(s), sKB, sQK, sPP);
             mma_commit(&sw.mma2_done);
             mma_commit(&sw.kbp_free[s]);
+            mma_commit(&sw.qk_free[s]);                  // Qhat read by the output product
         }
         mma_pending = true; pending_bar = &sw.mma2_done; pending_ph = m2_ph;
         if (have_prev) {                                 // previous output, under this chunk's MMAs
@@ -938,7 +955,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         m2_ph ^= 1u; mma_pending = false;
         KDA_PHASE(13);
         tc_fence_after();
-        if (leader && more) refill(x, maps, n + 2, s, false, false, true);   // Qhat consumed
         ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
         have_prev = true; prev_s = s; prev_L = L; prev_t0 = t0;
         tc_fence_before();
@@ -988,8 +1004,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         mbar_init(&sw->gram_done, 1);
         mbar_init(&sw->mma1_done, 1);
         mbar_init(&sw->mma2_done, 1);
-        mbar_init(&sw->wu_done[0], 1);
-        mbar_init(&sw->wu_done[1], 1);
+        mbar_init(&sw->av_free[0], 1);
+        mbar_init(&sw->av_free[1], 1);
+        mbar_init(&sw->qk_free[0], 1);
+        mbar_init(&sw->qk_free[1], 1);
         mbar_init(&sw->u_free[0], 1);
         mbar_init(&sw->u_free[1], 1);
         fence_mbar_init();
@@ -1009,7 +1027,13 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     tc_fence_after();
     x.tb = sw->tmem_base;
 
-    const bool ok = in_group_a() ? run_group_a(x, maps, beta) : run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
+    bool ok = true;
+    if (in_group_a())
+        ok = run_group_a(x, beta);
+    else if (tid < kProducer)
+        ok = run_group_b(x, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
+    else if (tid == kProducer)
+        run_producer(x, maps);
     if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
 
     tc_fence_before();
