@@ -98,7 +98,7 @@ __device__ __forceinline__ uint32_t tm_apw(int s) { return 384u + 64u * s; }
 constexpr uint32_t kTmCols = 512;
 
 struct Maps {
-    CUtensorMap q, k, v, a;
+    CUtensorMap q, k, v, a, o;
 };
 
 // Barriers and small per-slot data in the kSmall area.
@@ -545,6 +545,37 @@ __device__ void o_store(const uint32_t (&opk)[32], uint8_t* stg, __nv_bfloat16* 
     group_sync(kBarB);
 }
 
+// A full 64-row output tile: stage it in the 128-byte-swizzled layout of the
+// output tensor map (two halves of 64 rows x 128 B) and hand it to the TMA
+// engine; the caller waits for the bulk read before reusing the tile.  Lane
+// pairs swap halves so every staging store is a 4-byte column pair; in step i
+// the even lane writes row 2i and the odd lane row 2(i^2)+1, whose swizzle
+// phases differ by 5, so the two rows a warp writes at once use disjoint banks.
+__device__ void o_store_tma(const uint32_t (&opk)[32], uint8_t* stg, const Maps& maps, int64_t t0, int h,
+                            bool leader) {
+    const int t = lt();
+    const bool odd = t & 1;
+    const int col = t & ~1;
+    uint8_t* half = stg + (col >> 6) * 8192;
+    const uint32_t cb = (col & 63) * 2;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int j = i ^ 2;
+        const uint32_t send = odd ? (opk[i] & 0xffffu) : (opk[j] >> 16);
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
+        const uint32_t word = odd ? (got | (opk[j] & 0xffff0000u)) : ((opk[i] & 0xffffu) | (got << 16));
+        const int r = odd ? 2 * j + 1 : 2 * i;
+        *reinterpret_cast<uint32_t*>(half + sw128_offset(r, cb)) = word;
+    }
+    fence_proxy_async_smem();
+    group_sync(kBarB);
+    if (leader) {
+        tma_store_3d(&maps.o, 0, h, (int)t0, stg);
+        tma_store_3d(&maps.o, 64, h, (int)t0, stg + 8192);
+        bulk_commit();
+    }
+}
+
 __device__ void load_state(uint32_t tb, const float* h0, size_t base) {
     const int j = lt();
 #pragma unroll 1
@@ -845,12 +876,17 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
 
 // Store the output a chunk left in its U slot (through the staging tile), then
 // release that U slot to group A.
-__device__ __forceinline__ void flush_prev(const Ctx& x, __nv_bfloat16* out, int prev_s, int64_t prev_t0,
-                                           int prev_L, bool leader) {
+__device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_bfloat16* out, int prev_s,
+                                           int64_t prev_t0, int prev_L, bool leader) {
     uint32_t opk[32];
     o_to_regs(x.tb, tm_u(prev_s), opk);
     tc_fence_before();
-    o_store(opk, x.sm + kWT, out, prev_t0, x.H, x.h, prev_L);
+    if (leader) bulk_wait_read();                    // an earlier tile store has read the staging tile
+    group_sync(kBarB);
+    if (prev_L == C)
+        o_store_tma(opk, x.sm + kWT, maps, prev_t0, x.h, leader);
+    else                                             // ragged last chunk: rows [0, L) only
+        o_store(opk, x.sm + kWT, out, prev_t0, x.H, x.h, prev_L);
     if (leader) mbar_arrive(&x.sw->u_free[prev_s]);
 }
 
@@ -871,7 +907,7 @@ __device__ __noinline__ void run_producer(const Ctx& x, const Maps& maps) {
 }
 
 // ============================ group B loop =======================================
-__device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict__ out,
+__device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bfloat16* __restrict__ out,
                             const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
                             const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
     Small& sw = *x.sw;
@@ -907,7 +943,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
             if (have_prev) {
-                flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
+                flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
                 have_prev = false;
             }
             token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], out, t0, x.H, x.h, L);
@@ -925,6 +961,8 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict
         }
         decay_state(x.tb, sw.gam[s]);
         KDA_PHASE(9);
+        if (leader) bulk_wait_read();                    // the staging tile is also the -W'^T tile
+        group_sync(kBarB);
         read_w(x.tb, tm_apw(s), x.sm + kWT);
         group_publish(kBarB);
         KDA_PHASE(10);
@@ -948,7 +986,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict
         }
         mma_pending = true; pending_bar = &sw.mma2_done; pending_ph = m2_ph;
         if (have_prev) {                                 // previous output, under this chunk's MMAs
-            flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
+            flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
             have_prev = false;
         }
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
@@ -963,11 +1001,12 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, __nv_bfloat16* __restrict
         KDA_PHASE(14);
     }
     if (ok) {
-        if (have_prev) flush_prev(x, out, prev_s, prev_t0, prev_L, leader);
+        if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
         if (hT) store_state(x.tb, hT, sbase);
     } else if (mma_pending) {
         mbar_wait_bounded(pending_bar, pending_ph, kWaitLimitNs);
     }
+    if (leader) bulk_wait_all();                     // tile stores complete before the block exits
     return ok;
 }
 
@@ -1015,6 +1054,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
         tma_prefetch_desc(&maps.a);
+        tma_prefetch_desc(&maps.o);
         for (int k = 0; k < 3; ++k)
             for (int s = 0; s < 2; ++s) sw->issued[k][s] = sw->consumed[k][s] = 0;
     }
@@ -1031,7 +1071,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     if (in_group_a())
         ok = run_group_a(x, beta);
     else if (tid < kProducer)
-        ok = run_group_b(x, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
+        ok = run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
     else if (tid == kProducer)
         run_producer(x, maps);
     if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
@@ -1104,7 +1144,9 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
         !make_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.a, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H, 128,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+                  CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map(&maps.o, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
