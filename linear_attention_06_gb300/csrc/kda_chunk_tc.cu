@@ -79,7 +79,7 @@ constexpr uint32_t kV0 = 65536;       // 2 x 16 KB: [v_h0 | v_h1]
 constexpr uint32_t kA0 = 98304;       // 2 x 32 KB: log_alpha fp32 [64][128]; then solve scratch + T
 constexpr uint32_t kKB0 = 163840;     // 2 x 16 KB: Kb [halves]
 constexpr uint32_t kPP0 = 196608;     // 2 x 8 KB: masked P, K-major
-constexpr uint32_t kWT = 212992;      // 16 KB: -W'^T (MN-major), then the output staging tile
+constexpr uint32_t kWT = 212992;      // 16 KB: -W'^T (MN-major), then 4 x 4 KB output staging tiles
 constexpr uint32_t kSmall = 229376;   // 2 KB: barriers, flags, beta, gamma
 constexpr uint32_t kSmemUsed = kSmall + 2048;
 constexpr uint32_t kSmemDynamic = kSmemUsed + 1024;   // + alignment slack = 232448
@@ -109,7 +109,7 @@ struct Small {
     uint64_t gram_done, mma1_done, mma2_done;
     uint64_t av_free[2];                         // log_alpha / v slot free (W', U done, or token path)
     uint64_t qk_free[2];                         // q / k slot free (output product done, or token path)
-    uint64_t u_free[2];                          // group B read the output held in a U slot
+    uint64_t u_free[2];                          // group B read the output held in a U slot (4 warps)
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
     int pad[5];
@@ -117,6 +117,9 @@ struct Small {
     int consumed[3][2];                          //   (kind, slot), to drain after a timeout
     float beta[2][C];
     float gam[2][D];
+#ifdef KDA_PHASE_TIMING
+    unsigned long long phase[24];                // diagnostic build only
+#endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
 
@@ -514,68 +517,6 @@ __device__ __forceinline__ void o_to_regs(uint32_t tb, uint32_t col, uint32_t (&
     }
 }
 
-// Transpose the held output rows (lane = column, words = row pairs) through a
-// 64 x 256-byte staging tile and write them as 16-byte row segments, rows
-// [0, L) only.  Neighbouring lanes swap halves so every staging store is a
-// 4-byte column pair; odd rows have their 16-byte chunks shifted by four so the
-// two rows a warp writes at once fall in different banks.
-__device__ void o_store(const uint32_t (&opk)[32], uint8_t* stg, __nv_bfloat16* out, int64_t t0, int H,
-                        int h, int L) {
-    const int t = lt();
-    const bool odd = t & 1;
-    const int col = t & ~1;                          // first column of the lane pair
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t mine = opk[i];                // rows 2i (low half) and 2i+1 (high half)
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
-        const uint32_t word = odd ? (got | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
-        const int r = 2 * i + (odd ? 1 : 0);
-        const int chunk = (col >> 3) ^ ((r & 1) << 2);
-        *reinterpret_cast<uint32_t*>(stg + r * 256 + chunk * 16 + (col * 2 & 15)) = word;
-    }
-    group_sync(kBarB);
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const int id = t + 128 * m, row = id >> 4, ch = id & 15;
-        if (row < L) {
-            const uint4 val = *reinterpret_cast<const uint4*>(stg + row * 256 + (ch ^ ((row & 1) << 2)) * 16);
-            *reinterpret_cast<uint4*>(out + ((t0 + row) * H + h) * D + ch * 8) = val;
-        }
-    }
-    group_sync(kBarB);
-}
-
-// A full 64-row output tile: stage it in the 128-byte-swizzled layout of the
-// output tensor map (two halves of 64 rows x 128 B) and hand it to the TMA
-// engine; the caller waits for the bulk read before reusing the tile.  Lane
-// pairs swap halves so every staging store is a 4-byte column pair; in step i
-// the even lane writes row 2i and the odd lane row 2(i^2)+1, whose swizzle
-// phases differ by 5, so the two rows a warp writes at once use disjoint banks.
-__device__ void o_store_tma(const uint32_t (&opk)[32], uint8_t* stg, const Maps& maps, int64_t t0, int h,
-                            bool leader) {
-    const int t = lt();
-    const bool odd = t & 1;
-    const int col = t & ~1;
-    uint8_t* half = stg + (col >> 6) * 8192;
-    const uint32_t cb = (col & 63) * 2;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int j = i ^ 2;
-        const uint32_t send = odd ? (opk[i] & 0xffffu) : (opk[j] >> 16);
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 1);
-        const uint32_t word = odd ? (got | (opk[j] & 0xffff0000u)) : ((opk[i] & 0xffffu) | (got << 16));
-        const int r = odd ? 2 * j + 1 : 2 * i;
-        *reinterpret_cast<uint32_t*>(half + sw128_offset(r, cb)) = word;
-    }
-    fence_proxy_async_smem();
-    group_sync(kBarB);
-    if (leader) {
-        tma_store_3d(&maps.o, 0, h, (int)t0, stg);
-        tma_store_3d(&maps.o, 64, h, (int)t0, stg + 8192);
-        bulk_commit();
-    }
-}
-
 __device__ void load_state(uint32_t tb, const float* h0, size_t base) {
     const int j = lt();
 #pragma unroll 1
@@ -702,14 +643,15 @@ __device__ __forceinline__ void mma_state_out(uint32_t tb, uint32_t ocol, uint32
 }
 
 #ifdef KDA_PHASE_TIMING
-// Diagnostic build only: cycles per phase of block 0, group A in slots 0-7
-// (thread 0), group B in slots 8-15 (thread 128).
-__device__ unsigned long long g_phase_cycles[16];
+// Diagnostic build only: cycles per phase, summed over the blocks, as seen by
+// the first thread of each group; accumulated in shared memory and added to
+// the global counters when the block ends.
+__device__ unsigned long long g_phase_cycles[24];
 #define KDA_PHASE(i)                                                                  \
     do {                                                                              \
-        if (blockIdx.x == 0 && lt() == 0) {                                           \
+        if (lt() == 0) {                                                              \
             const long long t_ = clock64();                                           \
-            g_phase_cycles[i] += (unsigned long long)(t_ - phase_t_);                 \
+            x.sw->phase[i] += (unsigned long long)(t_ - phase_t_);                    \
             phase_t_ = t_;                                                            \
         }                                                                             \
     } while (0)
@@ -810,7 +752,6 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
         KDA_PHASE(0);
         if (t == 0) ++sw.consumed[kLdA][s];
-        KDA_PHASE(1);
         if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_PHASE(2);
         if (t < C) sw.beta[s][t] = (t < L) ? braw : 0.f;
@@ -847,6 +788,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         group_sync(kBarA);
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s]);
+        KDA_PHASE(15);
         if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
         // the U slot still holds chunk n-2's output until group B has read it
@@ -862,6 +804,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
             mma_commit(&sw.ready[s]);
             mma_commit(&sw.av_free[s]);
         }
+        KDA_PHASE(1);
     }
     if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
         if (gram_pending) {
@@ -874,20 +817,67 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
     return ok;
 }
 
-// Store the output a chunk left in its U slot (through the staging tile), then
-// release that U slot to group A.
+// Write the held output rows straight to global memory, rows [0, L) only.
+// Lane pairs swap halves so each store is a 4-byte column pair; a warp store
+// covers two 64-byte row segments.
+__device__ __forceinline__ void o_store_direct(const uint32_t (&opk)[32], __nv_bfloat16* __restrict__ out,
+                                               int64_t t0, int H, int h, int L) {
+    const int t = lt();
+    const bool odd = t & 1;
+    const int col = t & ~1;
+    __nv_bfloat16* base = out + ((size_t)t0 * H + h) * D + col;
+    const size_t rs = (size_t)H * D;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t mine = opk[i];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
+        const uint32_t word = odd ? (got | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
+        const int r = 2 * i + (odd ? 1 : 0);
+        if (r < L) __stcs(reinterpret_cast<unsigned int*>(base + (size_t)r * rs), word);
+    }
+}
+
+// Full 64-row tile: each warp stages its 32 value channels (64 B per row,
+// row-major, no swizzle) and issues its own TMA store.  Even lanes write even
+// rows, odd lanes odd rows, so a warp's 32 stores hit 32 distinct banks.
+__device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint8_t* stg_all, const Maps& maps,
+                                                 int64_t t0, int h) {
+    const int t = lt();
+    const int lane = t & 31, wq = t >> 5;
+    const bool odd = t & 1;
+    uint8_t* stg = stg_all + wq * 4096;
+    const uint32_t cb = (uint32_t)(lane & ~1) * 2;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t mine = opk[i];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
+        const uint32_t word = odd ? (got | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
+        const int r = 2 * i + (odd ? 1 : 0);
+        *reinterpret_cast<uint32_t*>(stg + r * 64 + cb) = word;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(&maps.o, 32 * wq, h, (int)t0, stg);
+        bulk_commit();
+        bulk_wait_read();
+    }
+    __syncwarp();
+}
+
+// Store the output a chunk left in its U slot, then release that U slot to
+// group A (one arrival per warp, once its TMEM reads are done).
 __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_bfloat16* out, int prev_s,
                                            int64_t prev_t0, int prev_L, bool leader) {
     uint32_t opk[32];
     o_to_regs(x.tb, tm_u(prev_s), opk);
     tc_fence_before();
-    if (leader) bulk_wait_read();                    // an earlier tile store has read the staging tile
-    group_sync(kBarB);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&x.sw->u_free[prev_s]);
     if (prev_L == C)
-        o_store_tma(opk, x.sm + kWT, maps, prev_t0, x.h, leader);
-    else                                             // ragged last chunk: rows [0, L) only
-        o_store(opk, x.sm + kWT, out, prev_t0, x.H, x.h, prev_L);
-    if (leader) mbar_arrive(&x.sw->u_free[prev_s]);
+        o_store_warp_tma(opk, x.sm + kWT, maps, prev_t0, x.h);
+    else
+        o_store_direct(opk, out, prev_t0, x.H, x.h, prev_L);
 }
 
 // ============================ producer warp ======================================
@@ -953,7 +943,8 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
             if (leader) {
                 mbar_arrive(&sw.kbp_free[s]);
-                mbar_arrive(&sw.u_free[s]);              // this chunk left no output in its U slot
+                for (int w_ = 0; w_ < 4; ++w_)           // no output in this U slot: the four
+                    mbar_arrive(&sw.u_free[s]);          //   per-warp arrivals at once
                 mbar_arrive(&sw.av_free[s]);
                 mbar_arrive(&sw.qk_free[s]);
             }
@@ -961,8 +952,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         }
         decay_state(x.tb, sw.gam[s]);
         KDA_PHASE(9);
-        if (leader) bulk_wait_read();                    // the staging tile is also the -W'^T tile
-        group_sync(kBarB);
         read_w(x.tb, tm_apw(s), x.sm + kWT);
         group_publish(kBarB);
         KDA_PHASE(10);
@@ -989,6 +978,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
             have_prev = false;
         }
+        KDA_PHASE(16);
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
         m2_ph ^= 1u; mma_pending = false;
         KDA_PHASE(13);
@@ -1006,7 +996,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
     } else if (mma_pending) {
         mbar_wait_bounded(pending_bar, pending_ph, kWaitLimitNs);
     }
-    if (leader) bulk_wait_all();                     // tile stores complete before the block exits
+    if ((t & 31) == 0) bulk_wait_all();              // tile stores complete before the block exits
     return ok;
 }
 
@@ -1047,8 +1037,8 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         mbar_init(&sw->av_free[1], 1);
         mbar_init(&sw->qk_free[0], 1);
         mbar_init(&sw->qk_free[1], 1);
-        mbar_init(&sw->u_free[0], 1);
-        mbar_init(&sw->u_free[1], 1);
+        mbar_init(&sw->u_free[0], 4);
+        mbar_init(&sw->u_free[1], 4);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
@@ -1057,6 +1047,9 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         tma_prefetch_desc(&maps.o);
         for (int k = 0; k < 3; ++k)
             for (int s = 0; s < 2; ++s) sw->issued[k][s] = sw->consumed[k][s] = 0;
+#ifdef KDA_PHASE_TIMING
+        for (int i = 0; i < 24; ++i) sw->phase[i] = 0;
+#endif
     }
     if ((tid >> 5) == 0) {
         tmem_alloc(&sw->tmem_base, kTmCols);
@@ -1087,6 +1080,9 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
                     mbar_wait_bounded(&bars[k][s], (uint32_t)(sw->consumed[k][s] & 1), kWaitLimitNs);
     }
     __syncthreads();
+#ifdef KDA_PHASE_TIMING
+    if (tid < 24) atomicAdd(&g_phase_cycles[tid], sw->phase[tid]);
+#endif
     if ((tid >> 5) == 0) tmem_dealloc(x.tb, kTmCols);
 }
 
@@ -1120,10 +1116,10 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 
 #ifdef KDA_PHASE_TIMING
 extern "C" int kda_debug_phase_cycles(unsigned long long* host16, int reset) {
-    if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 16 * sizeof(unsigned long long)) != cudaSuccess)
+    if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 24 * sizeof(unsigned long long)) != cudaSuccess)
         return -1;
     if (reset) {
-        unsigned long long z[16] = {};
+        unsigned long long z[24] = {};
         if (cudaMemcpyToSymbol(g_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
     }
     return 0;
@@ -1145,8 +1141,8 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.a, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.total_tokens, a.H, 128,
                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map(&maps.o, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 64,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&maps.o, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 32,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
