@@ -118,7 +118,7 @@ struct Small {
     float beta[2][C];
     float gam[2][D];
 #ifdef KDA_PHASE_TIMING
-    unsigned long long phase[24];                // diagnostic build only
+    unsigned long long phase[32];                // diagnostic build only
 #endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
@@ -646,7 +646,7 @@ __device__ __forceinline__ void mma_state_out(uint32_t tb, uint32_t ocol, uint32
 // Diagnostic build only: cycles per phase, summed over the blocks, as seen by
 // the first thread of each group; accumulated in shared memory and added to
 // the global counters when the block ends.
-__device__ unsigned long long g_phase_cycles[24];
+__device__ unsigned long long g_phase_cycles[32];
 #define KDA_PHASE(i)                                                                  \
     do {                                                                              \
         if (lt() == 0) {                                                              \
@@ -656,7 +656,14 @@ __device__ unsigned long long g_phase_cycles[24];
         }                                                                             \
     } while (0)
 #define KDA_PHASE_INIT long long phase_t_ = clock64()
+// Event trace of block 0: the clock at named points of chunk n.
+__device__ long long g_trace[128][16];
+#define KDA_TRACE(n, ev)                                                              \
+    do {                                                                              \
+        if (blockIdx.x == 0 && lt() == 0 && (n) < 128) g_trace[(n)][(ev)] = clock64(); \
+    } while (0)
 #else
+#define KDA_TRACE(n, ev) do {} while (0)
 #define KDA_PHASE(i) do {} while (0)
 #define KDA_PHASE_INIT do {} while (0)
 #endif
@@ -726,11 +733,26 @@ __device__ __forceinline__ void refill(const Ctx& x, const Maps& maps, int c, in
     if (q) { load_qk(x.sm + kQK0 + s * kQKBytes, maps, x.h, tc, &sw.qk_full[s]); ++sw.issued[kLdQK][s]; }
 }
 
+// Warm L2 with chunk c's tiles, so that its loads, issued once their ring slots
+// free up, find the data close by.
+__device__ __forceinline__ void prefetch_chunk(const Ctx& x, const Maps& maps, int c) {
+    if (c >= x.nchunks) return;
+    const int tc = (int)(x.bos + (int64_t)c * C);
+    tma_prefetch_l2_3d(&maps.a, 0, x.h, tc);
+    tma_prefetch_l2_3d(&maps.v, 0, x.h, tc);
+    tma_prefetch_l2_3d(&maps.v, 64, x.h, tc);
+    tma_prefetch_l2_3d(&maps.k, 0, x.h, tc);
+    tma_prefetch_l2_3d(&maps.k, 64, x.h, tc);
+    tma_prefetch_l2_3d(&maps.q, 0, x.h, tc);
+    tma_prefetch_l2_3d(&maps.q, 64, x.h, tc);
+}
+
 // ============================ group A loop =======================================
-__device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __restrict__ beta) {
+__device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* __restrict__ beta) {
+    const Ctx x = x_in;
     Small& sw = *x.sw;
     const int t = lt();
-    uint32_t gram_ph = 0, u_ph[2] = {0u, 0u};
+    uint32_t gram_ph = 0, u_ph0 = 0, u_ph1 = 0;     // u_free parities of slots 0 and 1
     bool ok = true, gram_pending = false;
     float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
@@ -749,13 +771,17 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         uint8_t* kb = x.sm + kKB0 + s * 16384;
         uint8_t* pp = x.sm + kPP0 + s * 8192;
 
+        KDA_TRACE(n, 2);
         if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
+        KDA_TRACE(n, 3);
         KDA_PHASE(0);
         if (t == 0) ++sw.consumed[kLdA][s];
         if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
+        KDA_TRACE(n, 4);
         KDA_PHASE(2);
         if (t < C) sw.beta[s][t] = (t < L) ? braw : 0.f;
         if (!(ok = group_wait(kBarA, &sw.qk_full[s], ph))) break;
+        KDA_TRACE(n, 5);
         KDA_PHASE(3);
         if (t == 0) ++sw.consumed[kLdQK][s];
         const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s],
@@ -774,10 +800,12 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         KDA_PHASE(4);
         if (t == 0) {
             mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
+            KDA_PHASE(25);
             mma_commit(&sw.gram_done);
         }
         gram_pending = true;
         if (!(ok = group_wait(kBarA, &sw.gram_done, gram_ph))) break;
+        KDA_TRACE(n, 6);
         gram_ph ^= 1u;
         gram_pending = false;
         KDA_PHASE(5);
@@ -789,11 +817,16 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s]);
         KDA_PHASE(15);
+        KDA_TRACE(n, 7);
         if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
         // the U slot still holds chunk n-2's output until group B has read it
-        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], u_ph[s]))) break;
-        if (n >= 2) u_ph[s] ^= 1u;
+        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], s ? u_ph1 : u_ph0))) break;
+        KDA_TRACE(n, 8);
+        if (n >= 2) {
+            if (s) u_ph1 ^= 1u;
+            else u_ph0 ^= 1u;
+        }
         group_publish(kBarA);
         KDA_PHASE(7);
         if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival
@@ -801,9 +834,11 @@ __device__ __noinline__ bool run_group_a(const Ctx& x, const __nv_bfloat16* __re
             mbar_arrive(&sw.ready[s]);
             mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
                    smem_u32(aslot + kTT));
+            KDA_PHASE(23);
             mma_commit(&sw.ready[s]);
             mma_commit(&sw.av_free[s]);
         }
+        KDA_TRACE(n, 9);
         KDA_PHASE(1);
     }
     if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
@@ -882,24 +917,37 @@ __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_
 
 // ============================ producer warp ======================================
 // One thread issues every TMA load: chunks 0 and 1 up front, then chunk n into
-// slot n % 2 as soon as that slot's last reader for chunk n-2 is done.
-__device__ __noinline__ void run_producer(const Ctx& x, const Maps& maps) {
+// slot n % 2 as soon as that slot's last reader for chunk n-2 is done.  Each
+// chunk is prefetched into L2 two chunks ahead of its loads.
+__device__ __noinline__ void run_producer(const Ctx& x_in, const Maps& maps) {
+    const Ctx x = x_in;
     Small& sw = *x.sw;
     for (int c = 0; c < 2 && c < x.nchunks; ++c) refill(x, maps, c, c, true, true, true);
+    prefetch_chunk(x, maps, 2);
+    prefetch_chunk(x, maps, 3);
+    KDA_PHASE_INIT;
     for (int n = 2; n < x.nchunks; ++n) {
         const int s = n & 1;
         const uint32_t ph = ((n - 2) >> 1) & 1;
         if (!mbar_wait_parked(&sw.av_free[s], ph, kWaitLimitNs)) return;
+        KDA_PHASE(18);
         refill(x, maps, n, s, true, true, false);
+        KDA_TRACE(n, 0);
+        KDA_PHASE(19);
         if (!mbar_wait_parked(&sw.qk_free[s], ph, kWaitLimitNs)) return;
+        KDA_PHASE(20);
         refill(x, maps, n, s, false, false, true);
+        KDA_TRACE(n, 1);
+        prefetch_chunk(x, maps, n + 2);
+        KDA_PHASE(21);
     }
 }
 
 // ============================ group B loop =======================================
-__device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bfloat16* __restrict__ out,
+__device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv_bfloat16* __restrict__ out,
                             const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
                             const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
+    const Ctx x = x_in;
     Small& sw = *x.sw;
     Ckpt ck;
     ck.init(ck_cu, ck_pos, ck_states, x.seq);
@@ -929,6 +977,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
                        sPP = smem_u32(x.sm + kPP0 + s * 8192);
 
         if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
+        KDA_TRACE(n, 10);
         KDA_PHASE(8);
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
@@ -957,10 +1006,12 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         KDA_PHASE(10);
         if (leader) {
             mma_delta(x.tb, tm_u(s), sWT);
+            KDA_PHASE(24);
             mma_commit(&sw.mma1_done);
         }
         mma_pending = true; pending_bar = &sw.mma1_done; pending_ph = m1_ph;
         if (!(ok = group_wait(kBarB, &sw.mma1_done, m1_ph))) break;
+        KDA_TRACE(n, 11);
         m1_ph ^= 1u; mma_pending = false;
         KDA_PHASE(11);
         tc_fence_after();
@@ -969,6 +1020,8 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         KDA_PHASE(12);
         if (leader) {
             mma_state_out(x.tb, tm_u(s), sKB, sQK, sPP);
+            KDA_PHASE(22);
+            KDA_TRACE(n, 12);
             mma_commit(&sw.mma2_done);
             mma_commit(&sw.kbp_free[s]);
             mma_commit(&sw.qk_free[s]);                  // Qhat read by the output product
@@ -979,7 +1032,9 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
             have_prev = false;
         }
         KDA_PHASE(16);
+        KDA_TRACE(n, 13);
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
+        KDA_TRACE(n, 14);
         m2_ph ^= 1u; mma_pending = false;
         KDA_PHASE(13);
         tc_fence_after();
@@ -989,6 +1044,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x, const Maps& maps, __nv_bf
         group_sync(kBarB);
         tc_fence_after();
         KDA_PHASE(14);
+        KDA_TRACE(n, 15);
     }
     if (ok) {
         if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
@@ -1048,7 +1104,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         for (int k = 0; k < 3; ++k)
             for (int s = 0; s < 2; ++s) sw->issued[k][s] = sw->consumed[k][s] = 0;
 #ifdef KDA_PHASE_TIMING
-        for (int i = 0; i < 24; ++i) sw->phase[i] = 0;
+        for (int i = 0; i < 32; ++i) sw->phase[i] = 0;
 #endif
     }
     if ((tid >> 5) == 0) {
@@ -1081,7 +1137,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     }
     __syncthreads();
 #ifdef KDA_PHASE_TIMING
-    if (tid < 24) atomicAdd(&g_phase_cycles[tid], sw->phase[tid]);
+    if (tid < 32) atomicAdd(&g_phase_cycles[tid], sw->phase[tid]);
 #endif
     if ((tid >> 5) == 0) tmem_dealloc(x.tb, kTmCols);
 }
@@ -1115,11 +1171,14 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 }  // namespace
 
 #ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_trace(long long* host2048) {
+    return cudaMemcpyFromSymbol(host2048, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
 extern "C" int kda_debug_phase_cycles(unsigned long long* host16, int reset) {
-    if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 24 * sizeof(unsigned long long)) != cudaSuccess)
+    if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 32 * sizeof(unsigned long long)) != cudaSuccess)
         return -1;
     if (reset) {
-        unsigned long long z[24] = {};
+        unsigned long long z[32] = {};
         if (cudaMemcpyToSymbol(g_phase_cycles, z, sizeof(z)) != cudaSuccess) return -1;
     }
     return 0;
