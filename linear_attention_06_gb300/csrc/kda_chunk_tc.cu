@@ -752,7 +752,7 @@ __device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* _
     const Ctx x = x_in;
     Small& sw = *x.sw;
     const int t = lt();
-    uint32_t gram_ph = 0, u_ph0 = 0, u_ph1 = 0;     // u_free parities of slots 0 and 1
+    uint32_t gram_ph = 0;
     bool ok = true, gram_pending = false;
     float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
@@ -820,13 +820,10 @@ __device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* _
         KDA_TRACE(n, 7);
         if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
-        // the U slot still holds chunk n-2's output until group B has read it
-        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], s ? u_ph1 : u_ph0))) break;
+        // the U slot still holds chunk n-2's output until group B has read it (every chunk,
+        // tensor-core or token-by-token, completes one phase of its slot's u_free)
+        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_TRACE(n, 8);
-        if (n >= 2) {
-            if (s) u_ph1 ^= 1u;
-            else u_ph0 ^= 1u;
-        }
         group_publish(kBarA);
         KDA_PHASE(7);
         if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival

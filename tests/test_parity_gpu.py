@@ -99,6 +99,18 @@ def test_extreme_decay_and_beta(mode):
     compare_prefill(w)
 
 
+@pytest.mark.parametrize("token_chunk", [2, 3, 5])
+def test_token_chunk_between_tensor_core_chunks(token_chunk):
+    # One chunk whose decay leaves the tensor-core range (a -inf gate) in the middle of
+    # a run of ordinary chunks: the slots it shares with later chunks must be handed
+    # back in order.
+    T = 8 * 64
+    w = workloads.make_inputs(T, 2, 128, 128, dtype=torch.bfloat16, seed=31, cu_seqlens=[0, T],
+                              state_std=0.05).to(DEV)
+    w.log_alpha[64 * token_chunk + 17, :, ::5] = float("-inf")
+    compare_prefill(w)
+
+
 # ---- full-size workloads, sampled heads ---------------------------------------------
 def test_prefill_bf16_full_size_sampled_heads():
     w = workloads.prefill_bf16(device=DEV)
