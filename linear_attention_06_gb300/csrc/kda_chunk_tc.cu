@@ -36,15 +36,19 @@
 // on the state held in tensor memory (exact for any log_alpha <= 0, -inf
 // included); the K3-shaped inputs never need it.
 //
-// Work layout.  One CTA of 384 threads per (sequence, head) walks the
-// sequence's chunks in order, in two warp-specialised groups:
+// Work layout.  One CTA of 448 threads per (sequence, head) walks the
+// sequence's chunks in order, in warp-specialised roles:
 //   group A (warps 0-7) prepares chunk n+1 while group B (warps 8-11) runs the
 //   state recurrence for chunk n.
 //   A: decay-range check, Khat / Qhat / Kb tiles, the Gram product [Khat;Qhat]
-//      Kb^T, N = Diag(beta) L(A) and the masked P, the UT solve T.
-//   B: W'^T = Khat^T T^T and U^T = V^T T^T, the decayed state Ss and its bf16
-//      copy, Delta^T = U^T - Ss^T W'^T, O^T = Ss^T Qhat^T + Delta^T P^T,
-//      S^T += Delta^T Kb, the output store, and the TMA loads of chunk n+2.
+//      Kb^T, N = Diag(beta) L(A) and the masked P, the UT solve T, and
+//      W'^T = Khat^T T^T and U^T = V^T T^T.
+//   B: the decayed state Ss and its bf16 copy, Delta^T = U^T - Ss^T W'^T, the
+//      packed Delta, the output store (one TMA store per warp) and the final
+//      state.
+//   state/output issuer (warp 13): S^T += Delta^T Kb and O^T = Ss^T Qhat^T +
+//      Delta^T P^T, issued while group B stores the previous chunk's output.
+//   producer (warp 12): every TMA load, and L2 prefetches two chunks ahead.
 // q/k, v and log_alpha have separate two-slot rings, each refilled as soon as
 // its last reader is done.  Matrices that land in TMEM put a 128-wide
 // dimension on the 128 lanes (M = 128 everywhere); the state lives in TMEM as
@@ -67,8 +71,10 @@ using namespace sm103;
 
 constexpr int C = 64;          // chunk length (tokens)
 constexpr int D = 128;         // dk = dv
-constexpr int kThreads = 416;  // group A: 256 threads, group B: 128 threads, one producer warp
-constexpr int kGroupA = 256, kGroupB = 128, kProducer = kGroupA + kGroupB;
+// group A: 256 threads, group B: 128 threads, then two single-thread warps: the TMA
+// producer and the issuer of the state/output products
+constexpr int kThreads = 448;
+constexpr int kGroupA = 256, kGroupB = 128, kProducer = kGroupA + kGroupB, kIssuerOut = kProducer + 32;
 constexpr float kMaxExponent = 60.f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
 constexpr int kBarA = 1, kBarB = 2;                // named barriers of the groups
@@ -110,9 +116,11 @@ struct Small {
     uint64_t av_free[2];                         // log_alpha / v slot free (W', U done, or token path)
     uint64_t qk_free[2];                         // q / k slot free (output product done, or token path)
     uint64_t u_free[2];                          // group B read the output held in a U slot (4 warps)
+    uint64_t packed;                             // group B -> state/output issuer: Delta packed (slot in cmd_b)
+    uint64_t drain;                              // state/output issuer: its products landed (at exit)
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
-    int pad[5];
+    int cmd_b;                                   // slot of the packed chunk, -1: group B is done
     int issued[3][2];                            // TMA loads issued / waited for, per
     int consumed[3][2];                          //   (kind, slot), to drain after a timeout
     float beta[2][C];
@@ -131,9 +139,10 @@ __device__ __forceinline__ uint32_t half_off(uint32_t r, uint32_t c) {   // V an
 }
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ bool in_group_a() { return threadIdx.x < kGroupA; }
-// Index of the thread inside its group (0..255 in A, 0..127 in B).
+// Index of the thread inside its group (0..255 in A, 0..127 in B, the lane in the single-thread warps).
 __device__ __forceinline__ int lt() {
-    return in_group_a() ? (int)threadIdx.x : (int)threadIdx.x - (threadIdx.x < kProducer ? kGroupA : kProducer);
+    return in_group_a() ? (int)threadIdx.x
+                        : (threadIdx.x < kProducer ? (int)threadIdx.x - kGroupA : (int)(threadIdx.x & 31));
 }
 // First TMEM lane this warp may access (the warp's lane quarter).
 __device__ __forceinline__ uint32_t lane0() { return ((threadIdx.x >> 5) & 3) * 32; }
@@ -849,6 +858,36 @@ __device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* _
     return ok;
 }
 
+// ============================ state/output issuer ================================
+// One thread: for each chunk whose Delta group B has packed (slot in cmd_b),
+// S^T += Delta^T Kb and O^T = Ss^T Qhat^T + Delta^T P^T, committed to mma2_done
+// and to the Kb/P and q/k slot releases.  Group B publishes the next slot only
+// after mma2_done, so cmd_b is read before it changes; -1 ends the loop.
+__device__ __noinline__ bool run_out_issuer(const Ctx& x_in) {
+    const Ctx x = x_in;
+    Small& sw = *x.sw;
+    bool ok = true, issued = false;
+    uint32_t ph = 0;
+    for (;;) {
+        if (!(ok = mbar_wait_parked(&sw.packed, ph, kWaitLimitNs))) break;
+        ph ^= 1u;
+        const int s = sw.cmd_b;
+        if (s < 0) break;
+        tc_fence_after();
+        mma_state_out(x.tb, tm_u(s), smem_u32(x.sm + kKB0 + s * 16384), smem_u32(x.sm + kQK0 + s * kQKBytes),
+                      smem_u32(x.sm + kPP0 + s * 8192));
+        mma_commit(&sw.mma2_done);
+        mma_commit(&sw.kbp_free[s]);
+        mma_commit(&sw.qk_free[s]);                      // Qhat read by the output product
+        issued = true;
+    }
+    if (issued) {          // let this thread's products land before TMEM is freed (bounded)
+        mma_commit(&sw.drain);
+        mbar_wait_bounded(&sw.drain, 0, kWaitLimitNs);
+    }
+    return ok;
+}
+
 // Write the held output rows straight to global memory, rows [0, L) only.
 // Lane pairs swap halves so each store is a 4-byte column pair; a warp store
 // covers two 64-byte row segments.
@@ -951,9 +990,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     const int t = lt();
     const bool leader = (t == 0);
     uint32_t m1_ph = 0, m2_ph = 0;
-    bool mma_pending = false;
-    uint64_t* pending_bar = nullptr;
-    uint32_t pending_ph = 0;
+    bool mma1_pending = false;
     // the previous chunk's output waits in its U slot until the next Delta product is in flight
     bool have_prev = false;
     int prev_s = 0, prev_L = 0;
@@ -970,8 +1007,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* vs = x.sm + kV0 + s * kVBytes;
-        const uint32_t sQK = smem_u32(qk), sKB = smem_u32(x.sm + kKB0 + s * 16384),
-                       sPP = smem_u32(x.sm + kPP0 + s * 8192);
 
         if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
         KDA_TRACE(n, 10);
@@ -1006,24 +1041,21 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
             KDA_PHASE(24);
             mma_commit(&sw.mma1_done);
         }
-        mma_pending = true; pending_bar = &sw.mma1_done; pending_ph = m1_ph;
+        mma1_pending = true;
         if (!(ok = group_wait(kBarB, &sw.mma1_done, m1_ph))) break;
         KDA_TRACE(n, 11);
-        m1_ph ^= 1u; mma_pending = false;
+        m1_ph ^= 1u; mma1_pending = false;
         KDA_PHASE(11);
         tc_fence_after();
         pack_delta(x.tb, tm_u(s));
         group_publish(kBarB);
         KDA_PHASE(12);
-        if (leader) {
-            mma_state_out(x.tb, tm_u(s), sKB, sQK, sPP);
-            KDA_PHASE(22);
-            KDA_TRACE(n, 12);
-            mma_commit(&sw.mma2_done);
-            mma_commit(&sw.kbp_free[s]);
-            mma_commit(&sw.qk_free[s]);                  // Qhat read by the output product
+        if (leader) {                                    // the state/output issuer takes it from here
+            sw.cmd_b = s;
+            mbar_arrive(&sw.packed);
         }
-        mma_pending = true; pending_bar = &sw.mma2_done; pending_ph = m2_ph;
+        KDA_PHASE(22);
+        KDA_TRACE(n, 12);
         if (have_prev) {                                 // previous output, under this chunk's MMAs
             flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
             have_prev = false;
@@ -1032,7 +1064,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         KDA_TRACE(n, 13);
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
         KDA_TRACE(n, 14);
-        m2_ph ^= 1u; mma_pending = false;
+        m2_ph ^= 1u;
         KDA_PHASE(13);
         tc_fence_after();
         ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
@@ -1046,8 +1078,12 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     if (ok) {
         if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
         if (hT) store_state(x.tb, hT, sbase);
-    } else if (mma_pending) {
-        mbar_wait_bounded(pending_bar, pending_ph, kWaitLimitNs);
+    } else if (mma1_pending) {
+        mbar_wait_bounded(&sw.mma1_done, m1_ph, kWaitLimitNs);
+    }
+    if (leader) {                                    // end of the state/output issuer's loop
+        sw.cmd_b = -1;
+        mbar_arrive(&sw.packed);
     }
     if ((t & 31) == 0) bulk_wait_all();              // tile stores complete before the block exits
     return ok;
@@ -1092,6 +1128,8 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         mbar_init(&sw->qk_free[1], 1);
         mbar_init(&sw->u_free[0], 4);
         mbar_init(&sw->u_free[1], 4);
+        mbar_init(&sw->packed, 1);
+        mbar_init(&sw->drain, 1);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
@@ -1120,6 +1158,9 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         ok = run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
     else if (tid == kProducer)
         run_producer(x, maps);
+
+    else if (tid == kIssuerOut)
+        ok = run_out_issuer(x);
     if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
 
     tc_fence_before();
