@@ -37,17 +37,16 @@
 // included); the K3-shaped inputs never need it.
 //
 // Work layout.  One CTA of 448 threads per (sequence, head) walks the
-// sequence's chunks in order, in warp-specialised roles:
-//   group A (warps 0-7) prepares chunk n+1 while group B (warps 8-11) runs the
-//   state recurrence for chunk n.
-//   A: decay-range check, Khat / Qhat / Kb tiles, the Gram product [Khat;Qhat]
-//      Kb^T, N = Diag(beta) L(A) and the masked P, the UT solve T, and
-//      W'^T = Khat^T T^T and U^T = V^T T^T.
-//   B: the decayed state Ss and its bf16 copy, Delta^T = U^T - Ss^T W'^T, the
-//      packed Delta, the output store (one TMA store per warp) and the final
-//      state.
+// sequence's chunks in order, in warp-specialised roles that form a pipeline:
+//   team P (warps 0-3): decay-range check, Khat / Qhat / Kb tiles and the Gram
+//      product [Khat;Qhat] Kb^T of chunk n+2,
+//   team S (warps 4-7): N = Diag(beta) L(A) and the masked P, the UT solve T,
+//      and W'^T = Khat^T T^T, U^T = V^T T^T of chunk n+1,
+//   group B (warps 8-11): for chunk n the decayed state Ss and its bf16 copy,
+//      Delta^T = U^T - Ss^T W'^T, the packed Delta, the output store (one TMA
+//      store per warp) and the final state,
 //   state/output issuer (warp 13): S^T += Delta^T Kb and O^T = Ss^T Qhat^T +
-//      Delta^T P^T, issued while group B stores the previous chunk's output.
+//      Delta^T P^T, issued while group B stores the previous chunk's output,
 //   producer (warp 12): every TMA load, and L2 prefetches two chunks ahead.
 // q/k, v and log_alpha have separate two-slot rings, each refilled as soon as
 // its last reader is done.  Matrices that land in TMEM put a 128-wide
@@ -71,13 +70,15 @@ using namespace sm103;
 
 constexpr int C = 64;          // chunk length (tokens)
 constexpr int D = 128;         // dk = dv
-// group A: 256 threads, group B: 128 threads, then two single-thread warps: the TMA
-// producer and the issuer of the state/output products
+// group A: two teams of 128 threads (P: operands and Gram, S: UT solve and W'/U), group B:
+// 128 threads, then two single-thread warps: the TMA producer and the issuer of the
+// state/output products
 constexpr int kThreads = 448;
-constexpr int kGroupA = 256, kGroupB = 128, kProducer = kGroupA + kGroupB, kIssuerOut = kProducer + 32;
+constexpr int kTeam = 128, kGroupA = 2 * kTeam, kGroupB = 128, kProducer = kGroupA + kGroupB,
+              kIssuerOut = kProducer + 32;
 constexpr float kMaxExponent = 60.f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
-constexpr int kBarA = 1, kBarB = 2;                // named barriers of the groups
+constexpr int kBarP = 1, kBarB = 2, kBarS = 3;      // named barriers of the 128-thread groups
 
 // ---- dynamic shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t kQK0 = 0;          // 2 x 32 KB: [k_h0 | q_h0 | k_h1 | q_h1], 64 rows x 128 B, SW128
@@ -111,13 +112,14 @@ struct Maps {
 struct Small {
     uint64_t qk_full[2], v_full[2], a_full[2];   // TMA completions
     uint64_t ready[2];                           // group A -> B: chunk prepared and W', U computed (2 arrivals)
-    uint64_t kbp_free[2];                        // group B -> A: Kb / P / beta / gamma slot free
-    uint64_t gram_done, mma1_done, mma2_done;
+    uint64_t kbp_free[2];                        // state product -> team P: Kb / P / beta / gamma slot free
+    uint64_t gram_done[2];                       // team P -> team S: Gram product landed (or token chunk)
+    uint64_t mma1_done, mma2_done;
     uint64_t av_free[2];                         // log_alpha / v slot free (W', U done, or token path)
     uint64_t qk_free[2];                         // q / k slot free (output product done, or token path)
     uint64_t u_free[2];                          // group B read the output held in a U slot (4 warps)
     uint64_t packed;                             // group B -> state/output issuer: Delta packed (slot in cmd_b)
-    uint64_t drain;                              // state/output issuer: its products landed (at exit)
+    uint64_t drain, drain_p, drain_s;            // issuing threads: their products landed (at exit)
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
     int cmd_b;                                   // slot of the packed chunk, -1: group B is done
@@ -139,14 +141,15 @@ __device__ __forceinline__ uint32_t half_off(uint32_t r, uint32_t c) {   // V an
 }
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ bool in_group_a() { return threadIdx.x < kGroupA; }
-// Index of the thread inside its group (0..255 in A, 0..127 in B, the lane in the single-thread warps).
+__device__ __forceinline__ bool in_team_p() { return threadIdx.x < kTeam; }
+// Index of the thread inside its group (0..127 in teams P and S and in B, the lane in the
+// single-thread warps).
 __device__ __forceinline__ int lt() {
-    return in_group_a() ? (int)threadIdx.x
-                        : (threadIdx.x < kProducer ? (int)threadIdx.x - kGroupA : (int)(threadIdx.x & 31));
+    return threadIdx.x < kProducer ? (int)(threadIdx.x & 127) : (int)(threadIdx.x & 31);
 }
 // First TMEM lane this warp may access (the warp's lane quarter).
 __device__ __forceinline__ uint32_t lane0() { return ((threadIdx.x >> 5) & 3) * 32; }
-__device__ __forceinline__ int group_count(int id) { return id == kBarA ? kGroupA : kGroupB; }
+__device__ __forceinline__ int group_count(int) { return kTeam; }
 
 __device__ __forceinline__ void group_sync(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(group_count(id)) : "memory");
@@ -206,38 +209,33 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
 
 // ============================ group A: chunk-local stage =========================
 
-// Pass 1 (thread = key channel c and row half): suffix sums of log_alpha, written back in place
-// over the A slot as e[r][c] = sum_{r<t<L} a[t][c]; returns false when a channel's chunk total
-// leaves +-kMaxExponent.  gam[c] = e^{G_c}.  Pass 2 (thread = 16-byte chunk of 8 channels of one
-// row): Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector accesses.
-__device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float* gam, float* xchg) {
-    const int a = lt(), c = a & 127, hf = a >> 7;
-    float e[32];
+// Pass 1 (thread = key channel c): suffix sums of log_alpha over the chunk,
+// e[r][c] = sum_{r<t<L} a[t][c]; returns false (leaving log_alpha untouched) when a
+// channel's chunk total leaves +-kMaxExponent, else writes e back in place and
+// gam[c] = e^{G_c}.  Pass 2 (thread = 16-byte chunk of 8 channels of one row):
+// Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector
+// accesses.  Team P (128 threads).
+__device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float* gam) {
+    const int c = lt();
+    float e[C];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = 32 * hf + i;
-        e[i] = (r < L) ? A[r * D + c] : 0.f;
-    }
+    for (int r = 0; r < C; ++r) e[r] = (r < L) ? A[r * D + c] : 0.f;
     float run = 0.f;
 #pragma unroll
-    for (int i = 31; i >= 0; --i) {
-        const float ar = e[i];
-        e[i] = run;
+    for (int r = C - 1; r >= 0; --r) {
+        const float ar = e[r];
+        e[r] = run;
         run += ar;
     }
-    if (hf == 1) xchg[c] = run;
-    group_sync(kBarA);
-    const float off = (hf == 0) ? xchg[c] : 0.f;
-    const float total = run + off;
-    if (group_or(kBarA, hf == 0 && !(fabsf(total) <= kMaxExponent))) return false;
-    if (hf == 0) gam[c] = __expf(total);
+    if (group_or(kBarP, !(fabsf(run) <= kMaxExponent))) return false;
+    gam[c] = __expf(run);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) A[(32 * hf + i) * D + c] = e[i] + off;
-    group_sync(kBarA);
-    // pass 2: 64 rows x 16 chunks = 1024 units, 4 per thread
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int u = a + 256 * m, r = u >> 4, j = u & 15;
+    for (int r = 0; r < C; ++r) A[r * D + c] = e[r];
+    group_sync(kBarP);
+    // pass 2: 64 rows x 16 chunks = 1024 units, 8 per thread
+#pragma unroll 2
+    for (int m = 0; m < 8; ++m) {
+        const int u = c + kTeam * m, r = u >> 4, j = u & 15;
         const uint32_t ko = qk_off(false, r, 8 * j), qo = qk_off(true, r, 8 * j), bo = half_off(r, 8 * j);
         uint4 kh = make_uint4(0u, 0u, 0u, 0u), qh = kh, kbv = kh;
         if (r < L) {
@@ -276,48 +274,50 @@ __device__ __forceinline__ float* blk(float* base, int i, int j) {
 
 // TMEM lanes 0-63 hold A rows r: N = beta_r A_rs (s < r) as fp32
 // lower-triangular 16x16 blocks in the A slot.  Lanes 64-127 hold P rows r:
-// P_rs (s <= r) as the bf16 K-major operand tile.  Warps 0-3 of group A read
-// columns 0-31, warps 4-7 columns 32-63 of the same lanes.
+// P_rs (s <= r) as the bf16 K-major operand tile.  Team S: each thread takes
+// its lane's row, columns 0-31 then 32-63.
 __device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp, const float* beta) {
-    const int a = lt(), ch = (a >> 7);               // column half
-    const int row = (int)lane0() + (a & 31);
-    uint32_t v[32];
-    tmem_ld32(tmem_addr(tb, lane0(), col + 32 * ch), v);
-    tmem_wait_ld();
-    if (row < 64) {
-        const int r = row, bi = r >> 4, rr = r & 15;
-        const float b = beta[r];
-        float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
+    const int row = (int)lane0() + (lt() & 31);
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch) {                 // column half
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tb, lane0(), col + 32 * ch), v);
+        tmem_wait_ld();
+        if (row < 64) {
+            const int r = row, bi = r >> 4, rr = r & 15;
+            const float b = beta[r];
+            float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int bj = 2 * ch + k;
-            if (bj > bi) break;
-            float* dst = blk(Nb, bi, bj) + rr * kBlkStride;
+            for (int k = 0; k < 2; ++k) {
+                const int bj = 2 * ch + k;
+                if (bj > bi) break;
+                float* dst = blk(Nb, bi, bj) + rr * kBlkStride;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int s0 = 16 * bj + 4 * q4, i0 = 16 * k + 4 * q4;
-                float4 f;
-                f.x = (s0 + 0 < r) ? b * __uint_as_float(v[i0 + 0]) : 0.f;
-                f.y = (s0 + 1 < r) ? b * __uint_as_float(v[i0 + 1]) : 0.f;
-                f.z = (s0 + 2 < r) ? b * __uint_as_float(v[i0 + 2]) : 0.f;
-                f.w = (s0 + 3 < r) ? b * __uint_as_float(v[i0 + 3]) : 0.f;
-                *reinterpret_cast<float4*>(dst + 4 * q4) = f;
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int s0 = 16 * bj + 4 * q4, i0 = 16 * k + 4 * q4;
+                    float4 f;
+                    f.x = (s0 + 0 < r) ? b * __uint_as_float(v[i0 + 0]) : 0.f;
+                    f.y = (s0 + 1 < r) ? b * __uint_as_float(v[i0 + 1]) : 0.f;
+                    f.z = (s0 + 2 < r) ? b * __uint_as_float(v[i0 + 2]) : 0.f;
+                    f.w = (s0 + 3 < r) ? b * __uint_as_float(v[i0 + 3]) : 0.f;
+                    *reinterpret_cast<float4*>(dst + 4 * q4) = f;
+                }
             }
-        }
-    } else {
-        const int r = row - 64;
+        } else {
+            const int r = row - 64;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int chunk = 4 * ch + k;
-            uint32_t w[4];
+            for (int k = 0; k < 4; ++k) {
+                const int chunk = 4 * ch + k;
+                uint32_t w[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int s = 8 * chunk + 2 * u, i = 8 * k + 2 * u;
-                const float lo = (s <= r) ? __uint_as_float(v[i]) : 0.f;
-                const float hi = (s + 1 <= r) ? __uint_as_float(v[i + 1]) : 0.f;
-                w[u] = pack_bf16x2(lo, hi);
+                for (int u = 0; u < 4; ++u) {
+                    const int s = 8 * chunk + 2 * u, i = 8 * k + 2 * u;
+                    const float lo = (s <= r) ? __uint_as_float(v[i]) : 0.f;
+                    const float hi = (s + 1 <= r) ? __uint_as_float(v[i + 1]) : 0.f;
+                    w[u] = pack_bf16x2(lo, hi);
+                }
+                *reinterpret_cast<uint4*>(pp + sw128_offset(r, 16 * chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            *reinterpret_cast<uint4*>(pp + sw128_offset(r, 16 * chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
 }
@@ -367,7 +367,7 @@ __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP],
 // D_i = (I + N_ii)^{-1} by fp32 forward substitution; then the 32x32 halves
 // X_10 = -D_1 N_10 D_0, X_32 = -D_3 N_32 D_2; then the lower-left 32x32 quarter
 // -C^{-1} (B A^{-1}) with A^{-1}, C^{-1} the inverted halves and B = N[32:64, 0:32], using TF32
-// tensor-core block products with fp32 accumulation.  8 warps, 4 group barriers.
+// tensor-core block products with fp32 accumulation.  Team S (4 warps), 4 team barriers.
 __device__ void solve_T(uint8_t* aslot, const float* beta) {
     float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
     float* Xb = reinterpret_cast<float*>(aslot + kSolveX);
@@ -388,7 +388,7 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
     }
-    group_sync(kBarA);
+    group_sync(kBarS);
     // halves: warps 0-1 -> X_10 (n-tile w), warps 2-3 -> X_32 (n-tile w-2); Y via the block's own
     // Y slot, the chain stays inside the warp
     if (w < 4) {
@@ -408,10 +408,11 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
             blk_mma<1>(blk(Xb, i0 + 1, i0), A1, B1, nt, -1.f);
         }
     }
-    group_sync(kBarA);
+    group_sync(kBarS);
     // Y = B A^{-1}: Y_20 = N_20 D_0 + N_21 X_10, Y_21 = N_21 D_1, Y_30 = N_30 D_0 + N_31 X_10, Y_31 = N_31 D_1
-    {
-        const int ob = w >> 1, nt = w & 1;                   // ob: 0 Y20, 1 Y21, 2 Y30, 3 Y31
+#pragma unroll 1
+    for (int it = 0; it < 2; ++it) {
+        const int item = w + 4 * it, ob = item >> 1, nt = item & 1;   // ob: 0 Y20, 1 Y21, 2 Y30, 3 Y31
         const int ri = 2 + (ob >> 1), cj = ob & 1;
         float* Ys = Yb + ob * (kBlkBytes / 4);
         if (cj == 0) {
@@ -424,10 +425,11 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
             blk_mma<1>(Ys, A1, B1, nt, 1.f);
         }
     }
-    group_sync(kBarA);
+    group_sync(kBarS);
     // X_lower = -C^{-1} Y: X_20 = -D_2 Y_20, X_21 = -D_2 Y_21, X_30 = -(X_32 Y_20 + D_3 Y_30), X_31 = -(X_32 Y_21 + D_3 Y_31)
-    {
-        const int ob = w >> 1, nt = w & 1;
+#pragma unroll 1
+    for (int it = 0; it < 2; ++it) {
+        const int item = w + 4 * it, ob = item >> 1, nt = item & 1;
         const int ri = 2 + (ob >> 1), cj = ob & 1;
         if (ri == 2) {
             const float* A1[1] = {blk(Xb, 2, 2)};
@@ -439,9 +441,10 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
             blk_mma<2>(blk(Xb, 3, cj), A2, B2, nt, -1.f);
         }
     }
-    group_sync(kBarA);
-    {                                                // T[r][s] = X[r][s] beta_s (bf16)
-        const int r = t >> 2, q = t & 3, bi = r >> 4, rr = r & 15;
+    group_sync(kBarS);
+#pragma unroll 1
+    for (int it = 0; it < 2; ++it) {                 // T[r][s] = X[r][s] beta_s (bf16)
+        const int tt = t + kTeam * it, r = tt >> 2, q = tt & 3, bi = r >> 4, rr = r & 15;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int s0 = 16 * q + 8 * k;
@@ -756,13 +759,18 @@ __device__ __forceinline__ void prefetch_chunk(const Ctx& x, const Maps& maps, i
     tma_prefetch_l2_3d(&maps.q, 64, x.h, tc);
 }
 
-// ============================ group A loop =======================================
-__device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* __restrict__ beta) {
+// ============================ group A: team P loop ===============================
+// Team P (warps 0-3): chunk n's beta, the decay-range check, the Khat / Qhat / Kb
+// tiles and the Gram product, committed to gram_done[n % 2]; a token-by-token
+// chunk arrives there directly with mode 1.  Slot reuse: the A slot waits for
+// W'/U of chunk n-2 (its loads), Kb / P / beta / gamma for chunk n-2's state
+// product (kbp_free), and the Gram columns for chunk n-2's W' read, which comes
+// before that product.
+__device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __restrict__ beta) {
     const Ctx x = x_in;
     Small& sw = *x.sw;
     const int t = lt();
-    uint32_t gram_ph = 0;
-    bool ok = true, gram_pending = false;
+    bool ok = true, issued = false;
     float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
     for (int n = 0; n < x.nchunks; ++n) {
@@ -778,82 +786,106 @@ __device__ __noinline__ bool run_group_a(const Ctx& x_in, const __nv_bfloat16* _
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* kb = x.sm + kKB0 + s * 16384;
-        uint8_t* pp = x.sm + kPP0 + s * 8192;
 
         KDA_TRACE(n, 2);
-        if (!(ok = group_wait(kBarA, &sw.a_full[s], ph))) break;
+        if (!(ok = group_wait(kBarP, &sw.a_full[s], ph))) break;
         KDA_TRACE(n, 3);
         KDA_PHASE(0);
         if (t == 0) ++sw.consumed[kLdA][s];
-        if (n >= 2 && !(ok = group_wait(kBarA, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
+        if (n >= 2 && !(ok = group_wait(kBarP, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_TRACE(n, 4);
         KDA_PHASE(2);
         if (t < C) sw.beta[s][t] = (t < L) ? braw : 0.f;
-        if (!(ok = group_wait(kBarA, &sw.qk_full[s], ph))) break;
+        if (!(ok = group_wait(kBarP, &sw.qk_full[s], ph))) break;
         KDA_TRACE(n, 5);
         KDA_PHASE(3);
         if (t == 0) ++sw.consumed[kLdQK][s];
-        const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s],
-                                         reinterpret_cast<float*>(pp));
-        if (!fast) {                                     // token-by-token chunk
-            if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
+        const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s]);
+        if (!fast) {                                     // token-by-token chunk: no Gram product
+            if (t == 0) {
+                sw.mode[s] = 1;
+                mbar_arrive(&sw.gram_done[s]);
+            }
+            continue;
+        }
+        group_publish(kBarP);
+        KDA_PHASE(4);
+        if (t == 0) {
+            sw.mode[s] = 0;
+            mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
+            mma_commit(&sw.gram_done[s]);
+            issued = true;
+        }
+        KDA_TRACE(n, 6);
+        KDA_PHASE(25);
+    }
+    if (t == 0 && issued) {   // let this thread's products land before TMEM is freed (bounded)
+        mma_commit(&sw.drain_p);
+        mbar_wait_bounded(&sw.drain_p, 0, kWaitLimitNs);
+    }
+    return ok;
+}
+
+// ============================ group A: team S loop ===============================
+// Team S (warps 4-7): for chunk n, N and the masked P out of the Gram columns,
+// the UT solve T, then (once V has landed and chunk n-2's output has left the U
+// slot) W'^T = Khat^T T^T and U^T = V^T T^T; their commit is the second arrival
+// on ready.  A token-by-token chunk only waits for its V tile.
+__device__ __noinline__ bool run_team_s(const Ctx& x_in) {
+    const Ctx x = x_in;
+    Small& sw = *x.sw;
+    const int t = lt();
+    bool ok = true, issued = false;
+    KDA_PHASE_INIT;
+    for (int n = 0; n < x.nchunks; ++n) {
+        const int s = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        uint8_t* aslot = x.sm + kA0 + s * kABytes;
+        uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
+        uint8_t* pp = x.sm + kPP0 + s * 8192;
+
+        if (!(ok = group_wait(kBarS, &sw.gram_done[s], ph))) break;
+        KDA_PHASE(26);
+        if (sw.mode[s]) {                                // token-by-token chunk
+            if (!(ok = group_wait(kBarS, &sw.v_full[s], ph))) break;
             if (t == 0) {
                 ++sw.consumed[kLdV][s];
-                sw.mode[s] = 1;
                 mbar_arrive(&sw.ready[s]);
                 mbar_arrive(&sw.ready[s]);
             }
             continue;
         }
-        group_publish(kBarA);
-        KDA_PHASE(4);
-        if (t == 0) {
-            mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
-            KDA_PHASE(25);
-            mma_commit(&sw.gram_done);
-        }
-        gram_pending = true;
-        if (!(ok = group_wait(kBarA, &sw.gram_done, gram_ph))) break;
-        KDA_TRACE(n, 6);
-        gram_ph ^= 1u;
-        gram_pending = false;
-        KDA_PHASE(5);
         tc_fence_after();
         read_gram(x.tb, tm_apw(s), aslot, pp, sw.beta[s]);
         fence_proxy_async_smem();
         tc_fence_before();
-        group_sync(kBarA);
+        group_sync(kBarS);
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s]);
         KDA_PHASE(15);
         KDA_TRACE(n, 7);
-        if (!(ok = group_wait(kBarA, &sw.v_full[s], ph))) break;
+        if (!(ok = group_wait(kBarS, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
         // the U slot still holds chunk n-2's output until group B has read it (every chunk,
         // tensor-core or token-by-token, completes one phase of its slot's u_free)
-        if (n >= 2 && !(ok = group_wait(kBarA, &sw.u_free[s], ((n - 2) >> 1) & 1))) break;
+        if (n >= 2 && !(ok = group_wait(kBarS, &sw.u_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_TRACE(n, 8);
-        group_publish(kBarA);
+        group_publish(kBarS);
         KDA_PHASE(7);
         if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival
-            sw.mode[s] = 0;
             mbar_arrive(&sw.ready[s]);
             mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
                    smem_u32(aslot + kTT));
-            KDA_PHASE(23);
             mma_commit(&sw.ready[s]);
             mma_commit(&sw.av_free[s]);
+            issued = true;
         }
         KDA_TRACE(n, 9);
         KDA_PHASE(1);
     }
-    if (!ok && t == 0) {   // let every MMA this thread issued land before TMEM is freed (bounded)
-        if (gram_pending) {
-            mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);
-            gram_ph ^= 1u;
-        }
-        mma_commit(&sw.gram_done);
-        mbar_wait_bounded(&sw.gram_done, gram_ph, kWaitLimitNs);
+    if (t == 0 && issued) {
+        mma_commit(&sw.drain_s);
+        mbar_wait_bounded(&sw.drain_s, 0, kWaitLimitNs);
     }
     return ok;
 }
@@ -937,7 +969,7 @@ __device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint
 }
 
 // Store the output a chunk left in its U slot, then release that U slot to
-// group A (one arrival per warp, once its TMEM reads are done).
+// team S (one arrival per warp, once its TMEM reads are done).
 __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_bfloat16* out, int prev_s,
                                            int64_t prev_t0, int prev_L, bool leader) {
     uint32_t opk[32];
@@ -1119,7 +1151,8 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
             mbar_init(&sw->ready[s], 2);
             mbar_init(&sw->kbp_free[s], 1);
         }
-        mbar_init(&sw->gram_done, 1);
+        mbar_init(&sw->gram_done[0], 1);
+        mbar_init(&sw->gram_done[1], 1);
         mbar_init(&sw->mma1_done, 1);
         mbar_init(&sw->mma2_done, 1);
         mbar_init(&sw->av_free[0], 1);
@@ -1130,6 +1163,8 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         mbar_init(&sw->u_free[1], 4);
         mbar_init(&sw->packed, 1);
         mbar_init(&sw->drain, 1);
+        mbar_init(&sw->drain_p, 1);
+        mbar_init(&sw->drain_s, 1);
         fence_mbar_init();
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
@@ -1152,8 +1187,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     x.tb = sw->tmem_base;
 
     bool ok = true;
-    if (in_group_a())
-        ok = run_group_a(x, beta);
+    if (in_team_p())
+        ok = run_team_p(x, beta);
+    else if (in_group_a())
+        ok = run_team_s(x);
     else if (tid < kProducer)
         ok = run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
     else if (tid == kProducer)
