@@ -271,6 +271,11 @@ __device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float*
 __device__ __forceinline__ float* blk(float* base, int i, int j) {
     return base + (i * (i + 1) / 2 + j) * (kBlkBytes / 4);
 }
+// Element (r, c) of a 16x16 solve block sits at r * 16 + (c ^ blk_swz(r)): the swizzle
+// moves 4-column groups by row so that the m16n8k8 fragment loads and the 16-byte row
+// stores of a warp hit distinct banks.
+__device__ __forceinline__ int blk_swz(int r) { return ((r << 2) & 8) | (r & 4); }
+__device__ __forceinline__ int blk_at(int r, int c) { return r * kBlkStride + (c ^ blk_swz(r)); }
 
 // TMEM lanes 0-63 hold A rows r: N = beta_r A_rs (s < r) as fp32
 // lower-triangular 16x16 blocks in the A slot.  Lanes 64-127 hold P rows r:
@@ -291,7 +296,7 @@ __device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp
             for (int k = 0; k < 2; ++k) {
                 const int bj = 2 * ch + k;
                 if (bj > bi) break;
-                float* dst = blk(Nb, bi, bj) + rr * kBlkStride;
+                float* dst = blk(Nb, bi, bj);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const int s0 = 16 * bj + 4 * q4, i0 = 16 * k + 4 * q4;
@@ -300,7 +305,7 @@ __device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp
                     f.y = (s0 + 1 < r) ? b * __uint_as_float(v[i0 + 1]) : 0.f;
                     f.z = (s0 + 2 < r) ? b * __uint_as_float(v[i0 + 2]) : 0.f;
                     f.w = (s0 + 3 < r) ? b * __uint_as_float(v[i0 + 3]) : 0.f;
-                    *reinterpret_cast<float4*>(dst + 4 * q4) = f;
+                    *reinterpret_cast<float4*>(dst + blk_at(rr, 4 * q4)) = f;
                 }
             }
         } else {
@@ -337,8 +342,8 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// One warp: columns [8 nt, 8 nt + 8) of C = sign * sum_p A_p B_p for 16x16 blocks (row stride
-// kBlkStride floats).
+// One warp: columns [8 nt, 8 nt + 8) of C = sign * sum_p A_p B_p for 16x16 blocks (blk_at
+// layout).
 template <int NP>
 __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP], const float* const (&Bb)[NP],
                                         int nt, float sign) {
@@ -348,19 +353,18 @@ __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP],
     for (int p = 0; p < NP; ++p) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-            const float* A = Ab[p] + 8 * ks;
-            const float* B = Bb[p] + (8 * ks) * kBlkStride + 8 * nt;
-            const uint32_t af[4] = {to_tf32(A[g * kBlkStride + t]), to_tf32(A[(g + 8) * kBlkStride + t]),
-                                    to_tf32(A[g * kBlkStride + t + 4]), to_tf32(A[(g + 8) * kBlkStride + t + 4])};
-            const uint32_t bf[2] = {to_tf32(B[t * kBlkStride + g]), to_tf32(B[(t + 4) * kBlkStride + g])};
+            const float* A = Ab[p];
+            const float* B = Bb[p];
+            const int k0 = 8 * ks;
+            const uint32_t af[4] = {to_tf32(A[blk_at(g, k0 + t)]), to_tf32(A[blk_at(g + 8, k0 + t)]),
+                                    to_tf32(A[blk_at(g, k0 + t + 4)]), to_tf32(A[blk_at(g + 8, k0 + t + 4)])};
+            const uint32_t bf[2] = {to_tf32(B[blk_at(k0 + t, 8 * nt + g)]), to_tf32(B[blk_at(k0 + t + 4, 8 * nt + g)])};
             mma_tf32(d, af, bf);
         }
     }
-    float* C = Cb + 8 * nt;
-    C[g * kBlkStride + 2 * t] = sign * d[0];
-    C[g * kBlkStride + 2 * t + 1] = sign * d[1];
-    C[(g + 8) * kBlkStride + 2 * t] = sign * d[2];
-    C[(g + 8) * kBlkStride + 2 * t + 1] = sign * d[3];
+    const int c0 = 8 * nt + 2 * t;                   // a column pair stays adjacent under the swizzle
+    *reinterpret_cast<float2*>(Cb + blk_at(g, c0)) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2*>(Cb + blk_at(g + 8, c0)) = make_float2(sign * d[2], sign * d[3]);
 }
 
 // T = (I + N)^{-1} Diag(beta) with N strictly lower 64x64 (10 lower 16x16 blocks in the A slot):
@@ -381,12 +385,12 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
         for (int r = 0; r < 16; ++r) {
             float acc = (r == jl) ? 1.f : 0.f;
 #pragma unroll
-            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[r * kBlkStride + q], x[q], acc);
+            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[blk_at(r, q)], x[q], acc);
             x[r] = acc;
         }
         float* Xii = blk(Xb, i, i);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Xii[r * kBlkStride + jl] = x[r];
+        for (int r = 0; r < 16; ++r) Xii[blk_at(r, jl)] = x[r];
     }
     group_sync(kBarS);
     // halves: warps 0-1 -> X_10 (n-tile w), warps 2-3 -> X_32 (n-tile w-2); Y via the block's own
@@ -450,7 +454,10 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
             const int s0 = 16 * q + 8 * k;
             uint32_t wv[4];
             if (q <= bi) {
-                const float* xr = blk(Xb, bi, q) + rr * kBlkStride + 8 * k;
+                const float* xb = blk(Xb, bi, q);
+                const float4 lo = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k));
+                const float4 hi = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k + 4));
+                const float xr[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     wv[u] = pack_bf16x2(xr[2 * u] * beta[s0 + 2 * u], xr[2 * u + 1] * beta[s0 + 2 * u + 1]);
