@@ -58,6 +58,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "kda_internal.h"
@@ -132,6 +133,7 @@ struct Small {
 #endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
+static_assert(offsetof(Small, gam) % 16 == 0, "gamma rows are read as float4");
 
 __device__ __forceinline__ uint32_t qk_off(bool is_q, uint32_t r, uint32_t c) {
     return (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
@@ -482,7 +484,13 @@ __device__ void decay_state(uint32_t tb, const float* gam) {
         tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * gam[32 * cb + i]);
+        for (int i = 0; i < 8; ++i) {
+            const float4 g = *reinterpret_cast<const float4*>(gam + 32 * cb + 4 * i);
+            v[4 * i + 0] = __float_as_uint(__uint_as_float(v[4 * i + 0]) * g.x);
+            v[4 * i + 1] = __float_as_uint(__uint_as_float(v[4 * i + 1]) * g.y);
+            v[4 * i + 2] = __float_as_uint(__uint_as_float(v[4 * i + 2]) * g.z);
+            v[4 * i + 3] = __float_as_uint(__uint_as_float(v[4 * i + 3]) * g.w);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
         tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), v);
