@@ -161,6 +161,43 @@ kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
                            kda_stream_t stream);
 
 /*
+ * kda_frontend -- the steps of a KDA layer between its projections and the
+ * recurrence, as "Kimi K3 architecture: KDA, MLA and MoE" (section "Scale:
+ * Total vs Active Parameters and Serving Economics", Visual 1, the KDA inset)
+ * draws them: q and k pass a short convolution, SiLU and an L2 norm; v a short
+ * convolution and SiLU; the decay and beta a sigmoid.  Per sequence, token and
+ * head (W = conv_width):
+ *
+ *   y[t, c]   = sum_{i<W} conv[h, c, i] * x_raw[t-(W-1)+i, h, c]   (0 before the
+ *               sequence start: the convolution never reads another sequence)
+ *   q         = SiLU(y_q) / sqrt(|SiLU(y_q)|^2 + eps)    (norm over dk)
+ *   k         = SiLU(y_k) / sqrt(|SiLU(y_k)|^2 + eps)
+ *   v         = SiLU(y_v)
+ *   log_alpha = logsigmoid(a_raw),  beta = sigmoid(b_raw)
+ *
+ * The convolution width, its causal and depthwise form and eps are readings:
+ * the figure names the steps only.  The projections are the caller's GEMMs.
+ * shape:     as kda_prefill; q_raw, k_raw, v_raw, b_raw and the outputs q, k, v,
+ *            beta are in shape->dtype; a_raw and log_alpha are fp32.
+ * q_raw, k_raw, a_raw [T, H, dk]; v_raw [T, H, dv]; b_raw [T, H].
+ * conv_q, conv_k [H, dk, W], conv_v [H, dv, W]: fp32 taps, tap W-1 on the current
+ *            token; 1 <= W <= 4.
+ * eps:       added to the sum of squares of the L2 norm, finite and >= 0.
+ * q, k, v, log_alpha, beta: written in kda_prefill's input layout; they must not
+ *            overlap the raw inputs.
+ * cu_seqlens: as kda_prefill (NULL: N equal sequences).
+ * Errors: those of kda_prefill for the shape and the pointers, plus
+ *   KDA_ERR_UNSUPPORTED for W outside 1..4 and KDA_ERR_INVALID_ARG for a bad eps
+ *   or a NULL conv pointer.
+ */
+kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps,
+                        const void* q_raw, const void* k_raw, const void* v_raw,
+                        const float* a_raw, const void* b_raw, const float* conv_q,
+                        const float* conv_k, const float* conv_v,
+                        const int32_t* cu_seqlens, void* q, void* k, void* v,
+                        float* log_alpha, void* beta, kda_stream_t stream);
+
+/*
  * kda_check_cu_seqlens -- validate a HOST copy of a cu_seqlens table:
  * cu[0] == 0, non-decreasing, cu[num_seqs] == total_tokens.  Returns KDA_OK
  * or KDA_ERR_INVALID_ARG.  No CUDA call.

@@ -56,6 +56,8 @@ def lib():
         L.kda_check_cu_seqlens.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
         L.kda_device_status.restype = ctypes.c_int
+        L.kda_frontend.argtypes = [sp, ctypes.c_int32, ctypes.c_float] + [vp] * 15
+        L.kda_frontend.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_version.argtypes = []
@@ -187,6 +189,39 @@ def kda_prefill_checkpointed(q, k, v, log_alpha, beta, ckpt_pos, initial_state=N
                                         _ptr(ck_states), _stream(stream))
     _check("kda_prefill_checkpointed", st)
     return out, final_state, ck_states[:total]
+
+
+def kda_frontend(q_raw, k_raw, v_raw, a_raw, b_raw, conv_q, conv_k, conv_v, cu_seqlens=None,
+                 num_seqs=None, eps=1e-6, out=None, stream=None):
+    """Layer front end (see ``include/kda.h``): short convolution + SiLU (+ L2 norm
+    for q, k), logsigmoid for the decay, sigmoid for beta.
+
+    q_raw, k_raw: [T, H, dk]; v_raw: [T, H, dv]; b_raw: [T, H] (bf16 or fp32);
+    a_raw: [T, H, dk] fp32; conv_q, conv_k: [H, dk, W], conv_v: [H, dv, W] fp32.
+    Returns (q, k, v, log_alpha, beta) in kda_prefill's input layout, or fills
+    ``out`` (a tuple of five tensors) when given."""
+    T, H, dk = q_raw.shape
+    dv = v_raw.shape[2]
+    W = conv_q.shape[-1]
+    if cu_seqlens is not None and not (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda):
+        host_cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+        kda_check_cu_seqlens(host_cu, T)
+        cu_seqlens = host_cu.to(q_raw.device)
+    n = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    dev, dt = q_raw.device, q_raw.dtype
+    if out is None:
+        out = (torch.empty((T, H, dk), dtype=dt, device=dev), torch.empty((T, H, dk), dtype=dt, device=dev),
+               torch.empty((T, H, dv), dtype=dt, device=dev),
+               torch.empty((T, H, dk), dtype=torch.float32, device=dev),
+               torch.empty((T, H), dtype=dt, device=dev))
+    q, k, v, la, beta = out
+    shape = KdaShape(n, T, H, dk, dv, _dtype_code(q_raw))
+    st = lib().kda_frontend(ctypes.byref(shape), int(W), float(eps), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                            _ptr(a_raw), _ptr(b_raw), _ptr(conv_q), _ptr(conv_k), _ptr(conv_v),
+                            _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(la), _ptr(beta),
+                            _stream(stream))
+    _check("kda_frontend", st)
+    return q, k, v, la, beta
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):

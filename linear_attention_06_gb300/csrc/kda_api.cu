@@ -6,6 +6,7 @@
 // is allocated; the only library state is one device status word that the
 // tensor-core kernel sets if one of its bounded waits gives up.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -182,6 +183,36 @@ kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return finish(kda::launch_decode(a, s), s);
+}
+
+kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, const void* q_raw,
+                        const void* k_raw, const void* v_raw, const float* a_raw, const void* b_raw,
+                        const float* conv_q, const float* conv_k, const float* conv_v,
+                        const int32_t* cu_seqlens, void* q, void* k, void* v, float* log_alpha,
+                        void* beta, kda_stream_t stream) {
+    kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens && shape->num_seqs > 0 && shape->total_tokens % shape->num_seqs != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_UNSUPPORTED;
+    if (conv_width < 1 || conv_width > 4) return KDA_ERR_UNSUPPORTED;
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens == 0) return KDA_OK;
+    // the raw inputs and the outputs follow kda_prefill's pointer rules
+    st = check_tensor_ptrs(shape, q_raw, k_raw, v_raw, a_raw, b_raw, q);
+    if (st != KDA_OK) return st;
+    st = check_tensor_ptrs(shape, q, k, v, log_alpha, beta, v);
+    if (st != KDA_OK) return st;
+    if (!conv_q || !conv_k || !conv_v) return KDA_ERR_INVALID_ARG;
+    if (!aligned(conv_q, 4) || !aligned(conv_k, 4) || !aligned(conv_v, 4)) return KDA_ERR_UNSUPPORTED;
+    kda::FrontendArgs a{q_raw, k_raw, v_raw, conv_q, conv_k, conv_v, a_raw, b_raw, cu_seqlens,
+                        q, k, v, log_alpha, beta, shape->total_tokens, shape->num_seqs, shape->H,
+                        shape->dk, shape->dv, conv_width, eps,
+                        shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return finish(kda::launch_frontend(a, s), s);
 }
 
 kda_status kda_device_status(kda_stream_t stream) {

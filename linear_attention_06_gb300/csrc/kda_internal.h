@@ -47,6 +47,31 @@ struct DecodeArgs {
     DType dtype;
 };
 
+// Layer front end: projections -> recurrence inputs (see kda_frontend in kda.h).
+struct FrontendArgs {
+    const void* q_raw;            // [T, H, dk] dtype
+    const void* k_raw;            // [T, H, dk] dtype
+    const void* v_raw;            // [T, H, dv] dtype
+    const float* conv_q;          // [H, dk, W]
+    const float* conv_k;          // [H, dk, W]
+    const float* conv_v;          // [H, dv, W]
+    const float* a_raw;           // [T, H, dk] fp32 decay logits
+    const void* b_raw;            // [T, H] dtype beta logits
+    const int32_t* cu_seqlens;    // may be null (equal split)
+    void* q;                      // outputs in kda_prefill's layout
+    void* k;
+    void* v;
+    float* log_alpha;
+    void* beta;
+    int64_t total_tokens;
+    int32_t num_seqs;
+    int32_t H, dk, dv;
+    int32_t conv_width;           // 1..4
+    float eps;                    // L2-norm epsilon
+    DType dtype;
+};
+cudaError_t launch_frontend(const FrontendArgs& a, cudaStream_t s);
+
 // fp32 recurrent prefill (any supported dtype / head size).
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // Chunkwise tensor-core prefill: bf16, dk = dv = 128.

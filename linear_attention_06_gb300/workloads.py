@@ -17,6 +17,14 @@ lengths):
   beta   = sigmoid(N(0, 1)) per (token, head), in the input dtype.
   initial state: zeros, or N(0, 0.05) (standard deviation 0.05) in fp32.
   varlen lengths: floor(exp(U(ln 128, ln 32768))) per sequence.
+
+Layer inputs (``make_layer_inputs``, for the front end before the recurrence and
+the gated output after it; raw draws only, in the order q, k, v, a, b, gate,
+conv q, conv k, conv v, norm weight):
+  q_raw, k_raw, v_raw ~ N(0, 1) in the input dtype (projection outputs);
+  a_raw ~ N(mu, 1) fp32 (decay logits; logsigmoid of it is log_alpha);
+  b_raw ~ N(0, 1), gate logits g_raw ~ N(0, 1) in the input dtype;
+  convolution taps ~ N(0, 1/W) fp32 (width W), norm weight ~ 1 + N(0, 0.1) fp32.
 """
 from __future__ import annotations
 
@@ -85,6 +93,54 @@ def make_inputs(T, H, dk, dv, dtype=torch.bfloat16, seed=0, alpha_mu=3.0,
                     beta.to(dtype), h0, cu,
                     dict(T=T, H=H, dk=dk, dv=dv, dtype=str(dtype).replace("torch.", ""),
                          seed=seed, alpha_mu=alpha_mu))
+
+
+@dataclass
+class LayerInputs:
+    name: str
+    q_raw: torch.Tensor        # [T, H, dk]
+    k_raw: torch.Tensor        # [T, H, dk]
+    v_raw: torch.Tensor        # [T, H, dv]
+    a_raw: torch.Tensor        # [T, H, dk] fp32
+    b_raw: torch.Tensor        # [T, H]
+    g_raw: torch.Tensor        # [T, H, dv]
+    conv_q: torch.Tensor       # [H, dk, W] fp32
+    conv_k: torch.Tensor       # [H, dk, W] fp32
+    conv_v: torch.Tensor       # [H, dv, W] fp32
+    norm_weight: torch.Tensor  # [dv] fp32
+    cu_seqlens: torch.Tensor   # [N+1] int32 (host copy)
+
+    def to(self, device):
+        f = {k: (v.to(device) if isinstance(v, torch.Tensor) and k != "cu_seqlens" else v)
+             for k, v in self.__dict__.items()}
+        f["cu_seqlens"] = self.cu_seqlens.clone()
+        return LayerInputs(**f)
+
+
+def make_layer_inputs(T, H, dk, dv, W=4, dtype=torch.bfloat16, seed=0, alpha_mu=3.0,
+                      cu_seqlens=None, num_seqs=1, device="cpu", name="layer"):
+    """Raw projection outputs and layer weights for the front end and the gated
+    output (see the module docstring for the recipe)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    q = _normal((T, H, dk), gen, device)
+    k = _normal((T, H, dk), gen, device)
+    v = _normal((T, H, dv), gen, device)
+    a = _normal((T, H, dk), gen, device, mean=alpha_mu)
+    b = _normal((T, H), gen, device)
+    g = _normal((T, H, dv), gen, device)
+    std = 1.0 / math.sqrt(W)
+    cq = _normal((H, dk, W), gen, device, std=std)
+    ck = _normal((H, dk, W), gen, device, std=std)
+    cv = _normal((H, dv, W), gen, device, std=std)
+    nw = _normal((dv,), gen, device, mean=1.0, std=0.1)
+    if cu_seqlens is None:
+        assert T % num_seqs == 0
+        cu = torch.arange(num_seqs + 1, dtype=torch.int32) * (T // num_seqs)
+    else:
+        cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+    return LayerInputs(name, q.to(dtype), k.to(dtype), v.to(dtype), a.contiguous(), b.to(dtype),
+                       g.to(dtype), cq, ck, cv, nw, cu)
 
 
 def varlen_lengths(num_seqs, seed, lo=128, hi=32768):

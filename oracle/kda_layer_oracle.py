@@ -49,19 +49,19 @@ def _bounds(T, cu_seqlens, num_seqs):
 
 def short_conv(x, w, cu_seqlens=None, num_seqs=None):
     """Causal depthwise convolution per sequence: x [T, H, d], w [H, d, W];
-    y[t] = sum_i w[..., i] * x[t - (W-1) + i], zero before the sequence start."""
+    y[t] = sum_i w[..., i] * x[t - (W-1) + i], zero before the sequence start.
+    Tap i reads the input lag = W-1-i tokens back, so each tap adds the
+    sequence shifted down by its lag."""
     x, w = _f64(x), _f64(w)
     T = x.shape[0]
     W = w.shape[-1]
     y = np.zeros_like(x)
     for bos, eos in _bounds(T, cu_seqlens, num_seqs):
-        for t in range(bos, eos):
-            acc = np.zeros(x.shape[1:])
-            for i in range(W):
-                src = t - (W - 1) + i
-                if src >= bos:
-                    acc += w[..., i] * x[src]
-            y[t] = acc
+        n = eos - bos
+        for i in range(W):
+            lag = W - 1 - i
+            if lag < n:
+                y[bos + lag:eos] += w[..., i] * x[bos:eos - lag]
     return y
 
 

@@ -142,3 +142,24 @@ def test_prefill_checkpointed_rejects_null_tables(L):
     args = [ctypes.byref(sh)] + [p(FAKE)] * 5 + [None, None, p(FAKE), None]
     assert L.kda_prefill_checkpointed(*args, None, p(FAKE), p(FAKE), None) == _lib.KDA_ERR_INVALID_ARG
     assert L.kda_prefill_checkpointed(*args, p(FAKE), p(FAKE), p(FAKE + 8), None) == _lib.KDA_ERR_UNSUPPORTED
+
+
+def frontend_call(L, sh, W=4, eps=1e-6, ptrs=None, conv=FAKE):
+    p = ptrs or FAKE
+    P = ctypes.c_void_p
+    return L.kda_frontend(ctypes.byref(sh), W, ctypes.c_float(eps), P(p), P(p), P(p), P(p), P(p),
+                          P(conv), P(conv), P(conv), None, P(p), P(p), P(p), P(p), P(p), None)
+
+
+@pytest.mark.parametrize("W,eps,code", [(0, 1e-6, 2), (5, 1e-6, 2), (4, -1.0, 1), (4, float("nan"), 1),
+                                        (4, float("inf"), 1)])
+def test_frontend_rejects_width_and_eps(L, W, eps, code):
+    assert frontend_call(L, shape(), W=W, eps=eps) == code
+
+
+def test_frontend_rejects_pointers_and_shapes(L):
+    assert frontend_call(L, shape(), conv=0) == 1                 # null conv taps
+    assert frontend_call(L, shape(), ptrs=FAKE_MIS) == 2          # misaligned tensors
+    assert frontend_call(L, shape(dk=96)) == 2                    # unsupported head size
+    assert frontend_call(L, shape(n=3, T=128)) == 1               # T % N without cu_seqlens
+    assert frontend_call(L, shape(n=0, T=0)) == 0                 # empty: nothing enqueued
