@@ -132,6 +132,32 @@ kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const
                                     kda_stream_t stream);
 
 /*
+ * kda_prefill_gated -- kda_prefill whose stored output is the KDA layer's
+ * gated output instead of o: "Kimi K3 architecture: KDA, MLA and MoE"
+ * (section "Scale: Total vs Active Parameters and Serving Economics",
+ * Visual 1, the KDA inset) passes the KDA output through a norm and multiplies
+ * it by a sigmoid gate.  Per token t and head h:
+ *
+ *   out[t, h, j] = o[t, h, j] / sqrt(mean_j' o[t, h, j']^2 + norm_eps)
+ *                  * norm_weight[j] * sigmoid(gate[t, h, j])
+ *
+ * (an RMSNorm over the dv value channels with one weight per channel shared by
+ * the heads -- the figure says only "a norm"; this is the reading).
+ * gate:        [T, H, dv] in dtype, the gate logits, 16-byte aligned.
+ * norm_weight: [dv] fp32.   norm_eps: finite, >= 0.
+ * All other arguments are those of kda_prefill; final_state is unchanged by the
+ * gate.  The tensor-core path applies the gate in its output stores; the fp32
+ * recurrent path applies it in a second pass over out.
+ * Errors: those of kda_prefill, plus KDA_ERR_INVALID_ARG for a NULL gate or
+ *   weight or a bad eps and KDA_ERR_UNSUPPORTED for a misaligned gate.
+ */
+kda_status kda_prefill_gated(const kda_shape* shape, const void* q, const void* k,
+                             const void* v, const float* log_alpha, const void* beta,
+                             const float* initial_state, const int32_t* cu_seqlens,
+                             const void* gate, const float* norm_weight, float norm_eps,
+                             void* out, float* final_state, kda_stream_t stream);
+
+/*
  * kda_check_checkpoints -- validate HOST copies of a cu_seqlens table and of a
  * checkpoint table against the rules of kda_prefill_checkpointed.  Returns
  * KDA_OK or KDA_ERR_INVALID_ARG.  No CUDA call.
@@ -196,6 +222,18 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps,
                         const float* conv_k, const float* conv_v,
                         const int32_t* cu_seqlens, void* q, void* k, void* v,
                         float* log_alpha, void* beta, kda_stream_t stream);
+
+/*
+ * kda_decode_step_gated -- kda_decode_step whose stored output is the gated
+ * output of kda_prefill_gated (gate [N*T, H, dv] in dtype, norm_weight [dv]
+ * fp32, norm_eps >= 0), fused into the step's output store.  The state update
+ * is that of kda_decode_step.  Errors: those of kda_decode_step and of the gate
+ * arguments of kda_prefill_gated.
+ */
+kda_status kda_decode_step_gated(const kda_shape* shape, const void* q, const void* k,
+                                 const void* v, const float* log_alpha, const void* beta,
+                                 const void* gate, const float* norm_weight, float norm_eps,
+                                 float* state_inout, void* out, kda_stream_t stream);
 
 /*
  * kda_check_cu_seqlens -- validate a HOST copy of a cu_seqlens table:

@@ -1,10 +1,12 @@
 """GB300-native Kimi Delta Attention (KDA): prefill and decode behind the C ABI
 of libkda (include/kda.h).  This package is the thin Python side of it."""
 from ._lib import (KdaError, KdaShape, kda_check_cu_seqlens, kda_decode_step,  # noqa: F401
-                   kda_device_status, kda_frontend, kda_prefill, kda_prefill_checkpointed, lib,
+                   kda_decode_step_gated, kda_device_status, kda_frontend, kda_prefill, kda_prefill_checkpointed,
+                   kda_prefill_gated, lib,
                    status_string, version)
 from . import workloads  # noqa: F401
 
-__all__ = ["kda_prefill", "kda_prefill_checkpointed", "kda_decode_step", "kda_frontend", "kda_check_cu_seqlens",
+__all__ = ["kda_prefill", "kda_prefill_checkpointed", "kda_prefill_gated", "kda_decode_step",
+           "kda_decode_step_gated", "kda_frontend", "kda_check_cu_seqlens",
            "kda_device_status",
            "status_string", "version", "lib", "KdaError", "KdaShape", "workloads"]

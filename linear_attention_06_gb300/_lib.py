@@ -56,6 +56,10 @@ def lib():
         L.kda_check_cu_seqlens.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
         L.kda_device_status.restype = ctypes.c_int
+        L.kda_prefill_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+        L.kda_prefill_gated.restype = ctypes.c_int
+        L.kda_decode_step_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
+        L.kda_decode_step_gated.restype = ctypes.c_int
         L.kda_frontend.argtypes = [sp, ctypes.c_int32, ctypes.c_float] + [vp] * 15
         L.kda_frontend.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
@@ -189,6 +193,46 @@ def kda_prefill_checkpointed(q, k, v, log_alpha, beta, ckpt_pos, initial_state=N
                                         _ptr(ck_states), _stream(stream))
     _check("kda_prefill_checkpointed", st)
     return out, final_state, ck_states[:total]
+
+
+def kda_prefill_gated(q, k, v, log_alpha, beta, gate, norm_weight, norm_eps=1e-6, initial_state=None,
+                      cu_seqlens=None, out=None, final_state=None, num_seqs=None, stream=None):
+    """kda_prefill whose output is RMSNorm(o) * norm_weight * sigmoid(gate) per
+    (token, head) (see ``include/kda.h``).  gate: [T, H, dv] like v; norm_weight:
+    [dv] fp32.  Returns (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is not None and not (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda):
+        host_cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+        kda_check_cu_seqlens(host_cu, T)
+        cu_seqlens = host_cu.to(q.device)
+    n = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is True:
+        final_state = torch.empty((n, H, dk, dv), dtype=torch.float32, device=q.device)
+    shape = KdaShape(n, T, H, dk, dv, _dtype_code(q))
+    st = lib().kda_prefill_gated(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(initial_state), _ptr(cu_seqlens), _ptr(gate), _ptr(norm_weight),
+                                 float(norm_eps), _ptr(out), _ptr(final_state), _stream(stream))
+    _check("kda_prefill_gated", st)
+    return out, final_state
+
+
+def kda_decode_step_gated(q, k, v, log_alpha, beta, gate, norm_weight, state, norm_eps=1e-6, out=None,
+                          stream=None):
+    """kda_decode_step whose output is gated like kda_prefill_gated; state in place."""
+    rows, H, dk = q.shape
+    dv = v.shape[2]
+    N = state.shape[0]
+    if out is None:
+        out = torch.empty((rows, H, dv), dtype=q.dtype, device=q.device)
+    shape = KdaShape(N, rows, H, dk, dv, _dtype_code(q))
+    st = lib().kda_decode_step_gated(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                     _ptr(beta), _ptr(gate), _ptr(norm_weight), float(norm_eps), _ptr(state),
+                                     _ptr(out), _stream(stream))
+    _check("kda_decode_step_gated", st)
+    return out
 
 
 def kda_frontend(q_raw, k_raw, v_raw, a_raw, b_raw, conv_q, conv_k, conv_v, cu_seqlens=None,

@@ -65,6 +65,15 @@ kda_status check_tensor_ptrs(const kda_shape* s, const void* q, const void* k, c
     return KDA_OK;
 }
 
+// Gated-output arguments: gate [T, H, dv] like out, weight [dv] fp32, eps finite and >= 0.
+kda_status check_gate(const kda_shape* s, const void* gate, const float* norm_w, float eps) {
+    if (!gate || !norm_w) return KDA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(gate, 16) || !aligned(norm_w, 4)) return KDA_ERR_UNSUPPORTED;
+    (void)s;
+    return KDA_OK;
+}
+
 kda_status finish(cudaError_t e, cudaStream_t st) {
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (env_flag("KDA_DEBUG_SYNC")) return kda_device_status(st);
@@ -91,7 +100,8 @@ kda_status prefill_impl(const kda_shape* shape, const void* q, const void* k, co
                         const float* log_alpha, const void* beta, const float* initial_state,
                         const int32_t* cu_seqlens, void* out, float* final_state,
                         const int32_t* ckpt_cu, const int32_t* ckpt_pos, float* ckpt_states,
-                        kda_stream_t stream) {
+                        kda_stream_t stream, const void* gate = nullptr, const float* norm_w = nullptr,
+                        float norm_eps = 0.f) {
     kda_status st = check_shape(shape);
     if (st != KDA_OK) return st;
     if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
@@ -112,15 +122,19 @@ kda_status prefill_impl(const kda_shape* shape, const void* q, const void* k, co
     kda::PrefillArgs a{q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
                        shape->total_tokens, shape->num_seqs, shape->H, shape->dk, shape->dv,
                        shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, status,
-                       ckpt_cu, ckpt_pos, ckpt_states};
+                       ckpt_cu, ckpt_pos, ckpt_states, gate, norm_w, norm_eps};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const char* force = getenv("KDA_PREFILL_IMPL");
     const bool want_recurrent = force && strcmp(force, "recurrent") == 0;
     cudaError_t e;
-    if (!want_recurrent && kda::chunk_tc_supported(a))
-        e = kda::launch_chunk_tc_prefill(a, s);
-    else
+    if (!want_recurrent && kda::chunk_tc_supported(a)) {
+        e = kda::launch_chunk_tc_prefill(a, s);            // gated output fused into its stores
+    } else {
         e = kda::launch_recurrent_prefill(a, s);
+        if (e == cudaSuccess && gate)                      // then a row pass over the outputs
+            e = kda::launch_gated_norm(out, gate, norm_w, norm_eps, shape->total_tokens * shape->H,
+                                       shape->dv, a.dtype, s);
+    }
     return finish(e, s);
 }
 }  // namespace
@@ -148,6 +162,18 @@ kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const
                         ckpt_cu, ckpt_pos, ckpt_states, stream);
 }
 
+kda_status kda_prefill_gated(const kda_shape* shape, const void* q, const void* k, const void* v,
+                             const float* log_alpha, const void* beta, const float* initial_state,
+                             const int32_t* cu_seqlens, const void* gate, const float* norm_weight,
+                             float norm_eps, void* out, float* final_state, kda_stream_t stream) {
+    if (shape && shape->total_tokens > 0) {
+        const kda_status st = check_gate(shape, gate, norm_weight, norm_eps);
+        if (st != KDA_OK) return st;
+    }
+    return prefill_impl(shape, q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                        nullptr, nullptr, nullptr, stream, gate, norm_weight, norm_eps);
+}
+
 kda_status kda_check_checkpoints(const int32_t* cu, int32_t num_seqs, int64_t total_tokens,
                                  const int32_t* ckpt_cu, const int32_t* ckpt_pos) {
     if (kda_check_cu_seqlens(cu, num_seqs, total_tokens) != KDA_OK) return KDA_ERR_INVALID_ARG;
@@ -165,9 +191,12 @@ kda_status kda_check_checkpoints(const int32_t* cu, int32_t num_seqs, int64_t to
     return KDA_OK;
 }
 
-kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k, const void* v,
-                           const float* log_alpha, const void* beta, float* state_inout,
-                           void* out, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+kda_status decode_impl(const kda_shape* shape, const void* q, const void* k, const void* v,
+                       const float* log_alpha, const void* beta, float* state_inout, void* out,
+                       kda_stream_t stream, const void* gate, const float* norm_w, float norm_eps) {
     kda_status st = check_shape(shape);
     if (st != KDA_OK) return st;
     if (shape->num_seqs == 0) return shape->total_tokens == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
@@ -180,9 +209,29 @@ kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
     if (!aligned(state_inout, 16)) return KDA_ERR_UNSUPPORTED;
     kda::DecodeArgs a{q, k, v, log_alpha, beta, state_inout, out, shape->num_seqs, (int32_t)tps, shape->H,
                       shape->dk, shape->dv,
-                      shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
+                      shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, gate, norm_w, norm_eps};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return finish(kda::launch_decode(a, s), s);
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k, const void* v,
+                           const float* log_alpha, const void* beta, float* state_inout,
+                           void* out, kda_stream_t stream) {
+    return decode_impl(shape, q, k, v, log_alpha, beta, state_inout, out, stream, nullptr, nullptr, 0.f);
+}
+
+kda_status kda_decode_step_gated(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const void* beta, const void* gate,
+                                 const float* norm_weight, float norm_eps, float* state_inout, void* out,
+                                 kda_stream_t stream) {
+    if (shape && shape->total_tokens > 0) {
+        const kda_status st = check_gate(shape, gate, norm_weight, norm_eps);
+        if (st != KDA_OK) return st;
+    }
+    return decode_impl(shape, q, k, v, log_alpha, beta, state_inout, out, stream, gate, norm_weight, norm_eps);
 }
 
 kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, const void* q_raw,

@@ -126,14 +126,16 @@ struct Small {
     int cmd_b;                                   // slot of the packed chunk, -1: group B is done
     int issued[3][2];                            // TMA loads issued / waited for, per
     int consumed[3][2];                          //   (kind, slot), to drain after a timeout
-    float beta[2][C];
+    __nv_bfloat16 beta[2][C];                    // bf16 inputs: exact
     float gam[2][D];
+    float nacc[C];                               // gated output: per-token sums of squares, then 1/rms
 #ifdef KDA_PHASE_TIMING
     unsigned long long phase[32];                // diagnostic build only
 #endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
 static_assert(offsetof(Small, gam) % 16 == 0, "gamma rows are read as float4");
+static_assert(offsetof(Small, nacc) % 8 == 0, "1/rms pairs are read as float2");
 
 __device__ __forceinline__ uint32_t qk_off(bool is_q, uint32_t r, uint32_t c) {
     return (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
@@ -283,7 +285,7 @@ __device__ __forceinline__ int blk_at(int r, int c) { return r * kBlkStride + (c
 // lower-triangular 16x16 blocks in the A slot.  Lanes 64-127 hold P rows r:
 // P_rs (s <= r) as the bf16 K-major operand tile.  Team S: each thread takes
 // its lane's row, columns 0-31 then 32-63.
-__device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp, const float* beta) {
+__device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp, const __nv_bfloat16* beta) {
     const int row = (int)lane0() + (lt() & 31);
 #pragma unroll 1
     for (int ch = 0; ch < 2; ++ch) {                 // column half
@@ -292,7 +294,7 @@ __device__ void read_gram(uint32_t tb, uint32_t col, uint8_t* aslot, uint8_t* pp
         tmem_wait_ld();
         if (row < 64) {
             const int r = row, bi = r >> 4, rr = r & 15;
-            const float b = beta[r];
+            const float b = bf2f(beta[r]);
             float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -374,7 +376,7 @@ __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP],
 // X_10 = -D_1 N_10 D_0, X_32 = -D_3 N_32 D_2; then the lower-left 32x32 quarter
 // -C^{-1} (B A^{-1}) with A^{-1}, C^{-1} the inverted halves and B = N[32:64, 0:32], using TF32
 // tensor-core block products with fp32 accumulation.  Team S (4 warps), 4 team barriers.
-__device__ void solve_T(uint8_t* aslot, const float* beta) {
+__device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
     float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
     float* Xb = reinterpret_cast<float*>(aslot + kSolveX);
     float* Yb = reinterpret_cast<float*>(aslot + kSolveY);   // 4 blocks
@@ -462,7 +464,7 @@ __device__ void solve_T(uint8_t* aslot, const float* beta) {
                 const float xr[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    wv[u] = pack_bf16x2(xr[2 * u] * beta[s0 + 2 * u], xr[2 * u + 1] * beta[s0 + 2 * u + 1]);
+                    wv[u] = pack_bf16x2(xr[2 * u] * bf2f(beta[s0 + 2 * u]), xr[2 * u + 1] * bf2f(beta[s0 + 2 * u + 1]));
             } else {
                 wv[0] = wv[1] = wv[2] = wv[3] = 0u;
             }
@@ -573,8 +575,10 @@ __device__ void store_state(uint32_t tb, float* hT, size_t base) {
 // range: the state row of lane j (value channel) is updated in fp32 with the
 // recurrence itself (decay, erase with beta, write with beta, read after the
 // write).  log_alpha in the A slot is first turned into alpha in place.
+// The outputs o_r go to TMEM column ucol + r of the thread's lane (its value
+// channel), where the chunk's output is stored from like any other chunk's.
 __device__ __noinline__ void token_chunk(uint32_t tb, float* A, const uint8_t* qk, const uint8_t* vv,
-                            const float* beta, __nv_bfloat16* out, int64_t t0, int H, int h, int L) {
+                            const __nv_bfloat16* beta, uint32_t ucol, int L) {
     const int j = lt();
     for (int r = 0; r < L; ++r) A[r * D + j] = expf(A[r * D + j]);
     group_sync(kBarB);
@@ -596,14 +600,14 @@ __device__ __noinline__ void token_chunk(uint32_t tb, float* A, const uint8_t* q
             rk = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), rk);
         }
         const float vj = bf2f(*reinterpret_cast<const __nv_bfloat16*>(vv + half_off(r, j)));
-        const float d = beta[r] * (vj - rk);
+        const float d = bf2f(beta[r]) * (vj - rk);
         float y = 0.f;
 #pragma unroll
         for (int c = 0; c < D; ++c) {
             s[c] = fmaf(bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), d, s[c]);
             y = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(true, r, c))), y);
         }
-        out[((t0 + r) * H + h) * D + j] = __float2bfloat16_rn(y);
+        tmem_st1(tmem_addr(tb, lane0(), ucol + r), __float_as_uint(y));
     }
 #pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
@@ -810,7 +814,7 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         if (n >= 2 && !(ok = group_wait(kBarP, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_TRACE(n, 4);
         KDA_PHASE(2);
-        if (t < C) sw.beta[s][t] = (t < L) ? braw : 0.f;
+        if (t < C) sw.beta[s][t] = __float2bfloat16_rn((t < L) ? braw : 0.f);
         if (!(ok = group_wait(kBarP, &sw.qk_full[s], ph))) break;
         KDA_TRACE(n, 5);
         KDA_PHASE(3);
@@ -983,12 +987,93 @@ __device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint
     __syncwarp();
 }
 
+// Optional gated output of the layer (RMSNorm over the value channels of each
+// token, a weight per channel, times sigmoid(gate)); gate == nullptr: plain output.
+struct Epi {
+    const __nv_bfloat16* gate;
+    float w;                                         // this thread's channel weight
+    float eps;
+};
+
+// Sum over the 32 lanes of per-lane values v[i] (value i belongs to token i):
+// lane L returns the warp's sum for token L (a reduce-scatter, 31 shuffles).
+__device__ __forceinline__ float lane_sums32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+// Gated output of one chunk held in TMEM (lane = value channel, column = token):
+// the per-token 1/rms from the four warps' squares (shared-memory sums), then
+// o * (1/rms) * w * sigmoid(g) packed to bf16 pairs of rows.  The gate rows are
+// read as 4-byte channel pairs and split between the two lanes of each pair.
+__device__ __forceinline__ void o_gated_to_regs(const Ctx& x, uint32_t col, int64_t t0, int L, const Epi& e,
+                                                uint32_t (&opk)[32]) {
+    Small& sw = *x.sw;
+    const int t = lt();
+    const bool odd = t & 1;
+    if (t < C) sw.nacc[t] = 0.f;
+    const __nv_bfloat16* g0 = e.gate + (t0 * x.H + x.h) * D + (t & ~1);
+    const size_t rs = (size_t)x.H * D;
+    uint32_t graw[32];                               // row 2i (even lane) or 2i+1 (odd lane), channel pair
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int r = 2 * i + (odd ? 1 : 0);
+        graw[i] = (r < L) ? *reinterpret_cast<const uint32_t*>(g0 + (size_t)r * rs) : 0u;
+    }
+    group_sync(kBarB);                               // nacc cleared
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        float v[32];
+        tmem_ld32(tmem_addr(x.tb, lane0(), col + 32 * hf), *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= v[i];
+        atomicAdd(&sw.nacc[32 * hf + (t & 31)], lane_sums32(v));
+    }
+    group_sync(kBarB);                               // all squares in
+    if (t < C) sw.nacc[t] = rsqrtf(sw.nacc[t] * (1.f / D) + e.eps);
+    group_sync(kBarB);                               // 1/rms ready
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(x.tb, lane0(), col + 32 * hf), u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int pr = 16 * hf + i;              // row pair: rows 2 pr, 2 pr + 1
+            const uint32_t mine = graw[pr];
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
+            // this lane's channel: row 2pr in the low half, row 2pr+1 in the high half
+            const uint32_t gw = odd ? ((got & 0xffffu) | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
+            const float ga = __uint_as_float(gw << 16), gb = __uint_as_float(gw & 0xffff0000u);
+            const float2 rr = *reinterpret_cast<const float2*>(&sw.nacc[2 * pr]);
+            const float oa = __uint_as_float(u[2 * i]) * rr.x * e.w * __fdividef(1.f, 1.f + __expf(-ga));
+            const float ob = __uint_as_float(u[2 * i + 1]) * rr.y * e.w * __fdividef(1.f, 1.f + __expf(-gb));
+            opk[pr] = pack_bf16x2(oa, ob);
+        }
+    }
+}
+
 // Store the output a chunk left in its U slot, then release that U slot to
 // team S (one arrival per warp, once its TMEM reads are done).
+template <bool kGated>
 __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_bfloat16* out, int prev_s,
-                                           int64_t prev_t0, int prev_L, bool leader) {
+                                           int64_t prev_t0, int prev_L, const Epi& e) {
     uint32_t opk[32];
-    o_to_regs(x.tb, tm_u(prev_s), opk);
+    if constexpr (kGated)
+        o_gated_to_regs(x, tm_u(prev_s), prev_t0, prev_L, e, opk);
+    else
+        o_to_regs(x.tb, tm_u(prev_s), opk);
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&x.sw->u_free[prev_s]);
@@ -1027,11 +1112,14 @@ __device__ __noinline__ void run_producer(const Ctx& x_in, const Maps& maps) {
 }
 
 // ============================ group B loop =======================================
+template <bool kGated>
 __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv_bfloat16* __restrict__ out,
                             const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
-                            const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
+                            const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states,
+                            const __nv_bfloat16* gate, const float* norm_w, float norm_eps) {
     const Ctx x = x_in;
     Small& sw = *x.sw;
+    const Epi epi{gate, kGated ? norm_w[lt()] : 0.f, norm_eps};
     Ckpt ck;
     ck.init(ck_cu, ck_pos, ck_states, x.seq);
     const int t = lt();
@@ -1061,21 +1149,20 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
             if (have_prev) {
-                flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
+                flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
                 have_prev = false;
             }
-            token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], out, t0, x.H, x.h, L);
+            token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], tm_u(s), L);
             tc_fence_before();
             group_sync(kBarB);
             tc_fence_after();
             ck.after_chunk(x.tb, t0 + L - x.bos, t0 + L == x.eos, x.H, x.h);
-            if (leader) {
+            if (leader) {                                // the U slot is released when its output is stored
                 mbar_arrive(&sw.kbp_free[s]);
-                for (int w_ = 0; w_ < 4; ++w_)           // no output in this U slot: the four
-                    mbar_arrive(&sw.u_free[s]);          //   per-warp arrivals at once
                 mbar_arrive(&sw.av_free[s]);
                 mbar_arrive(&sw.qk_free[s]);
             }
+            have_prev = true; prev_s = s; prev_L = L; prev_t0 = t0;
             continue;
         }
         decay_state(x.tb, sw.gam[s]);
@@ -1104,7 +1191,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         KDA_PHASE(22);
         KDA_TRACE(n, 12);
         if (have_prev) {                                 // previous output, under this chunk's MMAs
-            flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
+            flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
             have_prev = false;
         }
         KDA_PHASE(16);
@@ -1123,7 +1210,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         KDA_TRACE(n, 15);
     }
     if (ok) {
-        if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L, leader);
+        if (have_prev) flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
         if (hT) store_state(x.tb, hT, sbase);
     } else if (mma1_pending) {
         mbar_wait_bounded(&sw.mma1_done, m1_ph, kWaitLimitNs);
@@ -1136,12 +1223,15 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     return ok;
 }
 
+// kGated: the layer's gated RMSNorm is applied to each chunk's output before its store.
+template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
                 const float* __restrict__ h0, const int32_t* __restrict__ cu,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ hT, int64_t T, int num_seqs,
                 int H, unsigned int* status, const int32_t* __restrict__ ck_cu,
-                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states) {
+                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states,
+                const __nv_bfloat16* __restrict__ gate, const float* __restrict__ norm_w, float norm_eps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1207,7 +1297,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     else if (in_group_a())
         ok = run_team_s(x);
     else if (tid < kProducer)
-        ok = run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
+        ok = run_group_b<kGated>(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states, gate, norm_w, norm_eps);
     else if (tid == kProducer)
         run_producer(x, maps);
 
@@ -1293,18 +1383,26 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
         !make_map(&maps.o, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 32,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemDynamic);
+    // the shared-memory opt-in is a per-device property of each kernel instance
+    static bool attr_set[2][64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const bool gated = a.gate != nullptr;
+    if (!attr_set[gated][dev]) {
+        cudaError_t e = gated ? cudaFuncSetAttribute(chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)kSmemDynamic)
+                              : cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     (int)kSmemDynamic);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[gated][dev] = true;
     }
     const unsigned blocks = (unsigned)((int64_t)a.num_seqs * a.H);
-    chunk_tc_kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
+    auto kernel = gated ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
+    kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
         maps, static_cast<const __nv_bfloat16*>(a.beta), a.initial_state, a.cu_seqlens,
         static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.status,
-        a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
+        a.ckpt_cu, a.ckpt_pos, a.ckpt_states, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w,
+        a.norm_eps);
     return cudaGetLastError();
 }
 

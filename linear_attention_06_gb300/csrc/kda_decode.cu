@@ -42,7 +42,8 @@ template <int DK, int DV, typename Tin>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ log_alpha, const Tin* __restrict__ beta,
-              float* __restrict__ S, Tin* __restrict__ out, int H, int T) {
+              float* __restrict__ S, Tin* __restrict__ out, int H, int T,
+              const Tin* __restrict__ gate, const float* __restrict__ norm_w, float norm_eps) {
     constexpr int LANES = DV / 4;          // threads per row (float4 each)
     constexpr int RG = kThreads / LANES;   // row groups
     constexpr int RPT = DK / RG;           // rows per thread
@@ -62,6 +63,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     __shared__ float ks[DK], qs[DK], al[DK], vs[DV], dl[DV];
     __shared__ float red_r[RG][DV], red_y[RG][DV];
     __shared__ float kq_s;
+    __shared__ float red_n[DV / 32];
     __shared__ float beta_s;
     // The T tokens of this sequence are rows n*T .. n*T+T-1; the state stays in
     // registers between them and crosses HBM once in each direction.
@@ -99,13 +101,32 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         *reinterpret_cast<float4*>(&red_y[g][4 * c4]) = y;
         __syncthreads();
 
-        for (int j = threadIdx.x; j < DV; j += kThreads) {
+        static_assert(DV <= kThreads, "one output channel per thread");
+        const int j = threadIdx.x;
+        float oj = 0.f;
+        if (j < DV) {
             float rj = 0.f, yj = 0.f;
 #pragma unroll
             for (int gg = 0; gg < RG; ++gg) { rj += red_r[gg][j]; yj += red_y[gg][j]; }
             const float d = beta_s * (vs[j] - rj);
             dl[j] = d;
-            store_as(&out[row * DV + j], fmaf(kq_s, d, yj));
+            oj = fmaf(kq_s, d, yj);
+            if (!gate) store_as(&out[row * DV + j], oj);
+        }
+        if (gate) {   // gated output: RMSNorm over the DV channels (warps 0 .. DV/32-1) x weight x sigmoid(gate)
+            float ss = oj * oj;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if ((j & 31) == 0 && j < DV) red_n[j >> 5] = ss;
+            __syncthreads();
+            if (j < DV) {
+                float tot = 0.f;
+#pragma unroll
+                for (int w = 0; w < DV / 32; ++w) tot += red_n[w];
+                const float r = rsqrtf(tot * (1.f / DV) + norm_eps);
+                const float gv = to_f32(gate[row * DV + j]);
+                store_as(&out[row * DV + j], oj * r * norm_w[j] / (1.f + __expf(-gv)));
+            }
         }
         __syncthreads();
 
@@ -129,13 +150,14 @@ cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
         decode_kernel<DK, DV, float><<<blocks, kThreads, 0, st>>>(
             static_cast<const float*>(a.q), static_cast<const float*>(a.k),
             static_cast<const float*>(a.v), a.log_alpha, static_cast<const float*>(a.beta),
-            a.state, static_cast<float*>(a.out), a.H, a.tokens_per_seq);
+            a.state, static_cast<float*>(a.out), a.H, a.tokens_per_seq, static_cast<const float*>(a.gate),
+            a.norm_w, a.norm_eps);
     } else {
         decode_kernel<DK, DV, __nv_bfloat16><<<blocks, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
             static_cast<const __nv_bfloat16*>(a.v), a.log_alpha,
             static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out), a.H,
-            a.tokens_per_seq);
+            a.tokens_per_seq, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w, a.norm_eps);
     }
     return cudaGetLastError();
 }

@@ -31,6 +31,11 @@ struct PrefillArgs {
     const int32_t* ckpt_cu = nullptr;
     const int32_t* ckpt_pos = nullptr;
     float* ckpt_states = nullptr;
+    // optional gated output: out = o / sqrt(mean_j o_j^2 + norm_eps) * norm_w * sigmoid(gate)
+    // per (token, head); gate [T, H, dv] in dtype, norm_w [dv] fp32 (all null when not requested)
+    const void* gate = nullptr;
+    const float* norm_w = nullptr;
+    float norm_eps = 0.f;
 };
 
 struct DecodeArgs {
@@ -45,7 +50,13 @@ struct DecodeArgs {
     int32_t tokens_per_seq;       // T >= 1: rows n*T .. n*T+T-1 belong to sequence n
     int32_t H, dk, dv;
     DType dtype;
+    const void* gate = nullptr;   // optional gated output, as in PrefillArgs
+    const float* norm_w = nullptr;
+    float norm_eps = 0.f;
 };
+// In-place gated RMSNorm over rows of dv values (after the fp32 recurrent prefill).
+cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float eps, int64_t rows, int dv,
+                              DType dt, cudaStream_t s);
 
 // Layer front end: projections -> recurrence inputs (see kda_frontend in kda.h).
 struct FrontendArgs {

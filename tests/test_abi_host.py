@@ -163,3 +163,29 @@ def test_frontend_rejects_pointers_and_shapes(L):
     assert frontend_call(L, shape(dk=96)) == 2                    # unsupported head size
     assert frontend_call(L, shape(n=3, T=128)) == 1               # T % N without cu_seqlens
     assert frontend_call(L, shape(n=0, T=0)) == 0                 # empty: nothing enqueued
+
+
+def gated_prefill_call(L, sh, gate=FAKE, w=FAKE, eps=1e-6):
+    P = ctypes.c_void_p
+    return L.kda_prefill_gated(ctypes.byref(sh), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), None, None,
+                               P(gate), P(w), ctypes.c_float(eps), P(FAKE), None, None)
+
+
+def test_gated_prefill_rejects_gate_arguments(L):
+    assert gated_prefill_call(L, shape(), gate=0) == 1
+    assert gated_prefill_call(L, shape(), w=0) == 1
+    assert gated_prefill_call(L, shape(), eps=-1.0) == 1
+    assert gated_prefill_call(L, shape(), eps=float("nan")) == 1
+    assert gated_prefill_call(L, shape(), gate=FAKE_MIS) == 2
+    assert gated_prefill_call(L, shape(n=0, T=0), gate=0) == 0      # empty: nothing checked, nothing enqueued
+
+
+def test_gated_decode_rejects_gate_arguments(L):
+    P = ctypes.c_void_p
+    sh = shape(n=4, T=4)
+    call = lambda g, w, e: L.kda_decode_step_gated(ctypes.byref(sh), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                                                   P(FAKE), P(g), P(w), ctypes.c_float(e), P(FAKE), P(FAKE), None)
+    assert call(0, FAKE, 1e-6) == 1
+    assert call(FAKE, 0, 1e-6) == 1
+    assert call(FAKE, FAKE, -2.0) == 1
+    assert call(FAKE_MIS, FAKE, 1e-6) == 2

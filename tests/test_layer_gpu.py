@@ -91,3 +91,78 @@ def test_frontend_output_feeds_prefill():
     n = q.float().norm(dim=-1)
     assert torch.allclose(n, torch.ones_like(n), atol=1e-2)
     assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
+
+
+# ---- gated output (RMSNorm x weight x sigmoid(gate)) after the recurrence ----------
+
+def gated_ref(w, x, heads=None, eps=1e-6):
+    from tests.gpu_helpers import oracle_prefill
+    sel = slice(None) if heads is None else list(heads)
+    ro, rf = oracle_prefill(w, heads)
+    return lo.gated_rmsnorm(ro, np64(x.g_raw[:, sel]), np64(x.norm_weight), eps), rf
+
+
+def run_gated(w, x, eps=1e-6):
+    d = w.to(DEV)
+    out, fin = kda.kda_prefill_gated(d.q, d.k, d.v, d.log_alpha, d.beta, x.g_raw.to(DEV),
+                                     x.norm_weight.to(DEV), norm_eps=eps, initial_state=d.initial_state,
+                                     cu_seqlens=d.cu_seqlens, final_state=True)
+    plain_out, plain_fin = kda.kda_prefill(d.q, d.k, d.v, d.log_alpha, d.beta, d.initial_state, d.cu_seqlens,
+                                           final_state=True)
+    torch.cuda.synchronize()
+    return out, fin, plain_fin
+
+
+@pytest.mark.parametrize("mode", ["plain", "token_chunks", "ragged_only"])
+def test_prefill_gated_tensor_core_path(mode):
+    cu = [0, 64, 214, 300] if mode != "ragged_only" else [0, 37, 100]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, dtype=torch.bfloat16, seed=61, cu_seqlens=cu, state_std=0.05)
+    if mode == "token_chunks":
+        w.log_alpha[70::41, :, ::4] = float("-inf")   # some chunks run token by token
+    x = workloads.make_layer_inputs(cu[-1], 2, 128, 128, dtype=torch.bfloat16, seed=62, cu_seqlens=cu)
+    out, fin, plain_fin = run_gated(w, x)
+    ro, rf = gated_ref(w, x)
+    e_out = rel_l2(np64(out), ro)
+    assert e_out <= 5e-3, f"gated out rel L2 {e_out:.3e}"
+    assert torch.equal(fin, plain_fin)                 # the gate does not touch the state
+    assert rel_l2(np64(fin), rf) <= 5e-3
+
+
+def test_prefill_gated_recurrent_path_fp32():
+    cu = [0, 50, 130]
+    w = workloads.make_inputs(cu[-1], 2, 64, 64, dtype=torch.float32, seed=63, cu_seqlens=cu)
+    x = workloads.make_layer_inputs(cu[-1], 2, 64, 64, dtype=torch.float32, seed=64, cu_seqlens=cu)
+    out, fin, _ = run_gated(w, x, eps=1e-5)
+    ro, _ = gated_ref(w, x, eps=1e-5)
+    assert rel_l2(np64(out), ro) <= 1e-4
+
+
+def test_prefill_gated_full_size_sampled_heads():
+    w = workloads.prefill_bf16(device=DEV)
+    x = workloads.make_layer_inputs(w.total_tokens, 32, 128, 128, dtype=torch.bfloat16, seed=65,
+                                    num_seqs=4, device=DEV)
+    out, fin, plain_fin = run_gated(w, x)
+    heads = [3, 30]
+    ro, _ = gated_ref(w, x, heads=heads)
+    assert rel_l2(np64(out[:, heads]), ro) <= 5e-3
+    assert torch.equal(fin, plain_fin)
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_decode_gated(T):
+    from oracle import kda_oracle
+    n = 6
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, 4, 128, 128, dtype=torch.bfloat16, seed=66 + T, cu_seqlens=cu,
+                              state_std=0.05)
+    x = workloads.make_layer_inputs(n * T, 4, 128, 128, dtype=torch.bfloat16, seed=67, cu_seqlens=cu)
+    d = w.to(DEV)
+    S = d.initial_state.clone()
+    out = kda.kda_decode_step_gated(d.q, d.k, d.v, d.log_alpha, d.beta, x.g_raw.to(DEV), x.norm_weight.to(DEV),
+                                    S, norm_eps=1e-6)
+    torch.cuda.synchronize()
+    ro, rf = kda_oracle.prefill(np64(w.q), np64(w.k), np64(w.v), np64(w.log_alpha), np64(w.beta),
+                                np64(w.initial_state), cu_seqlens=cu)
+    ref = lo.gated_rmsnorm(ro, np64(x.g_raw), np64(x.norm_weight), 1e-6)
+    assert rel_l2(np64(out), ref) <= 5e-3
+    assert rel_l2(np64(S), rf) <= 5e-3
