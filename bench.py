@@ -41,6 +41,14 @@ def prefill_bytes(tokens, heads, num_seqs, with_h0=False):
     return tokens * heads * BYTES_PER_TOKEN_HEAD + num_seqs * heads * D * D * 4 * (2 if with_h0 else 1)
 
 
+def frontend_bytes(tokens, heads, d=128, width=4):
+    """Front end, bf16 (d = dk = dv): raw q, k, v read and q, k, v written (2 B each),
+    decay logits read and log_alpha written (4 B), beta logits and beta (2 B), plus the
+    fp32 convolution taps."""
+    per = 3 * d * 2 * 2 + d * 4 * 2 + 2 * 2
+    return tokens * heads * per + 3 * heads * d * width * 4
+
+
 def decode_bytes(n, heads):
     # state read + write (fp32) + q, k, v, out bf16 + log_alpha fp32 + beta bf16
     return n * heads * (2 * D * D * 4 + 4 * D * 2 + D * 4 + 2)
@@ -280,6 +288,35 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     t_decode = max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+
+    # ---- the layer steps around the recurrence, on the same workload shapes
+    layer = None
+    if not args.no_layer:
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            barrier()
+            ev0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            return max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+
+        lx = workloads.make_layer_inputs(B * T, H, D, D, W=4, dtype=torch.bfloat16, seed=11 + rank,
+                                         num_seqs=B, device=dev)
+        fe_out = tuple(torch.empty_like(t) for t in (w.q, w.k, w.v, w.log_alpha, w.beta))
+        t_fe = timed(lambda: kda.kda_frontend(lx.q_raw, lx.k_raw, lx.v_raw, lx.a_raw, lx.b_raw, lx.conv_q,
+                                              lx.conv_k, lx.conv_v, num_seqs=B, out=fe_out, stream=stream))
+        t_pg = timed(lambda: kda.kda_prefill_gated(w.q, w.k, w.v, w.log_alpha, w.beta, lx.g_raw, lx.norm_weight,
+                                                   cu_seqlens=cu, out=out, final_state=fin, stream=stream))
+        gx = workloads.make_layer_inputs(DEC_N, H, D, D, dtype=torch.bfloat16, seed=12 + rank,
+                                         cu_seqlens=list(range(DEC_N + 1)), device=dev)
+        t_dg = timed(lambda: kda.kda_decode_step_gated(dw.q, dw.k, dw.v, dw.log_alpha, dw.beta, gx.g_raw,
+                                                       gx.norm_weight, S, out=dout, stream=stream))
+        layer = {"t_fe": t_fe, "t_pg": t_pg, "t_dg": t_dg}
     clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers (pinned)
@@ -344,6 +381,25 @@ def run_ours(args):
                    "algorithmic_bytes_per_launch": dbytes, "kernel": "decode_kernel"},
         "e2e": e2e, "gpu_launches": prefill_launches, "clocks": clocks,
     }
+    if layer is not None:
+        fbytes = frontend_bytes(B * T, H)
+        gbytes = pbytes + B * T * H * D * 2                  # + the bf16 gate read once
+        dgbytes = dbytes + DEC_N * H * D * 2
+        line["layer"] = {
+            "frontend": {"workload": f"kda_frontend_bf16_B{B}_H{H}_T{T}_d{D}_W4",
+                         "us_per_step": layer["t_fe"] * 1e6, "achieved_gbs": fbytes / layer["t_fe"] / 1e9,
+                         "peak_gbs": hbm, "frac": fbytes / layer["t_fe"] / 1e9 / hbm,
+                         "algorithmic_bytes_per_launch": fbytes, "kernel": "frontend_kernel"},
+            "prefill_gated": {"workload": WORKLOAD + "_gated", "ms_per_step": layer["t_pg"] * 1e3,
+                              "value": world * B * T / layer["t_pg"], "unit": UNIT,
+                              "achieved_gbs": gbytes / layer["t_pg"] / 1e9,
+                              "frac": gbytes / layer["t_pg"] / 1e9 / hbm,
+                              "algorithmic_bytes_per_launch": gbytes, "kernel": "chunk_tc_kernel<gated>"},
+            "decode_gated": {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}_gated",
+                             "us_per_step": layer["t_dg"] * 1e6, "achieved_gbs": dgbytes / layer["t_dg"] / 1e9,
+                             "frac": dgbytes / layer["t_dg"] / 1e9 / hbm,
+                             "algorithmic_bytes_per_launch": dgbytes, "kernel": "decode_kernel<gated>"},
+        }
     if world == 1 and not args.no_cpu_baseline:
         run, nseq, cores, used = oracle_sample(args.cpu_budget)
         t = run()
@@ -362,6 +418,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-layer", action="store_true", help="skip the front-end / gated-output timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-budget", type=float, default=4.0,

@@ -146,8 +146,8 @@ kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const
  * gate:        [T, H, dv] in dtype, the gate logits, 16-byte aligned.
  * norm_weight: [dv] fp32.   norm_eps: finite, >= 0.
  * All other arguments are those of kda_prefill; final_state is unchanged by the
- * gate.  The tensor-core path applies the gate in its output stores; the fp32
- * recurrent path applies it in a second pass over out.
+ * gate.  The gate is applied by a second, memory-bound pass over out on the same
+ * stream (one read of o and of the gate, one write).
  * Errors: those of kda_prefill, plus KDA_ERR_INVALID_ARG for a NULL gate or
  *   weight or a bad eps and KDA_ERR_UNSUPPORTED for a misaligned gate.
  */

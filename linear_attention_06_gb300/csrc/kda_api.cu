@@ -127,14 +127,13 @@ kda_status prefill_impl(const kda_shape* shape, const void* q, const void* k, co
     const char* force = getenv("KDA_PREFILL_IMPL");
     const bool want_recurrent = force && strcmp(force, "recurrent") == 0;
     cudaError_t e;
-    if (!want_recurrent && kda::chunk_tc_supported(a)) {
-        e = kda::launch_chunk_tc_prefill(a, s);            // gated output fused into its stores
-    } else {
+    if (!want_recurrent && kda::chunk_tc_supported(a))
+        e = kda::launch_chunk_tc_prefill(a, s);
+    else
         e = kda::launch_recurrent_prefill(a, s);
-        if (e == cudaSuccess && gate)                      // then a row pass over the outputs
-            e = kda::launch_gated_norm(out, gate, norm_w, norm_eps, shape->total_tokens * shape->H,
-                                       shape->dv, a.dtype, s);
-    }
+    if (e == cudaSuccess && gate)                          // gated output: one row pass over out
+        e = kda::launch_gated_norm(out, gate, norm_w, norm_eps, shape->total_tokens * shape->H,
+                                   shape->dv, a.dtype, s);
     return finish(e, s);
 }
 }  // namespace

@@ -128,14 +128,12 @@ struct Small {
     int consumed[3][2];                          //   (kind, slot), to drain after a timeout
     __nv_bfloat16 beta[2][C];                    // bf16 inputs: exact
     float gam[2][D];
-    float nacc[C];                               // gated output: per-token sums of squares, then 1/rms
 #ifdef KDA_PHASE_TIMING
     unsigned long long phase[32];                // diagnostic build only
 #endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
 static_assert(offsetof(Small, gam) % 16 == 0, "gamma rows are read as float4");
-static_assert(offsetof(Small, nacc) % 8 == 0, "1/rms pairs are read as float2");
 
 __device__ __forceinline__ uint32_t qk_off(bool is_q, uint32_t r, uint32_t c) {
     return (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
@@ -987,93 +985,12 @@ __device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint
     __syncwarp();
 }
 
-// Optional gated output of the layer (RMSNorm over the value channels of each
-// token, a weight per channel, times sigmoid(gate)); gate == nullptr: plain output.
-struct Epi {
-    const __nv_bfloat16* gate;
-    float w;                                         // this thread's channel weight
-    float eps;
-};
-
-// Sum over the 32 lanes of per-lane values v[i] (value i belongs to token i):
-// lane L returns the warp's sum for token L (a reduce-scatter, 31 shuffles).
-__device__ __forceinline__ float lane_sums32(float (&v)[32]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = lane & o;
-#pragma unroll
-        for (int i = 0; i < o; ++i) {
-            const float send = up ? v[i] : v[i + o];
-            const float keep = up ? v[i + o] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0];
-}
-
-// Gated output of one chunk held in TMEM (lane = value channel, column = token):
-// the per-token 1/rms from the four warps' squares (shared-memory sums), then
-// o * (1/rms) * w * sigmoid(g) packed to bf16 pairs of rows.  The gate rows are
-// read as 4-byte channel pairs and split between the two lanes of each pair.
-__device__ __forceinline__ void o_gated_to_regs(const Ctx& x, uint32_t col, int64_t t0, int L, const Epi& e,
-                                                uint32_t (&opk)[32]) {
-    Small& sw = *x.sw;
-    const int t = lt();
-    const bool odd = t & 1;
-    if (t < C) sw.nacc[t] = 0.f;
-    const __nv_bfloat16* g0 = e.gate + (t0 * x.H + x.h) * D + (t & ~1);
-    const size_t rs = (size_t)x.H * D;
-    uint32_t graw[32];                               // row 2i (even lane) or 2i+1 (odd lane), channel pair
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = 2 * i + (odd ? 1 : 0);
-        graw[i] = (r < L) ? *reinterpret_cast<const uint32_t*>(g0 + (size_t)r * rs) : 0u;
-    }
-    group_sync(kBarB);                               // nacc cleared
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
-        float v[32];
-        tmem_ld32(tmem_addr(x.tb, lane0(), col + 32 * hf), *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= v[i];
-        atomicAdd(&sw.nacc[32 * hf + (t & 31)], lane_sums32(v));
-    }
-    group_sync(kBarB);                               // all squares in
-    if (t < C) sw.nacc[t] = rsqrtf(sw.nacc[t] * (1.f / D) + e.eps);
-    group_sync(kBarB);                               // 1/rms ready
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(x.tb, lane0(), col + 32 * hf), u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int pr = 16 * hf + i;              // row pair: rows 2 pr, 2 pr + 1
-            const uint32_t mine = graw[pr];
-            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
-            // this lane's channel: row 2pr in the low half, row 2pr+1 in the high half
-            const uint32_t gw = odd ? ((got & 0xffffu) | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
-            const float ga = __uint_as_float(gw << 16), gb = __uint_as_float(gw & 0xffff0000u);
-            const float2 rr = *reinterpret_cast<const float2*>(&sw.nacc[2 * pr]);
-            const float oa = __uint_as_float(u[2 * i]) * rr.x * e.w * __fdividef(1.f, 1.f + __expf(-ga));
-            const float ob = __uint_as_float(u[2 * i + 1]) * rr.y * e.w * __fdividef(1.f, 1.f + __expf(-gb));
-            opk[pr] = pack_bf16x2(oa, ob);
-        }
-    }
-}
-
 // Store the output a chunk left in its U slot, then release that U slot to
 // team S (one arrival per warp, once its TMEM reads are done).
-template <bool kGated>
 __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_bfloat16* out, int prev_s,
-                                           int64_t prev_t0, int prev_L, const Epi& e) {
+                                           int64_t prev_t0, int prev_L) {
     uint32_t opk[32];
-    if constexpr (kGated)
-        o_gated_to_regs(x, tm_u(prev_s), prev_t0, prev_L, e, opk);
-    else
-        o_to_regs(x.tb, tm_u(prev_s), opk);
+    o_to_regs(x.tb, tm_u(prev_s), opk);
     tc_fence_before();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&x.sw->u_free[prev_s]);
@@ -1112,14 +1029,11 @@ __device__ __noinline__ void run_producer(const Ctx& x_in, const Maps& maps) {
 }
 
 // ============================ group B loop =======================================
-template <bool kGated>
 __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv_bfloat16* __restrict__ out,
                             const float* __restrict__ h0, float* __restrict__ hT, size_t sbase,
-                            const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states,
-                            const __nv_bfloat16* gate, const float* norm_w, float norm_eps) {
+                            const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states) {
     const Ctx x = x_in;
     Small& sw = *x.sw;
-    const Epi epi{gate, kGated ? norm_w[lt()] : 0.f, norm_eps};
     Ckpt ck;
     ck.init(ck_cu, ck_pos, ck_states, x.seq);
     const int t = lt();
@@ -1149,7 +1063,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
             if (have_prev) {
-                flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
+                flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
                 have_prev = false;
             }
             token_chunk(x.tb, reinterpret_cast<float*>(aslot), qk, vs, sw.beta[s], tm_u(s), L);
@@ -1191,7 +1105,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         KDA_PHASE(22);
         KDA_TRACE(n, 12);
         if (have_prev) {                                 // previous output, under this chunk's MMAs
-            flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
+            flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
             have_prev = false;
         }
         KDA_PHASE(16);
@@ -1210,7 +1124,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         KDA_TRACE(n, 15);
     }
     if (ok) {
-        if (have_prev) flush_prev<kGated>(x, maps, out, prev_s, prev_t0, prev_L, epi);
+        if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
         if (hT) store_state(x.tb, hT, sbase);
     } else if (mma1_pending) {
         mbar_wait_bounded(&sw.mma1_done, m1_ph, kWaitLimitNs);
@@ -1223,15 +1137,12 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     return ok;
 }
 
-// kGated: the layer's gated RMSNorm is applied to each chunk's output before its store.
-template <bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
                 const float* __restrict__ h0, const int32_t* __restrict__ cu,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ hT, int64_t T, int num_seqs,
                 int H, unsigned int* status, const int32_t* __restrict__ ck_cu,
-                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states,
-                const __nv_bfloat16* __restrict__ gate, const float* __restrict__ norm_w, float norm_eps) {
+                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1297,7 +1208,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     else if (in_group_a())
         ok = run_team_s(x);
     else if (tid < kProducer)
-        ok = run_group_b<kGated>(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states, gate, norm_w, norm_eps);
+        ok = run_group_b(x, maps, out, h0, hT, sbase, ck_cu, ck_pos, ck_states);
     else if (tid == kProducer)
         run_producer(x, maps);
 
@@ -1383,26 +1294,21 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
         !make_map(&maps.o, a.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 32,
                   CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    // the shared-memory opt-in is a per-device property of each kernel instance
-    static bool attr_set[2][64] = {};
+    // the shared-memory opt-in is a per-device property of the kernel
+    static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const bool gated = a.gate != nullptr;
-    if (!attr_set[gated][dev]) {
-        cudaError_t e = gated ? cudaFuncSetAttribute(chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)kSmemDynamic)
-                              : cudaFuncSetAttribute(chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     (int)kSmemDynamic);
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemDynamic);
         if (e != cudaSuccess) return e;
-        attr_set[gated][dev] = true;
+        attr_set[dev] = true;
     }
     const unsigned blocks = (unsigned)((int64_t)a.num_seqs * a.H);
-    auto kernel = gated ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
-    kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
+    chunk_tc_kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
         maps, static_cast<const __nv_bfloat16*>(a.beta), a.initial_state, a.cu_seqlens,
         static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.status,
-        a.ckpt_cu, a.ckpt_pos, a.ckpt_states, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w,
-        a.norm_eps);
+        a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
     return cudaGetLastError();
 }
 

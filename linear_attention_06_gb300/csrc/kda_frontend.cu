@@ -42,6 +42,9 @@ __device__ __forceinline__ void load_row(const T* p, float (&x)[CPL]) {
     } else if constexpr (sizeof(T) == 4 && CPL == 4) {
         const float4 f = *reinterpret_cast<const float4*>(p);
         x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else if constexpr (sizeof(T) == 4 && CPL == 2) {
+        const float2 f = *reinterpret_cast<const float2*>(p);
+        x[0] = f.x; x[1] = f.y;
     } else {
 #pragma unroll
         for (int i = 0; i < CPL; ++i) x[i] = to_f(p[i]);
@@ -60,6 +63,8 @@ __device__ __forceinline__ void store_row(T* p, const float (&x)[CPL]) {
         *reinterpret_cast<__nv_bfloat162*>(p) = v;
     } else if constexpr (sizeof(T) == 4 && CPL == 4) {
         *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    } else if constexpr (sizeof(T) == 4 && CPL == 2) {
+        *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
     } else {
 #pragma unroll
         for (int i = 0; i < CPL; ++i) p[i] = from_f<T>(x[i]);
@@ -146,14 +151,14 @@ __global__ void __launch_bounds__(kWarps * 32) frontend_kernel(FrontendArgs a) {
 #pragma unroll
         for (int i = 0; i < W; ++i) wv[i][c] = a.conv_v[((int64_t)h * dv + cv + c) * W + i];
 
-    const T* qr = static_cast<const T*>(a.q_raw);
-    const T* kr = static_cast<const T*>(a.k_raw);
-    const T* vr = static_cast<const T*>(a.v_raw);
-    const T* br = static_cast<const T*>(a.b_raw);
-    T* qo = static_cast<T*>(a.q);
-    T* ko = static_cast<T*>(a.k);
-    T* vo = static_cast<T*>(a.v);
-    T* bo = static_cast<T*>(a.beta);
+    const T* __restrict__ qr = static_cast<const T*>(a.q_raw);
+    const T* __restrict__ kr = static_cast<const T*>(a.k_raw);
+    const T* __restrict__ vr = static_cast<const T*>(a.v_raw);
+    const T* __restrict__ br = static_cast<const T*>(a.b_raw);
+    T* __restrict__ qo = static_cast<T*>(a.q);
+    T* __restrict__ ko = static_cast<T*>(a.k);
+    T* __restrict__ vo = static_cast<T*>(a.v);
+    T* __restrict__ bo = static_cast<T*>(a.beta);
 
     int n = 0;
     int64_t bos = 0, eos = a.total_tokens;
@@ -182,7 +187,20 @@ __global__ void __launch_bounds__(kWarps * 32) frontend_kernel(FrontendArgs a) {
         }
     }
 
+    // software pipeline: the raw rows of token t+1 are in flight while token t is computed
+    float cq[CPK], ckk[CPK], cvv[CPV], ca[CPK], cb = 0.f;
+    auto fetch = [&](int64_t t, float (&xq)[CPK], float (&xk)[CPK], float (&xv)[CPV], float (&xa)[CPK], float& xb) {
+        const int64_t rk = (t * H + h) * dk + ck, rv = (t * H + h) * dv + cv;
+        load_row<T, CPK>(qr + rk, xq);
+        load_row<T, CPK>(kr + rk, xk);
+        load_row<T, CPV>(vr + rv, xv);
+        load_row<float, CPK>(a.a_raw + rk, xa);
+        xb = lane == 0 ? to_f(br[t * H + h]) : 0.f;
+    };
+    fetch(t_begin, cq, ckk, cvv, ca, cb);
     for (int64_t t = t_begin; t < t_end; ++t) {
+        float nq[CPK], nk[CPK], nv[CPV], na[CPK], nb = 0.f;
+        if (t + 1 < t_end) fetch(t + 1, nq, nk, nv, na, nb);
         if (t >= eos) {                                  // a new sequence starts here
             if (a.cu_seqlens) {
                 find_seq(a.cu_seqlens, a.num_seqs, a.total_tokens, t, n, bos, eos);
@@ -199,21 +217,24 @@ __global__ void __launch_bounds__(kWarps * 32) frontend_kernel(FrontendArgs a) {
             }
         }
         const int64_t rk = (t * H + h) * dk + ck, rv = (t * H + h) * dv + cv;
-        float x[CPK], y[CPK], xv[CPV], yv[CPV];
-        load_row<T, CPK>(qr + rk, x);
-        conv_step<CPK, W>(x, hq, wq, y);
+        float y[CPK], yv[CPV], la[CPK];
+        conv_step<CPK, W>(cq, hq, wq, y);
         l2_normalize<CPK>(y, a.eps);
         store_row<T, CPK>(qo + rk, y);
-        load_row<T, CPK>(kr + rk, x);
-        conv_step<CPK, W>(x, hk, wk, y);
+        conv_step<CPK, W>(ckk, hk, wk, y);
         l2_normalize<CPK>(y, a.eps);
         store_row<T, CPK>(ko + rk, y);
-        load_row<T, CPV>(vr + rv, xv);
-        conv_step<CPV, W>(xv, hv, wv, yv);
+        conv_step<CPV, W>(cvv, hv, wv, yv);
         store_row<T, CPV>(vo + rv, yv);
 #pragma unroll
-        for (int c = 0; c < CPK; ++c) a.log_alpha[rk + c] = logsigmoid(a.a_raw[rk + c]);
-        if (lane == 0) bo[t * H + h] = from_f<T>(sigmoid(to_f(br[t * H + h])));
+        for (int c = 0; c < CPK; ++c) la[c] = logsigmoid(ca[c]);
+        store_row<float, CPK>(a.log_alpha + rk, la);
+        if (lane == 0) bo[t * H + h] = from_f<T>(sigmoid(cb));
+#pragma unroll
+        for (int c = 0; c < CPK; ++c) { cq[c] = nq[c]; ckk[c] = nk[c]; ca[c] = na[c]; }
+#pragma unroll
+        for (int c = 0; c < CPV; ++c) cvv[c] = nv[c];
+        cb = nb;
     }
 }
 

@@ -4,10 +4,12 @@
 // "Scale: Total vs Active Parameters and Serving Economics", Visual 1: the KDA
 // output passes a norm and is multiplied by the sigmoid gate).
 //
-// This row kernel finishes the fp32 recurrent prefill path, whose blocks each
-// own a slice of the value channels; the tensor-core prefill and the decode
-// step apply the same epilogue inside their own output stores.  One warp per
-// (token, head) row, in place on `out`.
+// Prefill applies it with this row kernel, in place on `out`, after the
+// recurrence: one read of o and of the gate and one write, memory-bound.  (The
+// decode step applies it inside its own output store.)  Done inside the
+// tensor-core prefill's output stores instead, the gate loads, the cross-warp
+// sums and their barriers lengthen the output warps' per-chunk loop, which is
+// on that kernel's critical path, and cost more than this pass.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -18,36 +20,85 @@ namespace kda {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kRows = 2;       // rows per warp, loads of both issued first
 
-__device__ __forceinline__ float ld(const float* p) { return *p; }
-__device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-__device__ __forceinline__ void st(float* p, float x) { *p = x; }
-__device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+template <typename T, int CPL> struct Vec;
+template <> struct Vec<__nv_bfloat16, 4> {
+    static __device__ __forceinline__ void ld(const __nv_bfloat16* p, float (&x)[4]) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+        x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, const float (&x)[4]) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]), hi = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo);
+        u.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+};
+template <> struct Vec<__nv_bfloat16, 2> {
+    static __device__ __forceinline__ void ld(const __nv_bfloat16* p, float (&x)[2]) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        x[0] = __uint_as_float(u << 16); x[1] = __uint_as_float(u & 0xffff0000u);
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, const float (&x)[2]) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x[0], x[1]);
+    }
+};
+template <> struct Vec<float, 4> {
+    static __device__ __forceinline__ void ld(const float* p, float (&x)[4]) {
+        const float4 f = *reinterpret_cast<const float4*>(p);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    }
+    static __device__ __forceinline__ void st(float* p, const float (&x)[4]) {
+        *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+};
+template <> struct Vec<float, 2> {
+    static __device__ __forceinline__ void ld(const float* p, float (&x)[2]) {
+        const float2 f = *reinterpret_cast<const float2*>(p);
+        x[0] = f.x; x[1] = f.y;
+    }
+    static __device__ __forceinline__ void st(float* p, const float (&x)[2]) {
+        *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    }
+};
 
+// Lane l owns the CPL consecutive channels [l*CPL, l*CPL + CPL) of each row, so a
+// row is one contiguous 32*CPL-element segment per warp instruction.
 template <typename T, int CPL>
-__global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* out, const T* gate, const float* w,
-                                                                 float eps, int64_t rows) {
-    const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* __restrict__ out, const T* __restrict__ gate,
+                                                                 const float* __restrict__ w, float eps,
+                                                                 int64_t rows) {
     constexpr int DV = 32 * CPL;
-    T* o = out + row * DV;
-    const T* g = gate + row * DV;
-    float x[CPL];
-    float ss = 0.f;
+    const int lane = threadIdx.x & 31;
+    const int64_t row0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows;
+    const int c0 = lane * CPL;
+    float wv[CPL];
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        x[i] = ld(o + lane + 32 * i);
-        ss = fmaf(x[i], x[i], ss);
+    for (int i = 0; i < CPL; ++i) wv[i] = w[c0 + i];
+    float x[kRows][CPL], g[kRows][CPL];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        if (row0 + r < rows) {
+            Vec<T, CPL>::ld(out + (row0 + r) * DV + c0, x[r]);
+            Vec<T, CPL>::ld(gate + (row0 + r) * DV + c0, g[r]);
+        }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
-    const float r = rsqrtf(ss * (1.f / DV) + eps);
+    for (int r = 0; r < kRows; ++r) {
+        if (row0 + r >= rows) break;
+        float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-        const int c = lane + 32 * i;
-        const float gv = ld(g + c);
-        st(o + c, x[i] * r * w[c] / (1.f + __expf(-gv)));
+        for (int i = 0; i < CPL; ++i) ss = fmaf(x[r][i], x[r][i], ss);
+#pragma unroll
+        for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
+        const float rr = rsqrtf(ss * (1.f / DV) + eps);
+        float y[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) y[i] = x[r][i] * rr * wv[i] * __fdividef(1.f, 1.f + __expf(-g[r][i]));
+        Vec<T, CPL>::st(out + (row0 + r) * DV + c0, y);
     }
 }
 
@@ -56,7 +107,7 @@ __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* out, const T
 cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float eps, int64_t rows, int dv,
                               DType dt, cudaStream_t s) {
     if (rows == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
+    const unsigned blocks = (unsigned)((rows + kWarps * kRows - 1) / (kWarps * kRows));
     if (dt == DType::BF16) {
         auto* o = static_cast<__nv_bfloat16*>(out);
         auto* g = static_cast<const __nv_bfloat16*>(gate);
