@@ -4,12 +4,13 @@
 // ("Kimi K3 architecture: KDA, MLA and MoE", section "Scale: Total vs Active
 // Parameters and Serving Economics", Visual 1, the KDA inset).
 //
-// Memory-bound.  One warp walks a run of 32 consecutive tokens of one head;
-// lane l holds channels [l*CPL, l*CPL + CPL) of each row, so every row access is
-// one coalesced 256-byte (bf16, d = 128) segment.  The W-1 previous raw rows of
-// q, k and v stay in registers as the warp advances, so each raw row is read
-// once (plus W-1 halo rows per run), and the convolution restarts from zeros at
-// every sequence start.
+// Memory-bound.  A convolution warp walks a run of 32 consecutive tokens of one
+// head for one of q, k, v; lane l holds channels [l*CPL, l*CPL + CPL) of each row,
+// so every row access is one coalesced 256-byte (bf16, d = 128) segment.  Rows
+// are loaded eight tokens at a time (all in flight together); the W-1 previous
+// raw rows stay in registers as the warp advances, so each raw row is read once
+// (plus W-1 halo rows per run), and the convolution restarts from zeros at every
+// sequence start.  The decay and beta gates are a separate elementwise kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -71,11 +72,11 @@ __device__ __forceinline__ void store_row(T* p, const float (&x)[CPL]) {
     }
 }
 
-__device__ __forceinline__ float silu(float y) { return y / (1.f + __expf(-y)); }
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 __device__ __forceinline__ float logsigmoid(float x) {
     return -(fmaxf(-x, 0.f) + log1pf(__expf(-fabsf(x))));
 }
-__device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 // Sequence containing token t: largest n with cu[n] <= t (offsets clamped into
 // [0, T]); returns its start and end.
@@ -127,144 +128,161 @@ __device__ __forceinline__ void l2_normalize(float (&y)[CPL], float eps) {
     for (int c = 0; c < CPL; ++c) y[c] *= r;
 }
 
-template <typename T, int CPK, int CPV, int W>
-__global__ void __launch_bounds__(kWarps * 32) frontend_kernel(FrontendArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRun;
-    if (t_begin >= a.total_tokens) return;
-    const int64_t t_end = min(t_begin + kRun, a.total_tokens);
-    const int H = a.H, dk = a.dk, dv = a.dv;
-    const int ck = lane * CPK, cv = lane * CPV;
-
-    // taps of this lane's channels
-    float wq[W][CPK], wk[W][CPK], wv[W][CPV];
-#pragma unroll
-    for (int c = 0; c < CPK; ++c)
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-            wq[i][c] = a.conv_q[((int64_t)h * dk + ck + c) * W + i];
-            wk[i][c] = a.conv_k[((int64_t)h * dk + ck + c) * W + i];
-        }
-#pragma unroll
-    for (int c = 0; c < CPV; ++c)
-#pragma unroll
-        for (int i = 0; i < W; ++i) wv[i][c] = a.conv_v[((int64_t)h * dv + cv + c) * W + i];
-
-    const T* __restrict__ qr = static_cast<const T*>(a.q_raw);
-    const T* __restrict__ kr = static_cast<const T*>(a.k_raw);
-    const T* __restrict__ vr = static_cast<const T*>(a.v_raw);
-    const T* __restrict__ br = static_cast<const T*>(a.b_raw);
-    T* __restrict__ qo = static_cast<T*>(a.q);
-    T* __restrict__ ko = static_cast<T*>(a.k);
-    T* __restrict__ vo = static_cast<T*>(a.v);
-    T* __restrict__ bo = static_cast<T*>(a.beta);
-
-    int n = 0;
-    int64_t bos = 0, eos = a.total_tokens;
+// Sequence bounds of token t (clamped offsets, or the equal split).
+__device__ __forceinline__ void seq_of(const FrontendArgs& a, int64_t t, int64_t& bos, int64_t& eos) {
     if (a.cu_seqlens) {
-        find_seq(a.cu_seqlens, a.num_seqs, a.total_tokens, t_begin, n, bos, eos);
+        int n;
+        find_seq(a.cu_seqlens, a.num_seqs, a.total_tokens, t, n, bos, eos);
     } else {
         const int64_t len = a.total_tokens / a.num_seqs;
-        bos = (t_begin / len) * len;
+        bos = (t / len) * len;
         eos = bos + len;
-    }
-
-    constexpr int WH = W > 1 ? W - 1 : 1;
-    float hq[WH][CPK], hk[WH][CPK], hv[WH][CPV];
-#pragma unroll
-    for (int i = 0; i < WH; ++i) {                       // raw rows t_begin-(W-1) .. t_begin-1
-        const int64_t src = t_begin - (W - 1) + i;
-        const bool in = W > 1 && src >= bos;
-#pragma unroll
-        for (int c = 0; c < CPK; ++c) hq[i][c] = hk[i][c] = 0.f;
-#pragma unroll
-        for (int c = 0; c < CPV; ++c) hv[i][c] = 0.f;
-        if (in) {
-            load_row<T, CPK>(qr + (src * H + h) * dk + ck, hq[i]);
-            load_row<T, CPK>(kr + (src * H + h) * dk + ck, hk[i]);
-            load_row<T, CPV>(vr + (src * H + h) * dv + cv, hv[i]);
-        }
-    }
-
-    // software pipeline: the raw rows of token t+1 are in flight while token t is computed
-    float cq[CPK], ckk[CPK], cvv[CPV], ca[CPK], cb = 0.f;
-    auto fetch = [&](int64_t t, float (&xq)[CPK], float (&xk)[CPK], float (&xv)[CPV], float (&xa)[CPK], float& xb) {
-        const int64_t rk = (t * H + h) * dk + ck, rv = (t * H + h) * dv + cv;
-        load_row<T, CPK>(qr + rk, xq);
-        load_row<T, CPK>(kr + rk, xk);
-        load_row<T, CPV>(vr + rv, xv);
-        load_row<float, CPK>(a.a_raw + rk, xa);
-        xb = lane == 0 ? to_f(br[t * H + h]) : 0.f;
-    };
-    fetch(t_begin, cq, ckk, cvv, ca, cb);
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        float nq[CPK], nk[CPK], nv[CPV], na[CPK], nb = 0.f;
-        if (t + 1 < t_end) fetch(t + 1, nq, nk, nv, na, nb);
-        if (t >= eos) {                                  // a new sequence starts here
-            if (a.cu_seqlens) {
-                find_seq(a.cu_seqlens, a.num_seqs, a.total_tokens, t, n, bos, eos);
-            } else {
-                bos = eos;
-                eos = bos + a.total_tokens / a.num_seqs;
-            }
-#pragma unroll
-            for (int i = 0; i < WH; ++i) {
-#pragma unroll
-                for (int c = 0; c < CPK; ++c) hq[i][c] = hk[i][c] = 0.f;
-#pragma unroll
-                for (int c = 0; c < CPV; ++c) hv[i][c] = 0.f;
-            }
-        }
-        const int64_t rk = (t * H + h) * dk + ck, rv = (t * H + h) * dv + cv;
-        float y[CPK], yv[CPV], la[CPK];
-        conv_step<CPK, W>(cq, hq, wq, y);
-        l2_normalize<CPK>(y, a.eps);
-        store_row<T, CPK>(qo + rk, y);
-        conv_step<CPK, W>(ckk, hk, wk, y);
-        l2_normalize<CPK>(y, a.eps);
-        store_row<T, CPK>(ko + rk, y);
-        conv_step<CPV, W>(cvv, hv, wv, yv);
-        store_row<T, CPV>(vo + rv, yv);
-#pragma unroll
-        for (int c = 0; c < CPK; ++c) la[c] = logsigmoid(ca[c]);
-        store_row<float, CPK>(a.log_alpha + rk, la);
-        if (lane == 0) bo[t * H + h] = from_f<T>(sigmoid(cb));
-#pragma unroll
-        for (int c = 0; c < CPK; ++c) { cq[c] = nq[c]; ckk[c] = nk[c]; ca[c] = na[c]; }
-#pragma unroll
-        for (int c = 0; c < CPV; ++c) cvv[c] = nv[c];
-        cb = nb;
     }
 }
 
-template <typename T, int CPK, int CPV>
-cudaError_t launch_w(const FrontendArgs& a, dim3 grid, cudaStream_t s) {
+// Asynchronous global -> shared copy of one lane's row segment (bytes = 4, 8 or 16).
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* dst_smem, const void* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem));
+    if constexpr (BYTES == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(src), "n"(BYTES) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// One of q (tensor z0 + blockIdx.z = 0), k (1) or v (2) for a run of kRun tokens of
+// one head.  The run's raw rows are copied into shared memory kStage at a time
+// (every lane its own channels, all copies in flight together, no registers held),
+// then convolved with the history kept in registers, passed through SiLU and (q,
+// k) normalised.
+template <typename T, int CPL, int W>
+__global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z0) {
+    constexpr int kSeg = CPL * (int)sizeof(T);                    // bytes per lane and row
+    constexpr int kStage = kSeg * 32 * kRun <= 8192 ? kRun : 8192 / (kSeg * 32);
+    __shared__ __align__(16) uint8_t stage[kWarps][kStage][32 * kSeg];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int h = blockIdx.y, which = z0 + (int)blockIdx.z;
+    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
+    if (t_begin >= a.total_tokens) return;
+    const int64_t t_end = min(t_begin + kRun, a.total_tokens);
+    const int H = a.H, d = which == 2 ? a.dv : a.dk;
+    const int c0 = lane * CPL;
+    const T* __restrict__ src = static_cast<const T*>(which == 0 ? a.q_raw : which == 1 ? a.k_raw : a.v_raw);
+    T* __restrict__ dst = static_cast<T*>(which == 0 ? a.q : which == 1 ? a.k : a.v);
+    const float* __restrict__ conv = which == 0 ? a.conv_q : which == 1 ? a.conv_k : a.conv_v;
+    const bool norm = which != 2;
+
+    float wt[W][CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c)
+#pragma unroll
+        for (int i = 0; i < W; ++i) wt[i][c] = conv[((int64_t)h * d + c0 + c) * W + i];
+
+    int64_t bos, eos;
+    seq_of(a, t_begin, bos, eos);
+    constexpr int WH = W > 1 ? W - 1 : 1;
+    float hist[WH][CPL];
+#pragma unroll
+    for (int i = 0; i < WH; ++i) {                       // raw rows t_begin-(W-1) .. t_begin-1
+        const int64_t sr = t_begin - (W - 1) + i;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
+        if (W > 1 && sr >= bos) load_row<T, CPL>(src + (sr * H + h) * d + c0, hist[i]);
+    }
+    uint8_t* mine = &stage[warp][0][lane * kSeg];
+    const int64_t rstride = (int64_t)H * d;              // elements from one token's row to the next
+    const T* sp = src + (t_begin * H + h) * d + c0;
+    T* dp = dst + (t_begin * H + h) * d + c0;
+    for (int64_t ts = t_begin; ts < t_end; ts += kStage) {
+        const int n = (int)min((int64_t)kStage, t_end - ts);
+        for (int j = 0; j < n; ++j, sp += rstride) cp_async<kSeg>(mine + j * 32 * kSeg, sp);
+        cp_async_wait_all();                             // this lane's own copies
+#pragma unroll 4
+        for (int j = 0; j < n; ++j, dp += rstride) {
+            const int64_t t = ts + j;
+            if (t >= eos) {                              // a new sequence starts here
+                seq_of(a, t, bos, eos);
+#pragma unroll
+                for (int i = 0; i < WH; ++i)
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
+            }
+            float xr[CPL], y[CPL];
+            load_row<T, CPL>(reinterpret_cast<const T*>(mine + j * 32 * kSeg), xr);
+            conv_step<CPL, W>(xr, hist, wt, y);
+            if (norm) l2_normalize<CPL>(y, a.eps);
+            store_row<T, CPL>(dp, y);
+        }
+    }
+}
+
+// log_alpha = logsigmoid(a_raw) and beta = sigmoid(b_raw): elementwise over rows
+// of dk channels (one warp per row, CPL channels per lane) and the beta column.
+template <typename T, int CPL>
+__global__ void __launch_bounds__(kWarps * 32) gate_kernel(FrontendArgs a) {
+    constexpr int kRowsPerWarp = 8;
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = a.total_tokens * a.H;
+    const int64_t r0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+    const int c0 = lane * CPL;
+    float x[kRowsPerWarp][CPL];
+#pragma unroll
+    for (int j = 0; j < kRowsPerWarp; ++j)
+        if (r0 + j < rows) load_row<float, CPL>(a.a_raw + (r0 + j) * a.dk + c0, x[j]);
+#pragma unroll
+    for (int j = 0; j < kRowsPerWarp; ++j) {
+        if (r0 + j >= rows) break;
+        float y[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) y[c] = logsigmoid(x[j][c]);
+        store_row<float, CPL>(a.log_alpha + (r0 + j) * a.dk + c0, y);
+    }
+    if (lane < kRowsPerWarp && r0 + lane < rows) {
+        const T* br = static_cast<const T*>(a.b_raw);
+        static_cast<T*>(a.beta)[r0 + lane] = from_f<T>(sigmoid(to_f(br[r0 + lane])));
+    }
+}
+
+template <typename T, int CPL>
+cudaError_t launch_conv(const FrontendArgs& a, dim3 grid, int z0, cudaStream_t s) {
     switch (a.conv_width) {
-        case 1: frontend_kernel<T, CPK, CPV, 1><<<grid, kWarps * 32, 0, s>>>(a); break;
-        case 2: frontend_kernel<T, CPK, CPV, 2><<<grid, kWarps * 32, 0, s>>>(a); break;
-        case 3: frontend_kernel<T, CPK, CPV, 3><<<grid, kWarps * 32, 0, s>>>(a); break;
-        case 4: frontend_kernel<T, CPK, CPV, 4><<<grid, kWarps * 32, 0, s>>>(a); break;
+        case 1: conv_kernel<T, CPL, 1><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 2: conv_kernel<T, CPL, 2><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 3: conv_kernel<T, CPL, 3><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 4: conv_kernel<T, CPL, 4><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_t(const FrontendArgs& a, dim3 grid, cudaStream_t s) {
-    if (a.dk == 128 && a.dv == 128) return launch_w<T, 4, 4>(a, grid, s);
-    if (a.dk == 128 && a.dv == 64) return launch_w<T, 4, 2>(a, grid, s);
-    if (a.dk == 64 && a.dv == 128) return launch_w<T, 2, 4>(a, grid, s);
-    return launch_w<T, 2, 2>(a, grid, s);
+cudaError_t launch_t(const FrontendArgs& a, cudaStream_t s) {
+    const int64_t runs = (a.total_tokens + kRun - 1) / kRun;
+    const unsigned bx = (unsigned)((runs + kWarps - 1) / kWarps);
+    cudaError_t e;
+    if (a.dk == a.dv) {                                  // q, k, v: grid.z = 0, 1, 2
+        e = a.dk == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 3), 0, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 3), 0, s);
+    } else {                                             // q and k, then v with its own width
+        e = a.dk == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 2), 0, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 2), 0, s);
+        if (e == cudaSuccess)
+            e = a.dv == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 1), 2, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 1), 2, s);
+    }
+    if (e != cudaSuccess) return e;
+    const int64_t rows = a.total_tokens * a.H;
+    const unsigned gb = (unsigned)((rows + kWarps * 8 - 1) / (kWarps * 8));
+    if (a.dk == 128) gate_kernel<T, 4><<<gb, kWarps * 32, 0, s>>>(a);
+    else gate_kernel<T, 2><<<gb, kWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_frontend(const FrontendArgs& a, cudaStream_t s) {
     if (a.total_tokens == 0) return cudaSuccess;
-    const int64_t runs = (a.total_tokens + kRun - 1) / kRun;
-    const dim3 grid((unsigned)((runs + kWarps - 1) / kWarps), (unsigned)a.H);
-    return a.dtype == DType::BF16 ? launch_t<__nv_bfloat16>(a, grid, s) : launch_t<float>(a, grid, s);
+    return a.dtype == DType::BF16 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
 }
 
 }  // namespace kda
