@@ -211,13 +211,16 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
 
 // ============================ group A: chunk-local stage =========================
 
-// Pass 1 (thread = key channel c): suffix sums of log_alpha over the chunk,
-// e[r][c] = sum_{r<t<L} a[t][c]; returns false (leaving log_alpha untouched) when a
-// channel's chunk total leaves +-kMaxExponent, else writes e back in place and
-// gam[c] = e^{G_c}.  Pass 2 (thread = 16-byte chunk of 8 channels of one row):
+// Operand build, team P (128 threads).
+// Pass 1 (build_suffix, thread = key channel c): suffix sums of log_alpha over the
+// chunk, e[r][c] = sum_{r<t<L} a[t][c]; returns false (leaving log_alpha untouched)
+// when a channel's chunk total leaves +-kMaxExponent, else writes e back in place and
+// returns g = e^{G_c}.  It touches only the log_alpha slot, so it runs before the
+// chunk's other slots are free; the caller publishes g once they are.
+// Pass 2 (build_tiles, thread = 16-byte chunk of 8 channels of one row):
 // Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector
-// accesses.  Team P (128 threads).
-__device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float* gam) {
+// accesses.
+__device__ bool build_suffix(float* A, int L, float& g) {
     const int c = lt();
     float e[C];
 #pragma unroll
@@ -230,10 +233,15 @@ __device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float*
         run += ar;
     }
     if (group_or(kBarP, !(fabsf(run) <= kMaxExponent))) return false;
-    gam[c] = __expf(run);
+    g = __expf(run);
 #pragma unroll
     for (int r = 0; r < C; ++r) A[r * D + c] = e[r];
     group_sync(kBarP);
+    return true;
+}
+
+__device__ void build_tiles(uint8_t* qk, uint8_t* kb, const float* A, int L) {
+    const int c = lt();
     // pass 2: 64 rows x 16 chunks = 1024 units, 8 per thread
 #pragma unroll 2
     for (int m = 0; m < 8; ++m) {
@@ -266,7 +274,6 @@ __device__ bool build_operands(uint8_t* qk, uint8_t* kb, float* A, int L, float*
         *reinterpret_cast<uint4*>(qk + qo) = qh;
         *reinterpret_cast<uint4*>(kb + bo) = kbv;
     }
-    return true;
 }
 
 
@@ -809,15 +816,20 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         KDA_TRACE(n, 3);
         KDA_PHASE(0);
         if (t == 0) ++sw.consumed[kLdA][s];
+        float gval = 0.f;
+        const bool fast = build_suffix(reinterpret_cast<float*>(aslot), L, gval);
+        KDA_PHASE(4);
+        // Kb / P / beta / gamma and the q/k tiles of this slot are chunk n-2's until its state product
         if (n >= 2 && !(ok = group_wait(kBarP, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
         KDA_TRACE(n, 4);
         KDA_PHASE(2);
         if (t < C) sw.beta[s][t] = __float2bfloat16_rn((t < L) ? braw : 0.f);
+        if (fast) sw.gam[s][t] = gval;
         if (!(ok = group_wait(kBarP, &sw.qk_full[s], ph))) break;
         KDA_TRACE(n, 5);
         KDA_PHASE(3);
         if (t == 0) ++sw.consumed[kLdQK][s];
-        const bool fast = build_operands(qk, kb, reinterpret_cast<float*>(aslot), L, sw.gam[s]);
+        if (fast) build_tiles(qk, kb, reinterpret_cast<const float*>(aslot), L);
         if (!fast) {                                     // token-by-token chunk: no Gram product
             if (t == 0) {
                 sw.mode[s] = 1;
@@ -826,7 +838,7 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
             continue;
         }
         group_publish(kBarP);
-        KDA_PHASE(4);
+        KDA_PHASE(5);
         if (t == 0) {
             sw.mode[s] = 0;
             mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
