@@ -134,6 +134,7 @@ struct Small {
 };
 static_assert(sizeof(Small) <= 2048, "small area");
 static_assert(offsetof(Small, gam) % 16 == 0, "gamma rows are read as float4");
+static_assert(offsetof(Small, beta) % 16 == 0, "beta is read eight at a time");
 
 __device__ __forceinline__ uint32_t qk_off(bool is_q, uint32_t r, uint32_t c) {
     return (c >> 6) * 16384u + (is_q ? 8192u : 0u) + sw128_offset(r, (c & 63u) * 2u);
@@ -381,7 +382,10 @@ __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP],
 // X_10 = -D_1 N_10 D_0, X_32 = -D_3 N_32 D_2; then the lower-left 32x32 quarter
 // -C^{-1} (B A^{-1}) with A^{-1}, C^{-1} the inverted halves and B = N[32:64, 0:32], using TF32
 // tensor-core block products with fp32 accumulation.  Team S (4 warps), 4 team barriers.
-__device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
+__device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) {
+#ifdef KDA_PHASE_TIMING
+    long long sp_ = clock64();
+#endif
     float* Nb = reinterpret_cast<float*>(aslot + kSolveN);
     float* Xb = reinterpret_cast<float*>(aslot + kSolveX);
     float* Yb = reinterpret_cast<float*>(aslot + kSolveY);   // 4 blocks
@@ -391,17 +395,20 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
         const float* Nii = blk(Nb, i, i);
         float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = (r == jl) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) {               // four partial sums: a short dependence chain
+            float p[4] = {(r == jl) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < r; ++q) acc = fmaf(-Nii[blk_at(r, q)], x[q], acc);
-            x[r] = acc;
+            for (int q = 0; q < r; ++q) p[q & 3] = fmaf(-Nii[blk_at(r, q)], x[q], p[q & 3]);
+            x[r] = (p[0] + p[1]) + (p[2] + p[3]);
         }
         float* Xii = blk(Xb, i, i);
 #pragma unroll
         for (int r = 0; r < 16; ++r) Xii[blk_at(r, jl)] = x[r];
     }
     group_sync(kBarS);
+#ifdef KDA_PHASE_TIMING
+    if (t == 0) { const long long c_ = clock64(); x_sw->phase[26 + 1] += (unsigned long long)(c_ - sp_); sp_ = c_; }
+#endif
     // halves: warps 0-1 -> X_10 (n-tile w), warps 2-3 -> X_32 (n-tile w-2); Y via the block's own
     // Y slot, the chain stays inside the warp
     if (w < 4) {
@@ -422,6 +429,9 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
         }
     }
     group_sync(kBarS);
+#ifdef KDA_PHASE_TIMING
+    if (t == 0) { const long long c_ = clock64(); x_sw->phase[26 + 2] += (unsigned long long)(c_ - sp_); sp_ = c_; }
+#endif
     // Y = B A^{-1}: Y_20 = N_20 D_0 + N_21 X_10, Y_21 = N_21 D_1, Y_30 = N_30 D_0 + N_31 X_10, Y_31 = N_31 D_1
 #pragma unroll 1
     for (int it = 0; it < 2; ++it) {
@@ -439,6 +449,9 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
         }
     }
     group_sync(kBarS);
+#ifdef KDA_PHASE_TIMING
+    if (t == 0) { const long long c_ = clock64(); x_sw->phase[26 + 3] += (unsigned long long)(c_ - sp_); sp_ = c_; }
+#endif
     // X_lower = -C^{-1} Y: X_20 = -D_2 Y_20, X_21 = -D_2 Y_21, X_30 = -(X_32 Y_20 + D_3 Y_30), X_31 = -(X_32 Y_21 + D_3 Y_31)
 #pragma unroll 1
     for (int it = 0; it < 2; ++it) {
@@ -455,7 +468,10 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
         }
     }
     group_sync(kBarS);
-#pragma unroll 1
+#ifdef KDA_PHASE_TIMING
+    if (t == 0) { const long long c_ = clock64(); x_sw->phase[26 + 4] += (unsigned long long)(c_ - sp_); sp_ = c_; }
+#endif
+#pragma unroll
     for (int it = 0; it < 2; ++it) {                 // T[r][s] = X[r][s] beta_s (bf16)
         const int tt = t + kTeam * it, r = tt >> 2, q = tt & 3, bi = r >> 4, rr = r & 15;
 #pragma unroll
@@ -467,9 +483,12 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta) {
                 const float4 lo = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k));
                 const float4 hi = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k + 4));
                 const float xr[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                const uint4 bw = *reinterpret_cast<const uint4*>(beta + s0);   // beta_{s0 .. s0+7}
+                const uint32_t bv[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    wv[u] = pack_bf16x2(xr[2 * u] * bf2f(beta[s0 + 2 * u]), xr[2 * u + 1] * bf2f(beta[s0 + 2 * u + 1]));
+                    wv[u] = pack_bf16x2(xr[2 * u] * __uint_as_float(bv[u] << 16),
+                                        xr[2 * u + 1] * __uint_as_float(bv[u] & 0xffff0000u));
             } else {
                 wv[0] = wv[1] = wv[2] = wv[3] = 0u;
             }
@@ -890,7 +909,7 @@ __device__ __noinline__ bool run_team_s(const Ctx& x_in) {
         tc_fence_before();
         group_sync(kBarS);
         KDA_PHASE(6);
-        solve_T(aslot, sw.beta[s]);
+        solve_T(aslot, sw.beta[s], x.sw);
         KDA_PHASE(15);
         KDA_TRACE(n, 7);
         if (!(ok = group_wait(kBarS, &sw.v_full[s], ph))) break;
