@@ -416,16 +416,16 @@ def run_ours(args):
             "frontend": {"workload": f"kda_frontend_bf16_B{B}_H{H}_T{T}_d{D}_W4",
                          "us_per_step": layer["t_fe"] * 1e6, "achieved_gbs": fbytes / layer["t_fe"] / 1e9,
                          "peak_gbs": hbm, "frac": fbytes / layer["t_fe"] / 1e9 / hbm,
-                         "algorithmic_bytes_per_launch": fbytes, "kernel": "frontend_kernel"},
+                         "algorithmic_bytes_per_launch": fbytes, "kernels": ["conv_kernel", "gate_kernel"]},
             "prefill_gated": {"workload": WORKLOAD + "_gated", "ms_per_step": layer["t_pg"] * 1e3,
                               "value": world * B * T / layer["t_pg"], "unit": UNIT,
                               "achieved_gbs": gbytes / layer["t_pg"] / 1e9,
                               "frac": gbytes / layer["t_pg"] / 1e9 / hbm,
-                              "algorithmic_bytes_per_launch": gbytes, "kernel": "chunk_tc_kernel<gated>"},
+                              "algorithmic_bytes_per_launch": gbytes, "kernels": ["chunk_tc_kernel", "gated_norm_kernel"]},
             "decode_gated": {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}_gated",
                              "us_per_step": layer["t_dg"] * 1e6, "achieved_gbs": dgbytes / layer["t_dg"] / 1e9,
                              "frac": dgbytes / layer["t_dg"] / 1e9 / hbm,
-                             "algorithmic_bytes_per_launch": dgbytes, "kernel": "decode_kernel<gated>"},
+                             "algorithmic_bytes_per_launch": dgbytes, "kernels": ["decode_kernel (gate and norm in its store)"]},
         }
     if world == 1 and not args.no_cpu_baseline:
         run, nseq, cores, used = oracle_sample(args.cpu_budget)

@@ -35,14 +35,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile (if stale) and return the path of libkda.so."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, tag=None) -> str:
+    """Compile (if stale) and return the path of libkda.so.
+
+    With ``tag`` the objects and the library go to ``_build/<tag>/`` instead (a
+    separately configured copy, e.g. a diagnostic build with extra ``-D`` flags);
+    the package's own ``libkda.so`` is left alone."""
+    obj_dir = os.path.join(BUILD, tag) if tag else BUILD
+    lib = os.path.join(obj_dir, "libkda.so") if tag else LIB
+    os.makedirs(obj_dir, exist_ok=True)
     deps_common = HEADERS + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
     flags = CFLAGS + list(extra_flags or [])
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + deps_common):
             cmd = [NVCC] + ARCH + flags + ["-c", src, "-o", obj]
@@ -58,10 +64,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
             print(out.decode(errors="replace"), file=sys.stderr)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"{s}\n{o}" for s, o in failed))
-    if force or _stale(LIB, objs):
-        cmd = [NVCC] + ARCH + ["-shared", "-o", LIB] + objs
+    if force or _stale(lib, objs):
+        cmd = [NVCC] + ARCH + ["-shared", "-o", lib] + objs
         subprocess.run(cmd, check=True)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -74,9 +74,18 @@ constexpr int D = 128;         // dk = dv
 // group A: two teams of 128 threads (P: operands and Gram, S: UT solve and W'/U), group B:
 // 128 threads, then two single-thread warps: the TMA producer and the issuer of the
 // state/output products
-constexpr int kThreads = 448;
+#ifdef KDA_TRACE_EVENTS
+#define KDA_DIAG_TRACE 1
+#endif
 constexpr int kTeam = 128, kGroupA = 2 * kTeam, kGroupB = 128, kProducer = kGroupA + kGroupB,
               kIssuerOut = kProducer + 32;
+#ifdef KDA_DIAG_TRACE
+constexpr int kObserver = kIssuerOut + 32;   // diagnostic build: a warp that watches the products
+constexpr int kThreads = kObserver + 32;
+constexpr int kTraceFirst = 48, kTraceChunks = 12, kTraceEvents = 8;   // traced chunks of block 0
+#else
+constexpr int kThreads = 448;
+#endif
 constexpr float kMaxExponent = 60.f;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s per bounded wait
 constexpr int kBarP = 1, kBarB = 2, kBarS = 3;      // named barriers of the 128-thread groups
@@ -130,6 +139,10 @@ struct Small {
     float gam[2][D];
 #ifdef KDA_PHASE_TIMING
     unsigned long long phase[32];                // diagnostic build only
+#endif
+#ifdef KDA_DIAG_TRACE
+    int cmd_n;                                   // chunk index of cmd_b (diagnostic build)
+    uint32_t trace[kTraceChunks][kTraceEvents];  // block 0's product events (diagnostic build)
 #endif
 };
 static_assert(sizeof(Small) <= 2048, "small area");
@@ -711,16 +724,25 @@ __device__ unsigned long long g_phase_cycles[32];
         }                                                                             \
     } while (0)
 #define KDA_PHASE_INIT long long phase_t_ = clock64()
-// Event trace of block 0: the clock at named points of chunk n.
-__device__ long long g_trace[128][16];
+#else
+#define KDA_PHASE(i) do {} while (0)
+#define KDA_PHASE_INIT do {} while (0)
+#endif
+#ifdef KDA_DIAG_TRACE
+// Event trace of block 0 (diagnostic build): the low 32 bits of the SM clock at
+// the issue (events 0, 2, 4, 6) and completion (1, 3, 5, 7) of the four product
+// groups of chunks kTraceFirst .. kTraceFirst + kTraceChunks - 1.  Kept in shared
+// memory during the run and copied out when the block ends: stamping straight to
+// global memory slowed the traced block, and so the launch, by a quarter.
+__device__ uint32_t g_trace[kTraceChunks][kTraceEvents];
+__device__ __forceinline__ bool trace_chunk(int n) { return (unsigned)(n - kTraceFirst) < (unsigned)kTraceChunks; }
 #define KDA_TRACE(n, ev)                                                              \
     do {                                                                              \
-        if (blockIdx.x == 0 && lt() == 0 && (n) < 128) g_trace[(n)][(ev)] = clock64(); \
+        if (blockIdx.x == 0 && lt() == 0 && trace_chunk(n))                           \
+            x.sw->trace[(n) - kTraceFirst][(ev)] = (uint32_t)clock64();               \
     } while (0)
 #else
 #define KDA_TRACE(n, ev) do {} while (0)
-#define KDA_PHASE(i) do {} while (0)
-#define KDA_PHASE_INIT do {} while (0)
 #endif
 
 // ============================ TMA ring refills ===================================
@@ -830,9 +852,7 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* kb = x.sm + kKB0 + s * 16384;
 
-        KDA_TRACE(n, 2);
         if (!(ok = group_wait(kBarP, &sw.a_full[s], ph))) break;
-        KDA_TRACE(n, 3);
         KDA_PHASE(0);
         if (t == 0) ++sw.consumed[kLdA][s];
         float gval = 0.f;
@@ -840,12 +860,10 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         KDA_PHASE(4);
         // Kb / P / beta / gamma and the q/k tiles of this slot are chunk n-2's until its state product
         if (n >= 2 && !(ok = group_wait(kBarP, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
-        KDA_TRACE(n, 4);
         KDA_PHASE(2);
         if (t < C) sw.beta[s][t] = __float2bfloat16_rn((t < L) ? braw : 0.f);
         if (fast) sw.gam[s][t] = gval;
         if (!(ok = group_wait(kBarP, &sw.qk_full[s], ph))) break;
-        KDA_TRACE(n, 5);
         KDA_PHASE(3);
         if (t == 0) ++sw.consumed[kLdQK][s];
         if (fast) build_tiles(qk, kb, reinterpret_cast<const float*>(aslot), L);
@@ -860,11 +878,11 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         KDA_PHASE(5);
         if (t == 0) {
             sw.mode[s] = 0;
+            KDA_TRACE(n, 0);
             mma_gram(x.tb, tm_apw(s), smem_u32(qk), smem_u32(kb));
             mma_commit(&sw.gram_done[s]);
             issued = true;
         }
-        KDA_TRACE(n, 6);
         KDA_PHASE(25);
     }
     if (t == 0 && issued) {   // let this thread's products land before TMEM is freed (bounded)
@@ -911,16 +929,15 @@ __device__ __noinline__ bool run_team_s(const Ctx& x_in) {
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s], x.sw);
         KDA_PHASE(15);
-        KDA_TRACE(n, 7);
         if (!(ok = group_wait(kBarS, &sw.v_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdV][s];
         // the U slot still holds chunk n-2's output until group B has read it (every chunk,
         // tensor-core or token-by-token, completes one phase of its slot's u_free)
         if (n >= 2 && !(ok = group_wait(kBarS, &sw.u_free[s], ((n - 2) >> 1) & 1))) break;
-        KDA_TRACE(n, 8);
         group_publish(kBarS);
         KDA_PHASE(7);
         if (t == 0) {                                    // W'^T and U^T; their commit is the 2nd arrival
+            KDA_TRACE(n, 2);
             mbar_arrive(&sw.ready[s]);
             mma_wu(x.tb, tm_apw(s), tm_u(s), smem_u32(qk), smem_u32(x.sm + kV0 + s * kVBytes),
                    smem_u32(aslot + kTT));
@@ -928,7 +945,6 @@ __device__ __noinline__ bool run_team_s(const Ctx& x_in) {
             mma_commit(&sw.av_free[s]);
             issued = true;
         }
-        KDA_TRACE(n, 9);
         KDA_PHASE(1);
     }
     if (t == 0 && issued) {
@@ -954,6 +970,9 @@ __device__ __noinline__ bool run_out_issuer(const Ctx& x_in) {
         const int s = sw.cmd_b;
         if (s < 0) break;
         tc_fence_after();
+#ifdef KDA_DIAG_TRACE
+        KDA_TRACE(sw.cmd_n, 6);
+#endif
         mma_state_out(x.tb, tm_u(s), smem_u32(x.sm + kKB0 + s * 16384), smem_u32(x.sm + kQK0 + s * kQKBytes),
                       smem_u32(x.sm + kPP0 + s * 8192));
         mma_commit(&sw.mma2_done);
@@ -1048,12 +1067,10 @@ __device__ __noinline__ void run_producer(const Ctx& x_in, const Maps& maps) {
         if (!mbar_wait_parked(&sw.av_free[s], ph, kWaitLimitNs)) return;
         KDA_PHASE(18);
         refill(x, maps, n, s, true, true, false);
-        KDA_TRACE(n, 0);
         KDA_PHASE(19);
         if (!mbar_wait_parked(&sw.qk_free[s], ph, kWaitLimitNs)) return;
         KDA_PHASE(20);
         refill(x, maps, n, s, false, false, true);
-        KDA_TRACE(n, 1);
         prefetch_chunk(x, maps, n + 2);
         KDA_PHASE(21);
     }
@@ -1089,7 +1106,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         uint8_t* vs = x.sm + kV0 + s * kVBytes;
 
         if (!(ok = group_wait(kBarB, &sw.ready[s], ph))) break;
-        KDA_TRACE(n, 10);
         KDA_PHASE(8);
         tc_fence_after();
         if (sw.mode[s]) {                                // token-by-token chunk (tiles already landed)
@@ -1116,13 +1132,13 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         group_publish(kBarB);
         KDA_PHASE(10);
         if (leader) {
+            KDA_TRACE(n, 4);
             mma_delta(x.tb, tm_u(s), sWT);
             KDA_PHASE(24);
             mma_commit(&sw.mma1_done);
         }
         mma1_pending = true;
         if (!(ok = group_wait(kBarB, &sw.mma1_done, m1_ph))) break;
-        KDA_TRACE(n, 11);
         m1_ph ^= 1u; mma1_pending = false;
         KDA_PHASE(11);
         tc_fence_after();
@@ -1130,19 +1146,19 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         group_publish(kBarB);
         KDA_PHASE(12);
         if (leader) {                                    // the state/output issuer takes it from here
+#ifdef KDA_DIAG_TRACE
+            sw.cmd_n = n;
+#endif
             sw.cmd_b = s;
             mbar_arrive(&sw.packed);
         }
         KDA_PHASE(22);
-        KDA_TRACE(n, 12);
         if (have_prev) {                                 // previous output, under this chunk's MMAs
             flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
             have_prev = false;
         }
         KDA_PHASE(16);
-        KDA_TRACE(n, 13);
         if (!(ok = group_wait(kBarB, &sw.mma2_done, m2_ph))) break;
-        KDA_TRACE(n, 14);
         m2_ph ^= 1u;
         KDA_PHASE(13);
         tc_fence_after();
@@ -1152,7 +1168,6 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
         group_sync(kBarB);
         tc_fence_after();
         KDA_PHASE(14);
-        KDA_TRACE(n, 15);
     }
     if (ok) {
         if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
@@ -1167,6 +1182,45 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     if ((t & 31) == 0) bulk_wait_all();              // tile stores complete before the block exits
     return ok;
 }
+
+#ifdef KDA_DIAG_TRACE
+// Diagnostic build only: lane 0 of an extra warp of block 0 probes, without
+// blocking, the completion barriers of the four product groups of each chunk
+// (Gram; W' and U; Delta; state and output), following every phase from chunk
+// 0 on, and records the clock at which it first sees each group of a traced
+// chunk complete (events 1, 3, 5, 7; the matching issue events 0, 2, 4, 6 are
+// taken by the issuing threads).  It stops once the traced chunks are done,
+// once group B has ended and a pass finds nothing new, or after kWaitLimitNs.
+__device__ void run_observer(const Ctx& x) {
+    if (blockIdx.x != 0 || (threadIdx.x & 31) != 0) return;
+    Small& sw = *x.sw;
+    const int nch = x.nchunks < kTraceFirst + kTraceChunks ? x.nchunks : kTraceFirst + kTraceChunks;
+    int next[4] = {0, 0, 0, 0};
+    const uint64_t t0 = globaltimer_ns();
+    bool b_done = false;
+    for (;;) {
+        bool pending = false, progress = false;
+        for (int g = 0; g < 4; ++g) {
+            const int n = next[g];
+            if (n >= nch) continue;
+            pending = true;
+            uint64_t* bar = g == 0 ? &sw.gram_done[n & 1]
+                          : g == 1 ? &sw.ready[n & 1]
+                          : g == 2 ? &sw.mma1_done : &sw.mma2_done;
+            const uint32_t par = g < 2 ? (uint32_t)((n >> 1) & 1) : (uint32_t)(n & 1);
+            if (mbar_test(bar, par)) {
+                if (trace_chunk(n)) sw.trace[n - kTraceFirst][2 * g + 1] = (uint32_t)clock64();
+                ++next[g];
+                progress = true;
+            }
+        }
+        if (!pending || (b_done && !progress)) break;
+        if (*reinterpret_cast<volatile int*>(&sw.cmd_b) == -1) b_done = true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        __nanosleep(32);             // leave the block's issue slots and shared-memory pipe alone
+    }
+}
+#endif
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
@@ -1220,6 +1274,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         tma_prefetch_desc(&maps.o);
         for (int k = 0; k < 3; ++k)
             for (int s = 0; s < 2; ++s) sw->issued[k][s] = sw->consumed[k][s] = 0;
+        sw->cmd_b = 0;
+#ifdef KDA_DIAG_TRACE
+        for (int i = 0; i < kTraceChunks * kTraceEvents; ++i) sw->trace[i / kTraceEvents][i % kTraceEvents] = 0u;
+#endif
 #ifdef KDA_PHASE_TIMING
         for (int i = 0; i < 32; ++i) sw->phase[i] = 0;
 #endif
@@ -1245,6 +1303,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
 
     else if (tid == kIssuerOut)
         ok = run_out_issuer(x);
+#ifdef KDA_DIAG_TRACE
+    else if (tid >= kObserver)
+        run_observer(x);
+#endif
     if (!ok && lt() == 0) atomicOr(status, kStatusTimeout);
 
     tc_fence_before();
@@ -1260,6 +1322,10 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     __syncthreads();
 #ifdef KDA_PHASE_TIMING
     if (tid < 32) atomicAdd(&g_phase_cycles[tid], sw->phase[tid]);
+#endif
+#ifdef KDA_DIAG_TRACE
+    if (blockIdx.x == 0 && tid < kTraceChunks * kTraceEvents)
+        g_trace[tid / kTraceEvents][tid % kTraceEvents] = sw->trace[tid / kTraceEvents][tid % kTraceEvents];
 #endif
     if ((tid >> 5) == 0) tmem_dealloc(x.tb, kTmCols);
 }
@@ -1292,10 +1358,13 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 
 }  // namespace
 
-#ifdef KDA_PHASE_TIMING
-extern "C" int kda_debug_trace(long long* host2048) {
-    return cudaMemcpyFromSymbol(host2048, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+#ifdef KDA_DIAG_TRACE
+// Diagnostic build: copy block 0's event trace (kTraceChunks x kTraceEvents clocks).
+extern "C" int kda_debug_trace(uint32_t* host_trace) {
+    return cudaMemcpyFromSymbol(host_trace, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
 }
+#endif
+#ifdef KDA_PHASE_TIMING
 extern "C" int kda_debug_phase_cycles(unsigned long long* host16, int reset) {
     if (cudaMemcpyFromSymbol(host16, g_phase_cycles, 32 * sizeof(unsigned long long)) != cudaSuccess)
         return -1;

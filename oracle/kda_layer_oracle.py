@@ -13,7 +13,7 @@ the step after it (``gated_rmsnorm``).
 
 Readings where the figure is silent (each also listed in the design notes):
 - the short convolution is depthwise and causal over the tokens of one
-  sequence, width W (the figure gives no width; the library takes W <= 8),
+  sequence, width W (the figure gives no width; the library takes W <= 4),
   with zero history before the sequence start and no bias:
   y[t, c] = sum_{i<W} w[c, i] * x[t - (W-1) + i, c];
 - the L2 norm is over the key dimension of one (token, head):
