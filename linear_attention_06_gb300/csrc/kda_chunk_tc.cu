@@ -54,6 +54,12 @@
 // fp32 S^T (lane = value channel, column = key channel) for the whole
 // sequence, and the bf16 copies of Ss^T and Delta^T are packed into TMEM as the
 // A operands of the products that read them.
+//
+// Diagnostic builds only: -DKDA_PHASE_TIMING adds per-role phase clock counters,
+// -DKDA_TRACE_EVENTS a trace of block 0's product issues and completions, taken
+// with one more warp that watches the completion barriers.  The product build
+// compiles neither.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1332,15 +1338,16 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
 
 // ============================ host side ==========================================
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    // looked up once (a function-local static is initialised once, even under concurrent calls)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1395,14 +1402,15 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
                   CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     // the shared-memory opt-in is a per-device property of the kernel
-    static bool attr_set[64] = {};
+    // (setting it twice from two host threads is harmless; the flags are atomic)
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemDynamic);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const unsigned blocks = (unsigned)((int64_t)a.num_seqs * a.H);
     chunk_tc_kernel<<<blocks, kThreads, kSmemDynamic, s>>>(

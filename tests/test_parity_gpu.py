@@ -54,6 +54,16 @@ def test_small_head_sizes(dk, dv, dtype):
     compare_prefill(w)
 
 
+def test_many_short_sequences_span_many_waves():
+    # 400 sequences x 4 heads = 1600 blocks (about ten waves of one block per SM), every
+    # chunk a ragged last chunk, lengths 0..40 with empty sequences among them
+    rng = np.random.default_rng(400)
+    lens = [int(v) for v in rng.integers(0, 41, size=400)]
+    cu = workloads.cu_from_lengths(lens)
+    w = workloads.make_inputs(cu[-1], 4, 128, 128, seed=400, cu_seqlens=cu, state_std=0.05).to(DEV)
+    compare_prefill(w)
+
+
 def test_dense_batch_without_cu_seqlens():
     w = workloads.make_inputs(4 * 150, 2, 128, 128, seed=5, num_seqs=4).to(DEV)
     out, fin = kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, None, None,
