@@ -88,7 +88,7 @@ constexpr int kTeam = 128, kGroupA = 2 * kTeam, kGroupB = 128, kProducer = kGrou
 #ifdef KDA_DIAG_TRACE
 constexpr int kObserver = kIssuerOut + 32;   // diagnostic build: a warp that watches the products
 constexpr int kThreads = kObserver + 32;
-constexpr int kTraceFirst = 48, kTraceChunks = 12, kTraceEvents = 8;   // traced chunks of block 0
+constexpr int kTraceChunks = 12, kTraceEvents = 8;   // traced chunks of block 0 (from g_trace_first)
 #else
 constexpr int kThreads = 448;
 #endif
@@ -148,6 +148,7 @@ struct Small {
 #endif
 #ifdef KDA_DIAG_TRACE
     int cmd_n;                                   // chunk index of cmd_b (diagnostic build)
+    int trace_first;                             // first traced chunk (diagnostic build)
     uint32_t trace[kTraceChunks][kTraceEvents];  // block 0's product events (diagnostic build)
 #endif
 };
@@ -737,15 +738,19 @@ __device__ unsigned long long g_phase_cycles[32];
 #ifdef KDA_DIAG_TRACE
 // Event trace of block 0 (diagnostic build): the low 32 bits of the SM clock at
 // the issue (events 0, 2, 4, 6) and completion (1, 3, 5, 7) of the four product
-// groups of chunks kTraceFirst .. kTraceFirst + kTraceChunks - 1.  Kept in shared
+// groups of chunks g_trace_first .. g_trace_first + kTraceChunks - 1 (set by
+// kda_debug_set_trace_first, 48 unless changed).  Kept in shared
 // memory during the run and copied out when the block ends: stamping straight to
 // global memory slowed the traced block, and so the launch, by a quarter.
 __device__ uint32_t g_trace[kTraceChunks][kTraceEvents];
-__device__ __forceinline__ bool trace_chunk(int n) { return (unsigned)(n - kTraceFirst) < (unsigned)kTraceChunks; }
+__device__ int g_trace_first = 48;
+__device__ __forceinline__ bool trace_chunk(const Small& sw, int n) {
+    return (unsigned)(n - sw.trace_first) < (unsigned)kTraceChunks;
+}
 #define KDA_TRACE(n, ev)                                                              \
     do {                                                                              \
-        if (blockIdx.x == 0 && lt() == 0 && trace_chunk(n))                           \
-            x.sw->trace[(n) - kTraceFirst][(ev)] = (uint32_t)clock64();               \
+        if (blockIdx.x == 0 && lt() == 0 && trace_chunk(*x.sw, (n)))                  \
+            x.sw->trace[(n) - x.sw->trace_first][(ev)] = (uint32_t)clock64();         \
     } while (0)
 #else
 #define KDA_TRACE(n, ev) do {} while (0)
@@ -1200,7 +1205,8 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
 __device__ void run_observer(const Ctx& x) {
     if (blockIdx.x != 0 || (threadIdx.x & 31) != 0) return;
     Small& sw = *x.sw;
-    const int nch = x.nchunks < kTraceFirst + kTraceChunks ? x.nchunks : kTraceFirst + kTraceChunks;
+    const int last = sw.trace_first + kTraceChunks;
+    const int nch = x.nchunks < last ? x.nchunks : last;
     int next[4] = {0, 0, 0, 0};
     const uint64_t t0 = globaltimer_ns();
     bool b_done = false;
@@ -1215,7 +1221,7 @@ __device__ void run_observer(const Ctx& x) {
                           : g == 2 ? &sw.mma1_done : &sw.mma2_done;
             const uint32_t par = g < 2 ? (uint32_t)((n >> 1) & 1) : (uint32_t)(n & 1);
             if (mbar_test(bar, par)) {
-                if (trace_chunk(n)) sw.trace[n - kTraceFirst][2 * g + 1] = (uint32_t)clock64();
+                if (trace_chunk(sw, n)) sw.trace[n - sw.trace_first][2 * g + 1] = (uint32_t)clock64();
                 ++next[g];
                 progress = true;
             }
@@ -1223,7 +1229,9 @@ __device__ void run_observer(const Ctx& x) {
         if (!pending || (b_done && !progress)) break;
         if (*reinterpret_cast<volatile int*>(&sw.cmd_b) == -1) b_done = true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-        __nanosleep(32);             // leave the block's issue slots and shared-memory pipe alone
+        // sleep between passes so the watched block keeps its issue slots and shared-memory
+        // pipe (a spinning watcher slowed it by 6%); a stamp can then trail its completion
+        __nanosleep(32);
     }
 }
 #endif
@@ -1283,6 +1291,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
         sw->cmd_b = 0;
 #ifdef KDA_DIAG_TRACE
         for (int i = 0; i < kTraceChunks * kTraceEvents; ++i) sw->trace[i / kTraceEvents][i % kTraceEvents] = 0u;
+        sw->trace_first = g_trace_first;
 #endif
 #ifdef KDA_PHASE_TIMING
         for (int i = 0; i < 32; ++i) sw->phase[i] = 0;
@@ -1369,6 +1378,11 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esz,
 // Diagnostic build: copy block 0's event trace (kTraceChunks x kTraceEvents clocks).
 extern "C" int kda_debug_trace(uint32_t* host_trace) {
     return cudaMemcpyFromSymbol(host_trace, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -1;
+}
+// Diagnostic build: the first chunk of the traced window of later launches (>= 0).
+extern "C" int kda_debug_set_trace_first(int first) {
+    if (first < 0) return -1;
+    return cudaMemcpyToSymbol(g_trace_first, &first, sizeof(int)) == cudaSuccess ? 0 : -1;
 }
 #endif
 #ifdef KDA_PHASE_TIMING

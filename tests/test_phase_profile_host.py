@@ -29,9 +29,12 @@ def test_chunk_arithmetic_matches_the_chunkwise_flop_count():
 
 def test_trace_window_matches_the_kernel():
     src = open(SRC).read()
-    m = re.search(r"kTraceFirst = (\d+), kTraceChunks = (\d+), kTraceEvents = (\d+)", src)
+    m = re.search(r"kTraceChunks = (\d+), kTraceEvents = (\d+)", src)
     assert m, "trace window constants not found in the kernel source"
-    assert tuple(int(v) for v in m.groups()) == (pp.TRACE_FIRST, pp.TRACE_CHUNKS, pp.TRACE_EVENTS)
+    assert tuple(int(v) for v in m.groups()) == (pp.TRACE_CHUNKS, pp.TRACE_EVENTS)
+    assert "kda_debug_set_trace_first" in src
+    # every window fits the benchmark's 128 chunks per sequence
+    assert all(0 <= f and f + pp.TRACE_CHUNKS <= 128 for f in pp.TRACE_WINDOWS)
     # every issue event the tool reads is stamped in the kernel
     for _, issue, done, _ in pp.GROUPS:
         assert re.search(rf"KDA_TRACE\([^,]+, {issue}\);", src), issue
