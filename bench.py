@@ -32,6 +32,8 @@ UNIT = "tokens/s"
 WORKLOAD = "kda_prefill_bf16_B4_H32_T8192_d128"
 B, T, H, D = 4, 8192, 32, 128
 DEC_N = 256
+CKPT_EVERY = 1024          # checkpointed prefill: a state every 1024 tokens of each sequence
+DEC_MULTI_T = (4, 16)      # multi-token decode: tokens per sequence per call
 # algorithmic bytes per token-head: q, k, v bf16 (768) + log_alpha fp32 (512) + beta (2) + out (256)
 BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 2 + D * 2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -49,9 +51,32 @@ def frontend_bytes(tokens, heads, d=128, width=4):
     return tokens * heads * per + 3 * heads * d * width * 4
 
 
-def decode_bytes(n, heads):
-    # state read + write (fp32) + q, k, v, out bf16 + log_alpha fp32 + beta bf16
-    return n * heads * (2 * D * D * 4 + 4 * D * 2 + D * 4 + 2)
+# fp32 CUDA-core rate for the decode step's arithmetic: 152 SMs x 128 fp32 lanes x 2 flop (FMA)
+# x 2.07 GHz (the GB300's maximum SM clock)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# decode arithmetic per token-head (dk = dv = D): decay D*D multiplies, r = S^T k, y = S^T q and
+# the rank-1 update D*D fused multiply-adds each (2 flop)
+DECODE_FLOP_PER_TOKEN_HEAD = D * D + 3 * 2 * D * D
+
+
+def decode_bytes(n, heads, tokens=1):
+    # state read + write (fp32) once, + per token q, k, v, out bf16 + log_alpha fp32 + beta bf16
+    return n * heads * (2 * D * D * 4 + tokens * (4 * D * 2 + D * 4 + 2))
+
+
+def _multi_decode_entry(tm, t_m, world, hbm):
+    """One multi-token decode line: HBM and fp32-ALU fractions; the bound is the roof
+    whose ideal time is longer."""
+    nbytes = decode_bytes(DEC_N, H, tm)
+    flops = DEC_N * tm * H * DECODE_FLOP_PER_TOKEN_HEAD
+    t_hbm, t_alu = nbytes / (hbm * 1e9), flops / (FP32_ALU_TFLOPS * 1e12)
+    return {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}_T{tm}", "tokens_per_seq": tm,
+            "us_per_step": t_m * 1e6, "value": world * DEC_N * tm / t_m, "unit": UNIT,
+            "achieved_gbs": nbytes / t_m / 1e9, "frac_hbm": t_hbm / t_m,
+            "achieved_tflops": flops / t_m / 1e12, "frac_alu": t_alu / t_m,
+            "alu_peak_tflops": FP32_ALU_TFLOPS, "bound": "hbm" if t_hbm >= t_alu else "alu",
+            "frac": max(t_hbm, t_alu) / t_m,
+            "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops, "kernels": ["decode_kernel"]}
 
 
 def load_peaks():
@@ -317,6 +342,46 @@ def run_ours(args):
         t_dg = timed(lambda: kda.kda_decode_step_gated(dw.q, dw.k, dw.v, dw.log_alpha, dw.beta, gx.g_raw,
                                                        gx.norm_weight, S, out=dout, stream=stream))
         layer = {"t_fe": t_fe, "t_pg": t_pg, "t_dg": t_dg}
+
+        # NEXT-1: the benchmark prefill also saving every sequence's state each CKPT_EVERY
+        # tokens.  The checkpoint tables go to the device once (the binding would validate
+        # and copy them on every call), and the call goes straight through the C ABI.
+        import ctypes
+
+        from linear_attention_06_gb300 import _lib
+        L = _lib.lib()
+        per_seq = T // CKPT_EVERY
+        ck_cu_h = torch.arange(0, B * per_seq + 1, per_seq, dtype=torch.int32)
+        ck_pos_h = torch.tensor([p for _ in range(B) for p in range(CKPT_EVERY, T + 1, CKPT_EVERY)],
+                                dtype=torch.int32)
+        cu_h = w.cu_seqlens.to(torch.int32).cpu()
+        st = L.kda_check_checkpoints(ctypes.c_void_p(cu_h.data_ptr()), B, B * T,
+                                     ctypes.c_void_p(ck_cu_h.data_ptr()), ctypes.c_void_p(ck_pos_h.data_ptr()))
+        _lib._check("kda_check_checkpoints", st)
+        ck_cu, ck_pos = ck_cu_h.to(dev), ck_pos_h.to(dev)
+        ck_states = torch.empty((B * per_seq, H, D, D), dtype=torch.float32, device=dev)
+        ck_shape = _lib.KdaShape(B, B * T, H, D, D, _lib.KDA_BF16)
+
+        def ckpt_step():
+            rc = L.kda_prefill_checkpointed(ctypes.byref(ck_shape), _lib._ptr(w.q), _lib._ptr(w.k), _lib._ptr(w.v),
+                                            _lib._ptr(w.log_alpha), _lib._ptr(w.beta), None, _lib._ptr(cu),
+                                            _lib._ptr(out), _lib._ptr(fin), _lib._ptr(ck_cu), _lib._ptr(ck_pos),
+                                            _lib._ptr(ck_states), _lib._stream(stream))
+            _lib._check("kda_prefill_checkpointed", rc)
+
+        layer["t_ck"] = timed(ckpt_step)
+        layer["n_ck"] = B * per_seq
+
+        # NEXT-4: decode steps of several tokens per sequence (state read and written once)
+        layer["multi"] = {}
+        for tm in DEC_MULTI_T:
+            mw = workloads.make_inputs(DEC_N * tm, H, D, D, dtype=torch.bfloat16, seed=13 + tm + rank,
+                                       cu_seqlens=[tm * i for i in range(DEC_N + 1)], state_std=0.05, device=dev)
+            ms_state = mw.initial_state.clone()
+            m_out = torch.empty_like(mw.v)
+            layer["multi"][tm] = timed(lambda: kda.kda_decode_step(mw.q, mw.k, mw.v, mw.log_alpha, mw.beta,
+                                                                   ms_state, m_out, stream=stream))
+            del mw, ms_state, m_out
     clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers (pinned).  Every step copies
@@ -427,6 +492,15 @@ def run_ours(args):
                              "frac": dgbytes / layer["t_dg"] / 1e9 / hbm,
                              "algorithmic_bytes_per_launch": dgbytes, "kernels": ["decode_kernel (gate and norm in its store)"]},
         }
+        ckbytes = pbytes + layer["n_ck"] * H * D * D * 4        # + every checkpoint state written once
+        line["next"] = {
+            "prefill_checkpointed": {"workload": WORKLOAD + f"_ckpt{CKPT_EVERY}", "checkpoints": layer["n_ck"],
+                                     "ms_per_step": layer["t_ck"] * 1e3, "value": world * B * T / layer["t_ck"],
+                                     "unit": UNIT, "achieved_gbs": ckbytes / layer["t_ck"] / 1e9,
+                                     "frac": ckbytes / layer["t_ck"] / 1e9 / hbm,
+                                     "algorithmic_bytes_per_launch": ckbytes, "kernels": ["chunk_tc_kernel"]},
+            "decode_multi_token": [_multi_decode_entry(tm, t_m, world, hbm) for tm, t_m in layer["multi"].items()],
+        }
     if world == 1 and not args.no_cpu_baseline:
         run, nseq, cores, used = oracle_sample(args.cpu_budget)
         t = run()
@@ -445,7 +519,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-layer", action="store_true", help="skip the front-end / gated-output timings")
+    ap.add_argument("--no-layer", action="store_true", help="skip the front-end, gated-output, checkpointed-prefill and multi-token-decode timings")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-budget", type=float, default=4.0,

@@ -14,7 +14,9 @@
 //
 // Several tokens per sequence (tokens_per_seq = T, at most 16) run through the
 // same block one after another with the state held in registers, so a short
-// multi-token step costs the same state traffic as a single token.
+// multi-token step costs the same state traffic as a single token; the T tokens'
+// vectors are staged in shared memory up front, so the token loop waits on no
+// global load.
 //
 // Layout of the work: one block of 256 threads per (sequence, head).  A row of
 // S (dv fp32) is covered by dv/4 threads with 16-byte loads, so each warp
@@ -38,7 +40,9 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 __device__ __forceinline__ void store_as(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_as(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-template <int DK, int DV, typename Tin>
+// MAXT: the largest T the instance takes (1 for the single-token step, whose shared
+// memory then stays small, or kMaxDecodeTokens).
+template <int DK, int DV, typename Tin, int MAXT>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ log_alpha, const Tin* __restrict__ beta,
@@ -47,6 +51,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     constexpr int LANES = DV / 4;          // threads per row (float4 each)
     constexpr int RG = kThreads / LANES;   // row groups
     constexpr int RPT = DK / RG;           // rows per thread
+    constexpr int kWarps = kThreads / 32;
     static_assert(RPT * RG == DK, "row split");
 
     const size_t p = blockIdx.x;           // (sequence, head) pair
@@ -60,43 +65,62 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 #pragma unroll
     for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (size_t)(g + RG * m) * LANES + c4);
 
-    __shared__ float ks[DK], qs[DK], al[DK], vs[DV], dl[DV];
-    __shared__ float red_r[RG][DV], red_y[RG][DV];
-    __shared__ float kq_s;
-    __shared__ float red_n[DV / 32];
-    __shared__ float beta_s;
-    // The T tokens of this sequence are rows n*T .. n*T+T-1; the state stays in
-    // registers between them and crosses HBM once in each direction.
-    for (int tok = 0; tok < T; ++tok) {
-        const size_t row = (n * (size_t)T + tok) * H + h;
-        for (int i = threadIdx.x; i < DK; i += kThreads) {
-            ks[i] = to_f32(k[row * DK + i]);
-            qs[i] = to_f32(q[row * DK + i]);
-            al[i] = expf(log_alpha[row * DK + i]);
-        }
-        for (int j = threadIdx.x; j < DV; j += kThreads) vs[j] = to_f32(v[row * DV + j]);
-        if (threadIdx.x == 0) beta_s = to_f32(beta[row]);
-        __syncthreads();
-
-        if (threadIdx.x < 32) {               // k . q on warp 0
+    // The vectors of all T tokens of this sequence (rows n*T .. n*T+T-1) are staged in
+    // shared memory once, next to the state read, so the token loop below waits on no
+    // global load; the state stays in registers and crosses HBM once in each direction.
+    // (dl, red_r and red_y are accessed as float4: every array is 16-byte aligned, whatever
+    // the sizes of the ones before it)
+    __shared__ __align__(16) float ks[MAXT][DK];
+    __shared__ __align__(16) float qs[MAXT][DK];
+    __shared__ __align__(16) float al[MAXT][DK];
+    __shared__ __align__(16) float vs[MAXT][DV];
+    __shared__ __align__(16) float bt[MAXT];
+    __shared__ __align__(16) float kq[MAXT];
+    __shared__ __align__(16) float dl[DV];
+    __shared__ __align__(16) float red_r[RG][DV];
+    __shared__ __align__(16) float red_y[RG][DV];
+    __shared__ __align__(16) float red_n[DV / 32];
+    if (MAXT == 1) T = 1;                   // a compile-time trip count for the single-token step
+    const size_t row0 = n * (size_t)T * H + h;         // row of token 0; token t is row0 + t * H
+    for (int i = threadIdx.x; i < T * DK; i += kThreads) {
+        const int tok = i / DK, c = i % DK;
+        const size_t e = (row0 + (size_t)tok * H) * DK + c;
+        ks[tok][c] = to_f32(k[e]);
+        qs[tok][c] = to_f32(q[e]);
+        al[tok][c] = expf(log_alpha[e]);
+    }
+    for (int i = threadIdx.x; i < T * DV; i += kThreads) {
+        const int tok = i / DV, j = i % DV;
+        vs[tok][j] = to_f32(v[(row0 + (size_t)tok * H) * DV + j]);
+    }
+    if (threadIdx.x < T) bt[threadIdx.x] = to_f32(beta[row0 + (size_t)threadIdx.x * H]);
+    __syncthreads();
+    {                                       // k . q of every token, one warp per token
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int tok = w; tok < T; tok += kWarps) {
             float acc = 0.f;
-            for (int i = threadIdx.x; i < DK; i += 32) acc = fmaf(ks[i], qs[i], acc);
+            for (int i = lane; i < DK; i += 32) acc = fmaf(ks[tok][i], qs[tok][i], acc);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (threadIdx.x == 0) kq_s = acc;
+            if (lane == 0) kq[tok] = acc;
         }
+    }                                       // (read after the first barrier of the token loop)
 
+    for (int tok = 0; tok < T; ++tok) {
+        const size_t row = row0 + (size_t)tok * H;
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f), y = r;
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int i = g + RG * m;
-            const float a = al[i], ki = ks[i], qi = qs[i];
+            const float a = al[tok][i], ki = ks[tok][i], qi = qs[tok][i];
             s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
             r.x = fmaf(s[m].x, ki, r.x); r.y = fmaf(s[m].y, ki, r.y);
             r.z = fmaf(s[m].z, ki, r.z); r.w = fmaf(s[m].w, ki, r.w);
             y.x = fmaf(s[m].x, qi, y.x); y.y = fmaf(s[m].y, qi, y.y);
             y.z = fmaf(s[m].z, qi, y.z); y.w = fmaf(s[m].w, qi, y.w);
         }
+        // (every thread read the previous token's partial sums before that token's second
+        // barrier, so they can be overwritten now)
         *reinterpret_cast<float4*>(&red_r[g][4 * c4]) = r;
         *reinterpret_cast<float4*>(&red_y[g][4 * c4]) = y;
         __syncthreads();
@@ -108,9 +132,9 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
             float rj = 0.f, yj = 0.f;
 #pragma unroll
             for (int gg = 0; gg < RG; ++gg) { rj += red_r[gg][j]; yj += red_y[gg][j]; }
-            const float d = beta_s * (vs[j] - rj);
+            const float d = bt[tok] * (vs[tok][j] - rj);
             dl[j] = d;
-            oj = fmaf(kq_s, d, yj);
+            oj = fmaf(kq[tok], d, yj);
             if (!gate) store_as(&out[row * DV + j], oj);
         }
         if (gate) {   // gated output: RMSNorm over the DV channels (warps 0 .. DV/32-1) x weight x sigmoid(gate)
@@ -123,9 +147,9 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
                 float tot = 0.f;
 #pragma unroll
                 for (int w = 0; w < DV / 32; ++w) tot += red_n[w];
-                const float r = rsqrtf(tot * (1.f / DV) + norm_eps);
+                const float rn = rsqrtf(tot * (1.f / DV) + norm_eps);
                 const float gv = to_f32(gate[row * DV + j]);
-                store_as(&out[row * DV + j], oj * r * norm_w[j] / (1.f + __expf(-gv)));
+                store_as(&out[row * DV + j], oj * rn * norm_w[j] / (1.f + __expf(-gv)));
             }
         }
         __syncthreads();
@@ -133,33 +157,40 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         const float4 d4 = *reinterpret_cast<const float4*>(&dl[4 * c4]);
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
-            const float ki = ks[g + RG * m];
+            const float ki = ks[tok][g + RG * m];
             s[m].x = fmaf(ki, d4.x, s[m].x); s[m].y = fmaf(ki, d4.y, s[m].y);
             s[m].z = fmaf(ki, d4.z, s[m].z); s[m].w = fmaf(ki, d4.w, s[m].w);
         }
-        __syncthreads();   // the vectors of this token are dead before the next token's load
+        // the next token's dl and red_n are written only after its first barrier, which every
+        // thread reaches after this update
     }
 #pragma unroll
     for (int m = 0; m < RPT; ++m) __stcs(Sp + (size_t)(g + RG * m) * LANES + c4, s[m]);
 }
 
-template <int DK, int DV>
-cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
+template <int DK, int DV, int MAXT>
+cudaError_t launch_dims_t(const DecodeArgs& a, cudaStream_t st) {
     const unsigned blocks = (unsigned)((size_t)a.num_seqs * a.H);
     if (a.dtype == DType::F32) {
-        decode_kernel<DK, DV, float><<<blocks, kThreads, 0, st>>>(
+        decode_kernel<DK, DV, float, MAXT><<<blocks, kThreads, 0, st>>>(
             static_cast<const float*>(a.q), static_cast<const float*>(a.k),
             static_cast<const float*>(a.v), a.log_alpha, static_cast<const float*>(a.beta),
             a.state, static_cast<float*>(a.out), a.H, a.tokens_per_seq, static_cast<const float*>(a.gate),
             a.norm_w, a.norm_eps);
     } else {
-        decode_kernel<DK, DV, __nv_bfloat16><<<blocks, kThreads, 0, st>>>(
+        decode_kernel<DK, DV, __nv_bfloat16, MAXT><<<blocks, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
             static_cast<const __nv_bfloat16*>(a.v), a.log_alpha,
             static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out), a.H,
             a.tokens_per_seq, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w, a.norm_eps);
     }
     return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
+    if (a.tokens_per_seq < 1 || a.tokens_per_seq > kMaxDecodeTokens) return cudaErrorInvalidValue;
+    return a.tokens_per_seq == 1 ? launch_dims_t<DK, DV, 1>(a, st) : launch_dims_t<DK, DV, kMaxDecodeTokens>(a, st);
 }
 
 }  // namespace
