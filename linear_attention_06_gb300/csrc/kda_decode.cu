@@ -20,8 +20,10 @@
 //
 // Layout of the work: one block of 256 threads per (sequence, head).  A row of
 // S (dv fp32) is covered by dv/4 threads with 16-byte loads, so each warp
-// instruction moves whole 512-byte rows; each thread keeps its rows in
-// registers between the read and the write, so S crosses HBM exactly twice.
+// instruction moves whole 512-byte rows; each thread keeps its rows (a run of
+// consecutive key rows, so the per-row decay, k and q come as 16-byte shared
+// broadcasts) in registers between the read and the write, so S crosses HBM
+// exactly twice.
 // The two column reductions are done per thread over its rows, then across
 // row groups through shared memory.  Loads and stores use the streaming cache
 // hints (each byte is touched once).
@@ -52,7 +54,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     constexpr int RG = kThreads / LANES;   // row groups
     constexpr int RPT = DK / RG;           // rows per thread
     constexpr int kWarps = kThreads / 32;
-    static_assert(RPT * RG == DK, "row split");
+    static_assert(RPT * RG == DK && RPT % 4 == 0, "row split in groups of four rows");
 
     const size_t p = blockIdx.x;           // (sequence, head) pair
     const size_t n = p / H, h = p % H;
@@ -63,7 +65,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     // Issue the whole state read first so it overlaps the small loads.
     float4 s[RPT];
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (size_t)(g + RG * m) * LANES + c4);
+    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (size_t)(g * RPT + m) * LANES + c4);
 
     // The vectors of all T tokens of this sequence (rows n*T .. n*T+T-1) are staged in
     // shared memory once, next to the state read, so the token loop below waits on no
@@ -110,14 +112,22 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         const size_t row = row0 + (size_t)tok * H;
         float4 r = make_float4(0.f, 0.f, 0.f, 0.f), y = r;
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const int i = g + RG * m;
-            const float a = al[tok][i], ki = ks[tok][i], qi = qs[tok][i];
-            s[m].x *= a; s[m].y *= a; s[m].z *= a; s[m].w *= a;
-            r.x = fmaf(s[m].x, ki, r.x); r.y = fmaf(s[m].y, ki, r.y);
-            r.z = fmaf(s[m].z, ki, r.z); r.w = fmaf(s[m].w, ki, r.w);
-            y.x = fmaf(s[m].x, qi, y.x); y.y = fmaf(s[m].y, qi, y.y);
-            y.z = fmaf(s[m].z, qi, y.z); y.w = fmaf(s[m].w, qi, y.w);
+        for (int m = 0; m < RPT; m += 4) {         // a warp shares its rows: 16-byte broadcasts
+            const int i = g * RPT + m;
+            const float4 a4 = *reinterpret_cast<const float4*>(&al[tok][i]);
+            const float4 k4 = *reinterpret_cast<const float4*>(&ks[tok][i]);
+            const float4 q4 = *reinterpret_cast<const float4*>(&qs[tok][i]);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w},
+                        qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float4& e = s[m + u];
+                e.x *= av[u]; e.y *= av[u]; e.z *= av[u]; e.w *= av[u];
+                r.x = fmaf(e.x, kv[u], r.x); r.y = fmaf(e.y, kv[u], r.y);
+                r.z = fmaf(e.z, kv[u], r.z); r.w = fmaf(e.w, kv[u], r.w);
+                y.x = fmaf(e.x, qv[u], y.x); y.y = fmaf(e.y, qv[u], y.y);
+                y.z = fmaf(e.z, qv[u], y.z); y.w = fmaf(e.w, qv[u], y.w);
+            }
         }
         // (every thread read the previous token's partial sums before that token's second
         // barrier, so they can be overwritten now)
@@ -156,16 +166,21 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 
         const float4 d4 = *reinterpret_cast<const float4*>(&dl[4 * c4]);
 #pragma unroll
-        for (int m = 0; m < RPT; ++m) {
-            const float ki = ks[tok][g + RG * m];
-            s[m].x = fmaf(ki, d4.x, s[m].x); s[m].y = fmaf(ki, d4.y, s[m].y);
-            s[m].z = fmaf(ki, d4.z, s[m].z); s[m].w = fmaf(ki, d4.w, s[m].w);
+        for (int m = 0; m < RPT; m += 4) {
+            const float4 k4 = *reinterpret_cast<const float4*>(&ks[tok][g * RPT + m]);
+            const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float4& e = s[m + u];
+                e.x = fmaf(kv[u], d4.x, e.x); e.y = fmaf(kv[u], d4.y, e.y);
+                e.z = fmaf(kv[u], d4.z, e.z); e.w = fmaf(kv[u], d4.w, e.w);
+            }
         }
         // the next token's dl and red_n are written only after its first barrier, which every
         // thread reaches after this update
     }
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) __stcs(Sp + (size_t)(g + RG * m) * LANES + c4, s[m]);
+    for (int m = 0; m < RPT; ++m) __stcs(Sp + (size_t)(g * RPT + m) * LANES + c4, s[m]);
 }
 
 template <int DK, int DV, int MAXT>
