@@ -244,6 +244,18 @@ kda_status kda_check_cu_seqlens(const int32_t* host_cu_seqlens, int32_t num_seqs
                                 int64_t total_tokens);
 
 /*
+ * kda_selftest_timeout -- diagnostic for the timeout path.  Enqueues on
+ * `stream` one single-thread kernel that waits, with the same bounded wait as
+ * every kernel of the library, on a barrier that nothing completes; after
+ * `limit_ns` nanoseconds (1e3 .. 1e9) the wait gives up and the kernel sets the
+ * timeout bit of the status word, so the next kda_device_status returns
+ * KDA_ERR_TIMEOUT.  No GPU fault, trap or hang is involved.  Returns KDA_OK
+ * (enqueued), KDA_ERR_INVALID_ARG for a limit out of range (nothing enqueued)
+ * or KDA_ERR_CUDA if the launch fails.
+ */
+kda_status kda_selftest_timeout(uint64_t limit_ns, kda_stream_t stream);
+
+/*
  * kda_device_status -- synchronise `stream`, then read and clear the device
  * status word.  Returns KDA_ERR_TIMEOUT if a kernel's bounded wait gave up
  * since the last call (that kernel's outputs are then undefined), KDA_OK

@@ -56,6 +56,8 @@ def lib():
         L.kda_check_cu_seqlens.restype = ctypes.c_int
         L.kda_device_status.argtypes = [vp]
         L.kda_device_status.restype = ctypes.c_int
+        L.kda_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
+        L.kda_selftest_timeout.restype = ctypes.c_int
         L.kda_prefill_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
         L.kda_prefill_gated.restype = ctypes.c_int
         L.kda_decode_step_gated.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp, vp]
@@ -289,3 +291,10 @@ def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):
 def kda_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(lib().kda_device_status(_stream(stream)))
+
+
+def kda_selftest_timeout(limit_ns: int = 1_000_000, stream=None) -> None:
+    """Enqueue the timeout-path self test (see ``include/kda.h``): a bounded wait that
+    nothing completes gives up after ``limit_ns`` and sets the status word, so the next
+    kda_device_status returns KDA_ERR_TIMEOUT."""
+    _check("kda_selftest_timeout", lib().kda_selftest_timeout(int(limit_ns), _stream(stream)))

@@ -13,6 +13,7 @@
 
 #include "kda.h"
 #include "kda_internal.h"
+#include "sm103_primitives.cuh"
 
 // Device status word; bit kda::kStatusTimeout is set by a kernel whose bounded
 // wait ran out.  Read and cleared by kda_device_status.
@@ -37,6 +38,17 @@ unsigned int* status_word() {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One thread waits, with the library's bounded wait, on an mbarrier that nothing
+// arrives on; when the wait gives up it records the timeout as every kernel does.
+__global__ void selftest_timeout_kernel(unsigned int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        kda::sm103::mbar_init(&bar, 1);
+        kda::sm103::fence_mbar_init();
+        if (!kda::sm103::mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(status, kda::kStatusTimeout);
+    }
+}
 
 bool env_flag(const char* name) {
     const char* v = getenv(name);
@@ -261,6 +273,15 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, c
                         shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return finish(kda::launch_frontend(a, s), s);
+}
+
+kda_status kda_selftest_timeout(uint64_t limit_ns, kda_stream_t stream) {
+    if (limit_ns < 1000ull || limit_ns > 1000000000ull) return KDA_ERR_INVALID_ARG;
+    unsigned int* p = status_word();
+    if (!p) return KDA_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    selftest_timeout_kernel<<<1, 32, 0, s>>>(p, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_device_status(kda_stream_t stream) {

@@ -116,6 +116,12 @@ def test_valid_call_without_gpu_reports_cuda_error(L):
     assert prefill(L, shape()) == _lib.KDA_ERR_CUDA
 
 
+def test_selftest_timeout_rejects_limits_out_of_range(L):
+    # checked on the host before any CUDA call
+    for bad in (0, 999, 1_000_000_001, 2**63):
+        assert L.kda_selftest_timeout(bad, None) == _lib.KDA_ERR_INVALID_ARG
+
+
 def test_decode_multi_token_argument_rules(L):
     E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
     assert decode(L, shape(n=4, T=4 * 17)) == E_UNS         # more than 16 tokens per sequence

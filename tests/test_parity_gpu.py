@@ -219,6 +219,17 @@ def test_recurrent_and_chunk_paths_agree(monkeypatch):
     assert rel_l2(np64(o_a), np64(o_b)) < 5e-3 and rel_l2(np64(f_a), np64(f_b)) < 5e-3
 
 
+def test_timeout_path_sets_and_clears_the_status_word():
+    # a bounded wait that nothing completes (1 ms): no fault, the context stays usable
+    assert kda.kda_device_status() == 0
+    kda.kda_selftest_timeout(1_000_000)
+    assert kda.kda_device_status() == 4                    # KDA_ERR_TIMEOUT
+    assert kda.kda_device_status() == 0                    # read and cleared
+    w = workloads.make_inputs(64, 2, 128, 128, seed=77).to(DEV)
+    compare_prefill(w)                                     # the library still runs
+    assert kda.kda_device_status() == 0
+
+
 def test_device_status_is_clean():
     assert kda.kda_device_status() == 0
 
