@@ -374,9 +374,12 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 
 // One warp: columns [8 nt, 8 nt + 8) of C = sign * sum_p A_p B_p for 16x16 blocks (blk_at
 // layout).
-template <int NP>
+// With WT, the block is also written, column-scaled by beta, as bf16 into the T tile at
+// rows trow0 + 0..15, columns tcol0 + 0..15.
+template <int NP, bool WT = false>
 __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP], const float* const (&Bb)[NP],
-                                        int nt, float sign) {
+                                        int nt, float sign, uint8_t* tt = nullptr, int trow0 = 0, int tcol0 = 0,
+                                        const __nv_bfloat16* beta = nullptr) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -395,13 +398,22 @@ __device__ __forceinline__ void blk_mma(float* Cb, const float* const (&Ab)[NP],
     const int c0 = 8 * nt + 2 * t;                   // a column pair stays adjacent under the swizzle
     *reinterpret_cast<float2*>(Cb + blk_at(g, c0)) = make_float2(sign * d[0], sign * d[1]);
     *reinterpret_cast<float2*>(Cb + blk_at(g + 8, c0)) = make_float2(sign * d[2], sign * d[3]);
+    if constexpr (WT) {
+        const float b0 = bf2f(beta[tcol0 + c0]), b1 = bf2f(beta[tcol0 + c0 + 1]);
+        const uint32_t cb = 2u * (uint32_t)(tcol0 + c0);
+        *reinterpret_cast<uint32_t*>(tt + sw128_offset(trow0 + g, cb)) = pack_bf16x2(sign * d[0] * b0, sign * d[1] * b1);
+        *reinterpret_cast<uint32_t*>(tt + sw128_offset(trow0 + g + 8, cb)) =
+            pack_bf16x2(sign * d[2] * b0, sign * d[3] * b1);
+    }
 }
 
 // T = (I + N)^{-1} Diag(beta) with N strictly lower 64x64 (10 lower 16x16 blocks in the A slot):
 // D_i = (I + N_ii)^{-1} by fp32 forward substitution; then the 32x32 halves
 // X_10 = -D_1 N_10 D_0, X_32 = -D_3 N_32 D_2; then the lower-left 32x32 quarter
 // -C^{-1} (B A^{-1}) with A^{-1}, C^{-1} the inverted halves and B = N[32:64, 0:32], using TF32
-// tensor-core block products with fp32 accumulation.  Team S (4 warps), 4 team barriers.
+// tensor-core block products with fp32 accumulation.  Each step writes the blocks of T it
+// finishes (X column-scaled by beta, bf16, into the swizzled T tile) as it stores them, and
+// the idle warps of the first step write T's zero blocks.  Team S (4 warps), 4 team barriers.
 __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) {
 #ifdef KDA_PHASE_TIMING
     long long sp_ = clock64();
@@ -424,6 +436,22 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) 
         float* Xii = blk(Xb, i, i);
 #pragma unroll
         for (int r = 0; r < 16; ++r) Xii[blk_at(r, jl)] = x[r];
+        const float bj = bf2f(beta[16 * i + jl]);        // T_ii column jl = D_i column jl x beta
+        uint8_t* tt = aslot + kTT;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            *reinterpret_cast<__nv_bfloat16*>(tt + sw128_offset(16 * i + r, 2 * (16 * i + jl))) =
+                __float2bfloat16_rn(x[r] * bj);
+    } else {                                         // the zero blocks above the diagonal of T
+        const int u = t - 64;                        // 64 threads x 3 of the 6 x 16 rows x 2 16-byte pieces
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int id = u + 64 * k;               // 0 .. 191: block (6), row (16), half (2)
+            const int b = id >> 5, rr = (id >> 1) & 15, hf = id & 1;
+            const int bi = b < 3 ? 0 : (b < 5 ? 1 : 2), q = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+            *reinterpret_cast<uint4*>(aslot + kTT + sw128_offset(16 * bi + rr, 32 * q + 16 * hf)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     group_sync(kBarS);
 #ifdef KDA_PHASE_TIMING
@@ -445,7 +473,7 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) 
         {
             const float* A1[1] = {blk(Xb, i0 + 1, i0 + 1)};
             const float* B1[1] = {Ys};
-            blk_mma<1>(blk(Xb, i0 + 1, i0), A1, B1, nt, -1.f);
+            blk_mma<1, true>(blk(Xb, i0 + 1, i0), A1, B1, nt, -1.f, aslot + kTT, 16 * (i0 + 1), 16 * i0, beta);
         }
     }
     group_sync(kBarS);
@@ -454,8 +482,8 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) 
 #endif
     // Y = B A^{-1}: Y_20 = N_20 D_0 + N_21 X_10, Y_21 = N_21 D_1, Y_30 = N_30 D_0 + N_31 X_10, Y_31 = N_31 D_1
 #pragma unroll 1
-    for (int it = 0; it < 2; ++it) {
-        const int item = w + 4 * it, ob = item >> 1, nt = item & 1;   // ob: 0 Y20, 1 Y21, 2 Y30, 3 Y31
+    for (int it = 0; it < 2; ++it) {                 // each warp: one two-term and one one-term block
+        const int ob = 2 * (w >> 1) + it, nt = w & 1;   // ob: 0 Y20, 1 Y21, 2 Y30, 3 Y31
         const int ri = 2 + (ob >> 1), cj = ob & 1;
         float* Ys = Yb + ob * (kBlkBytes / 4);
         if (cj == 0) {
@@ -480,42 +508,18 @@ __device__ void solve_T(uint8_t* aslot, const __nv_bfloat16* beta, Small* x_sw) 
         if (ri == 2) {
             const float* A1[1] = {blk(Xb, 2, 2)};
             const float* B1[1] = {Yb + cj * (kBlkBytes / 4)};
-            blk_mma<1>(blk(Xb, 2, cj), A1, B1, nt, -1.f);
+            blk_mma<1, true>(blk(Xb, 2, cj), A1, B1, nt, -1.f, aslot + kTT, 32, 16 * cj, beta);
         } else {
             const float* A2[2] = {blk(Xb, 3, 2), blk(Xb, 3, 3)};
             const float* B2[2] = {Yb + cj * (kBlkBytes / 4), Yb + (2 + cj) * (kBlkBytes / 4)};
-            blk_mma<2>(blk(Xb, 3, cj), A2, B2, nt, -1.f);
+            blk_mma<2, true>(blk(Xb, 3, cj), A2, B2, nt, -1.f, aslot + kTT, 48, 16 * cj, beta);
         }
     }
     group_sync(kBarS);
 #ifdef KDA_PHASE_TIMING
     if (t == 0) { const long long c_ = clock64(); x_sw->phase[26 + 4] += (unsigned long long)(c_ - sp_); sp_ = c_; }
 #endif
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {                 // T[r][s] = X[r][s] beta_s (bf16)
-        const int tt = t + kTeam * it, r = tt >> 2, q = tt & 3, bi = r >> 4, rr = r & 15;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int s0 = 16 * q + 8 * k;
-            uint32_t wv[4];
-            if (q <= bi) {
-                const float* xb = blk(Xb, bi, q);
-                const float4 lo = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k));
-                const float4 hi = *reinterpret_cast<const float4*>(xb + blk_at(rr, 8 * k + 4));
-                const float xr[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                const uint4 bw = *reinterpret_cast<const uint4*>(beta + s0);   // beta_{s0 .. s0+7}
-                const uint32_t bv[4] = {bw.x, bw.y, bw.z, bw.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    wv[u] = pack_bf16x2(xr[2 * u] * __uint_as_float(bv[u] << 16),
-                                        xr[2 * u + 1] * __uint_as_float(bv[u] & 0xffff0000u));
-            } else {
-                wv[0] = wv[1] = wv[2] = wv[3] = 0u;
-            }
-            *reinterpret_cast<uint4*>(aslot + kTT + sw128_offset(r, 16 * (2 * q + k))) =
-                make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        }
-    }
+    // (every block of T was written by the step that computed it)
 }
 
 // ============================ group B: state stage ===============================
@@ -934,9 +938,11 @@ __device__ __noinline__ bool run_team_s(const Ctx& x_in) {
         }
         tc_fence_after();
         read_gram(x.tb, tm_apw(s), aslot, pp, sw.beta[s]);
+        // the first solve step of each warp reads only the N rows that warp wrote (warp 0:
+        // blocks 0, 1; warp 1: blocks 2, 3; warps 2 and 3 wrote P and go on to T's zero
+        // blocks), so a warp barrier suffices here; the solve's own barriers order the rest
         fence_proxy_async_smem();
-        tc_fence_before();
-        group_sync(kBarS);
+        __syncwarp();
         KDA_PHASE(6);
         solve_T(aslot, sw.beta[s], x.sw);
         KDA_PHASE(15);
