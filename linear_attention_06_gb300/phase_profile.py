@@ -24,8 +24,9 @@ products ("GEMM phases": the union of the issue-to-completion intervals) that
 their arithmetic needs at the pipe's dense bf16 rate of 8192 flop per SM cycle
 (an M=128, N=256, K=16 product per 128 cycles); stamps can only be late, so
 that share is a lower bound.  Only block 0 is instrumented and the events stay
-in shared memory until the block ends; the launch time is printed to show that
-the kernel runs at its normal speed.
+in shared memory until the block ends; the launch time is printed so that it can
+be set against the uninstrumented kernel's (the stamped block runs a few per
+cent slower).
 
 The workload is the benchmark prefill: B=4 sequences of T=8192 tokens, H=32
 heads, dk=dv=128, bf16 inputs, zero initial state.
