@@ -33,7 +33,15 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // caller's buffers are 16-byte aligned and CPL * sizeof(T) divides 16).
 template <typename T, int CPL>
 __device__ __forceinline__ void load_row(const T* p, float (&x)[CPL]) {
-    if constexpr (sizeof(T) == 2 && CPL == 4) {
+    if constexpr (sizeof(T) == 2 && CPL == 8) {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else if constexpr (sizeof(T) == 2 && CPL == 4) {
         const uint2 u = *reinterpret_cast<const uint2*>(p);
         x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
         x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
@@ -53,7 +61,15 @@ __device__ __forceinline__ void load_row(const T* p, float (&x)[CPL]) {
 }
 template <typename T, int CPL>
 __device__ __forceinline__ void store_row(T* p, const float (&x)[CPL]) {
-    if constexpr (sizeof(T) == 2 && CPL == 4) {
+    if constexpr (sizeof(T) == 2 && CPL == 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (sizeof(T) == 2 && CPL == 4) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]), hi = __floats2bfloat162_rn(x[2], x[3]);
         uint2 u;
         u.x = *reinterpret_cast<uint32_t*>(&lo);
@@ -124,13 +140,14 @@ __device__ __forceinline__ void conv_step(const float (&x)[CPL], float (&hist)[W
     }
 }
 
-template <int CPL>
-__device__ __forceinline__ void l2_normalize(float (&y)[CPL], float eps) {
+// The LPR lanes of `mask` (an aligned group) hold one row between them.
+template <int CPL, int LPR>
+__device__ __forceinline__ void l2_normalize(float (&y)[CPL], float eps, unsigned mask) {
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) ss = fmaf(y[c], y[c], ss);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
     const float r = rsqrtf(ss + eps);
 #pragma unroll
     for (int c = 0; c < CPL; ++c) y[c] *= r;
@@ -161,23 +178,30 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// One of q (tensor z0 + blockIdx.z = 0), k (1) or v (2) for a run of kRun tokens of
-// one head.  The run's raw rows are copied into shared memory kStage at a time
-// (every lane its own channels, all copies in flight together, no registers held),
-// then convolved with the history kept in registers, passed through SiLU and (q,
-// k) normalised.
-template <typename T, int CPL, int W>
+// One of q (tensor z0 + blockIdx.z = 0), k (1) or v (2) for kRun tokens of one head
+// per warp.  LPR lanes hold a row (CPL channels each); with LPR = 16 the two halves of
+// a warp walk two runs of kRun / 2 tokens side by side.  A run's raw rows are copied
+// into shared memory kStage at a time (every lane its own channels, all copies in
+// flight together, no registers held), then convolved with the history kept in
+// registers, passed through SiLU and (q, k) normalised.
+template <typename T, int CPL, int W, int LPR>
 __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z0) {
+    static_assert(LPR == 16 || LPR == 32, "a row is half a warp or a warp");
+    constexpr int RPW = 32 / LPR;                                 // runs per warp
+    constexpr int kSub = kRun / RPW;                              // tokens per run
     constexpr int kSeg = CPL * (int)sizeof(T);                    // bytes per lane and row
-    constexpr int kStage = kSeg * 32 * kRun <= 8192 ? kRun : 8192 / (kSeg * 32);
-    __shared__ __align__(16) uint8_t stage[kWarps][kStage][32 * kSeg];
+    constexpr int kRow = LPR * kSeg;                              // bytes per staged row
+    constexpr int kStage = kRow * kRun <= 8192 ? kSub : 8192 / (kRow * RPW);
+    __shared__ __align__(16) uint8_t stage[kWarps][RPW][kStage][kRow];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LPR, ll = lane % LPR;
+    const unsigned mask = LPR == 32 ? 0xffffffffu : (0xffffu << (16 * sub));
     const int h = blockIdx.y, which = z0 + (int)blockIdx.z;
-    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
+    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + warp) * kRun + (int64_t)sub * kSub;
     if (t_begin >= a.total_tokens) return;
-    const int64_t t_end = min(t_begin + kRun, a.total_tokens);
+    const int64_t t_end = min(t_begin + kSub, a.total_tokens);
     const int H = a.H, d = which == 2 ? a.dv : a.dk;
-    const int c0 = lane * CPL;
+    const int c0 = ll * CPL;
     const T* __restrict__ src = static_cast<const T*>(which == 0 ? a.q_raw : which == 1 ? a.k_raw : a.v_raw);
     T* __restrict__ dst = static_cast<T*>(which == 0 ? a.q : which == 1 ? a.k : a.v);
     const float* __restrict__ conv = which == 0 ? a.conv_q : which == 1 ? a.conv_k : a.conv_v;
@@ -200,13 +224,13 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
         for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
         if (W > 1 && sr >= bos) load_row<T, CPL>(src + (sr * H + h) * d + c0, hist[i]);
     }
-    uint8_t* mine = &stage[warp][0][lane * kSeg];
+    uint8_t* mine = &stage[warp][sub][0][ll * kSeg];
     const int64_t rstride = (int64_t)H * d;              // elements from one token's row to the next
     const T* sp = src + (t_begin * H + h) * d + c0;
     T* dp = dst + (t_begin * H + h) * d + c0;
     for (int64_t ts = t_begin; ts < t_end; ts += kStage) {
         const int n = (int)min((int64_t)kStage, t_end - ts);
-        for (int j = 0; j < n; ++j, sp += rstride) cp_async<kSeg>(mine + j * 32 * kSeg, sp);
+        for (int j = 0; j < n; ++j, sp += rstride) cp_async<kSeg>(mine + j * kRow, sp);
         cp_async_wait_all();                             // this lane's own copies
 #pragma unroll 4
         for (int j = 0; j < n; ++j, dp += rstride) {
@@ -219,9 +243,9 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
                     for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
             }
             float xr[CPL], y[CPL];
-            load_row<T, CPL>(reinterpret_cast<const T*>(mine + j * 32 * kSeg), xr);
+            load_row<T, CPL>(reinterpret_cast<const T*>(mine + j * kRow), xr);
             conv_step<CPL, W, sizeof(T) == 2>(xr, hist, wt, y);   // bf16 outputs: the tanh form
-            if (norm) l2_normalize<CPL>(y, a.eps);
+            if (norm) l2_normalize<CPL, LPR>(y, a.eps, mask);
             store_row<T, CPL>(dp, y);
         }
     }
@@ -254,16 +278,26 @@ __global__ void __launch_bounds__(kWarps * 32) gate_kernel(FrontendArgs a) {
     }
 }
 
-template <typename T, int CPL>
+template <typename T, int CPL, int LPR>
 cudaError_t launch_conv(const FrontendArgs& a, dim3 grid, int z0, cudaStream_t s) {
     switch (a.conv_width) {
-        case 1: conv_kernel<T, CPL, 1><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 2: conv_kernel<T, CPL, 2><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 3: conv_kernel<T, CPL, 3><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 4: conv_kernel<T, CPL, 4><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 1: conv_kernel<T, CPL, 1, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 2: conv_kernel<T, CPL, 2, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 3: conv_kernel<T, CPL, 3, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 4: conv_kernel<T, CPL, 4, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+// A row of d channels: bf16 rows are split over half a warp (16-byte accesses), fp32 rows over
+// a warp.
+template <typename T>
+cudaError_t launch_rows(const FrontendArgs& a, int d, dim3 grid, int z0, cudaStream_t s) {
+    if constexpr (sizeof(T) == 2)
+        return d == 128 ? launch_conv<T, 8, 16>(a, grid, z0, s) : launch_conv<T, 4, 16>(a, grid, z0, s);
+    else
+        return d == 128 ? launch_conv<T, 4, 32>(a, grid, z0, s) : launch_conv<T, 2, 32>(a, grid, z0, s);
 }
 
 template <typename T>
@@ -272,11 +306,11 @@ cudaError_t launch_t(const FrontendArgs& a, cudaStream_t s) {
     const unsigned bx = (unsigned)((runs + kWarps - 1) / kWarps);
     cudaError_t e;
     if (a.dk == a.dv) {                                  // q, k, v: grid.z = 0, 1, 2
-        e = a.dk == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 3), 0, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 3), 0, s);
+        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 3), 0, s);
     } else {                                             // q and k, then v with its own width
-        e = a.dk == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 2), 0, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 2), 0, s);
+        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 2), 0, s);
         if (e == cudaSuccess)
-            e = a.dv == 128 ? launch_conv<T, 4>(a, dim3(bx, a.H, 1), 2, s) : launch_conv<T, 2>(a, dim3(bx, a.H, 1), 2, s);
+            e = launch_rows<T>(a, a.dv, dim3(bx, a.H, 1), 2, s);
     }
     if (e != cudaSuccess) return e;
     const int64_t rows = a.total_tokens * a.H;
