@@ -63,7 +63,8 @@ typedef enum {
     KDA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad cu_seqlens  */
     KDA_ERR_UNSUPPORTED = 2,  /* dtype / head size / alignment not supported  */
     KDA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed          */
-    KDA_ERR_TIMEOUT = 4       /* a bounded in-kernel wait gave up (see below)  */
+    KDA_ERR_TIMEOUT = 4,      /* a bounded in-kernel wait gave up (see below)  */
+    KDA_ERR_BOUNDS = 5        /* bounds-checked builds only: an index left its buffer */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -258,8 +259,10 @@ kda_status kda_selftest_timeout(uint64_t limit_ns, kda_stream_t stream);
 /*
  * kda_device_status -- synchronise `stream`, then read and clear the device
  * status word.  Returns KDA_ERR_TIMEOUT if a kernel's bounded wait gave up
- * since the last call (that kernel's outputs are then undefined), KDA_OK
- * otherwise, or KDA_ERR_CUDA if the synchronisation fails.  Setting the
+ * since the last call (that kernel's outputs are then undefined), KDA_ERR_BOUNDS
+ * if, in a library built with -DKDA_CHECK_BOUNDS (a diagnostic build), a kernel
+ * skipped a global-memory access whose index left its buffer, KDA_OK otherwise,
+ * or KDA_ERR_CUDA if the synchronisation fails.  Setting the
  * environment variable KDA_DEBUG_SYNC=1 makes kda_prefill and kda_decode_step
  * call this themselves before returning.
  */

@@ -145,7 +145,7 @@ kda_status prefill_impl(const kda_shape* shape, const void* q, const void* k, co
         e = kda::launch_recurrent_prefill(a, s);
     if (e == cudaSuccess && gate)                          // gated output: one row pass over out
         e = kda::launch_gated_norm(out, gate, norm_w, norm_eps, shape->total_tokens * shape->H,
-                                   shape->dv, a.dtype, s);
+                                   shape->dv, a.dtype, s, a.status);
     return finish(e, s);
 }
 }  // namespace
@@ -221,6 +221,8 @@ kda_status decode_impl(const kda_shape* shape, const void* q, const void* k, con
     kda::DecodeArgs a{q, k, v, log_alpha, beta, state_inout, out, shape->num_seqs, (int32_t)tps, shape->H,
                       shape->dk, shape->dv,
                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, gate, norm_w, norm_eps};
+    a.status = status_word();
+    if (!a.status) return KDA_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return finish(kda::launch_decode(a, s), s);
 }
@@ -271,6 +273,8 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, c
                         q, k, v, log_alpha, beta, shape->total_tokens, shape->num_seqs, shape->H,
                         shape->dk, shape->dv, conv_width, eps,
                         shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32};
+    a.status = status_word();
+    if (!a.status) return KDA_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return finish(kda::launch_frontend(a, s), s);
 }
@@ -297,7 +301,8 @@ kda_status kda_device_status(kda_stream_t stream) {
         if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
-    return (word & kda::kStatusTimeout) ? KDA_ERR_TIMEOUT : KDA_OK;
+    if (word & kda::kStatusTimeout) return KDA_ERR_TIMEOUT;
+    return (word & kda::kStatusBounds) ? KDA_ERR_BOUNDS : KDA_OK;
 }
 
 const char* kda_status_string(kda_status s) {
@@ -307,6 +312,7 @@ const char* kda_status_string(kda_status s) {
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_BOUNDS: return "KDA_ERR_BOUNDS";
     }
     return "KDA_ERR_UNKNOWN";
 }

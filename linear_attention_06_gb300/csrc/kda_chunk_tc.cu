@@ -594,20 +594,23 @@ __device__ __forceinline__ void o_to_regs(uint32_t tb, uint32_t col, uint32_t (&
     }
 }
 
-__device__ void load_state(uint32_t tb, const float* h0, size_t base) {
+// (lim: floats in the state buffer, for the index checks of bounds-checked builds)
+__device__ void load_state(uint32_t tb, const float* h0, size_t base, int64_t lim, unsigned int* status) {
     const int j = lt();
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            r[i] = h0 ? __float_as_uint(h0[base + (size_t)(32 * cb + i) * D + j]) : 0u;
+        for (int i = 0; i < 32; ++i) {
+            const size_t e = base + (size_t)(32 * cb + i) * D + j;
+            r[i] = (h0 && KDA_INDEX_OK(e, lim, status)) ? __float_as_uint(h0[e]) : 0u;
+        }
         tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), r);
     }
     tmem_wait_st();
 }
 
-__device__ void store_state(uint32_t tb, float* hT, size_t base) {
+__device__ void store_state(uint32_t tb, float* hT, size_t base, int64_t lim, unsigned int* status) {
     const int j = lt();
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
@@ -615,7 +618,10 @@ __device__ void store_state(uint32_t tb, float* hT, size_t base) {
         tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), r);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) hT[base + (size_t)(32 * cb + i) * D + j] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) {
+            const size_t e = base + (size_t)(32 * cb + i) * D + j;
+            if (KDA_INDEX_OK(e, lim, status)) hT[e] = __uint_as_float(r[i]);
+        }
     }
 }
 
@@ -784,6 +790,9 @@ struct Ctx {
     uint32_t tb;
     int64_t bos, eos;
     int nchunks, H, h, seq;
+    int64_t T;                   // tokens of the packed batch (index checks)
+    int num_seqs;
+    unsigned int* status;
 };
 
 // Optional checkpoints of one sequence: the state after ck_pos[c] tokens goes to
@@ -793,13 +802,19 @@ struct Ckpt {
     const int32_t* pos;
     float* states;
     int c, end;
-    __device__ void init(const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states, int seq) {
+    int64_t lim;                 // floats in the checkpoint buffer (index checks)
+    unsigned int* status;
+    __device__ void init(const int32_t* ck_cu, const int32_t* ck_pos, float* ck_states, int seq, int num_seqs,
+                         int H, unsigned int* st) {
         pos = ck_pos;
         states = ck_states;
+        status = st;
         c = end = 0;
+        lim = 0;
         if (ck_states) {
             c = ck_cu[seq];
             end = ck_cu[seq + 1];
+            lim = (int64_t)ck_cu[num_seqs] * H * D * D;
         }
     }
     // called by the whole group after the chunk that ends `done` tokens into the sequence
@@ -808,7 +823,7 @@ struct Ckpt {
             const int64_t p = pos[c];
             if (p > done) break;
             if (p == done && (done % C == 0 || seq_end))
-                store_state(tb, states, ((size_t)c * H + h) * D * D);
+                store_state(tb, states, ((size_t)c * H + h) * D * D, lim, status);
             ++c;
         }
     }
@@ -851,7 +866,8 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
     Small& sw = *x.sw;
     const int t = lt();
     bool ok = true, issued = false;
-    float braw_next = (t < C && x.bos + t < x.eos) ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
+    float braw_next = (t < C && x.bos + t < x.eos && KDA_INDEX_OK((x.bos + t) * x.H + x.h, x.T * x.H, x.status))
+                          ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     KDA_PHASE_INIT;
     for (int n = 0; n < x.nchunks; ++n) {
         const int s = n & 1;
@@ -861,7 +877,8 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         const float braw = braw_next;                    // loaded one chunk ahead
         if (n + 1 < x.nchunks) {
             const int64_t tn = t0 + C + t;
-            braw_next = (t < C && tn < x.eos) ? bf2f(beta[tn * x.H + x.h]) : 0.f;
+            braw_next = (t < C && tn < x.eos && KDA_INDEX_OK(tn * x.H + x.h, x.T * x.H, x.status))
+                            ? bf2f(beta[tn * x.H + x.h]) : 0.f;
         }
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
@@ -1008,7 +1025,8 @@ __device__ __noinline__ bool run_out_issuer(const Ctx& x_in) {
 // Lane pairs swap halves so each store is a 4-byte column pair; a warp store
 // covers two 64-byte row segments.
 __device__ __forceinline__ void o_store_direct(const uint32_t (&opk)[32], __nv_bfloat16* __restrict__ out,
-                                               int64_t t0, int H, int h, int L) {
+                                               int64_t t0, int H, int h, int L, int64_t T, unsigned int* status) {
+    (void)T; (void)status;                    // read by the index checks of bounds-checked builds
     const int t = lt();
     const bool odd = t & 1;
     const int col = t & ~1;
@@ -1020,7 +1038,8 @@ __device__ __forceinline__ void o_store_direct(const uint32_t (&opk)[32], __nv_b
         const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? (mine & 0xffffu) : (mine >> 16), 1);
         const uint32_t word = odd ? (got | (mine & 0xffff0000u)) : ((mine & 0xffffu) | (got << 16));
         const int r = 2 * i + (odd ? 1 : 0);
-        if (r < L) __stcs(reinterpret_cast<unsigned int*>(base + (size_t)r * rs), word);
+        if (r < L && KDA_INDEX_OK(((t0 + r) * H + h) * D + col + 1, T * H * D, status))
+            __stcs(reinterpret_cast<unsigned int*>(base + (size_t)r * rs), word);
     }
 }
 
@@ -1064,7 +1083,7 @@ __device__ __forceinline__ void flush_prev(const Ctx& x, const Maps& maps, __nv_
     if (prev_L == C)
         o_store_warp_tma(opk, x.sm + kWT, maps, prev_t0, x.h);
     else
-        o_store_direct(opk, out, prev_t0, x.H, x.h, prev_L);
+        o_store_direct(opk, out, prev_t0, x.H, x.h, prev_L, x.T, x.status);
 }
 
 // ============================ producer warp ======================================
@@ -1100,7 +1119,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     const Ctx x = x_in;
     Small& sw = *x.sw;
     Ckpt ck;
-    ck.init(ck_cu, ck_pos, ck_states, x.seq);
+    ck.init(ck_cu, ck_pos, ck_states, x.seq, x.num_seqs, x.H, x.status);
     const int t = lt();
     const bool leader = (t == 0);
     uint32_t m1_ph = 0, m2_ph = 0;
@@ -1109,7 +1128,8 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     bool have_prev = false;
     int prev_s = 0, prev_L = 0;
     int64_t prev_t0 = 0;
-    load_state(x.tb, h0, sbase);
+    const int64_t state_lim = (int64_t)x.num_seqs * x.H * D * D;
+    load_state(x.tb, h0, sbase, state_lim, x.status);
     const uint32_t sWT = smem_u32(x.sm + kWT);
     bool ok = true;
     KDA_PHASE_INIT;
@@ -1188,7 +1208,7 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
     }
     if (ok) {
         if (have_prev) flush_prev(x, maps, out, prev_s, prev_t0, prev_L);
-        if (hT) store_state(x.tb, hT, sbase);
+        if (hT) store_state(x.tb, hT, sbase, state_lim, x.status);
     } else if (mma1_pending) {
         mbar_wait_bounded(&sw.mma1_done, m1_ph, kWaitLimitNs);
     }
@@ -1260,6 +1280,9 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     x.h = blockIdx.x % H;
     const int n = blockIdx.x / H;
     x.seq = n;
+    x.T = T;
+    x.num_seqs = num_seqs;
+    x.status = status;
     seq_bounds(cu, n, num_seqs, T, x.bos, x.eos);
     x.nchunks = (int)((x.eos - x.bos + C - 1) / C);
     const size_t sbase = ((size_t)n * H + x.h) * D * D;

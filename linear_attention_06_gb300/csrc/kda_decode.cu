@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
               const float* __restrict__ log_alpha, const Tin* __restrict__ beta,
               float* __restrict__ S, Tin* __restrict__ out, int H, int T,
-              const Tin* __restrict__ gate, const float* __restrict__ norm_w, float norm_eps) {
+              const Tin* __restrict__ gate, const float* __restrict__ norm_w, float norm_eps,
+              unsigned int* status) {
     constexpr int LANES = DV / 4;          // threads per row (float4 each)
     constexpr int RG = kThreads / LANES;   // row groups
     constexpr int RPT = DK / RG;           // rows per thread
@@ -63,9 +64,15 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     float4* Sp = reinterpret_cast<float4*>(S + p * DK * DV);
 
     // Issue the whole state read first so it overlaps the small loads.
+    (void)status;                          // read by the index checks of bounds-checked builds
+    const int64_t n_state4 = (int64_t)gridDim.x * DK * DV / 4;   // float4s of S over all pairs
     float4 s[RPT];
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) s[m] = __ldcs(Sp + (size_t)(g * RPT + m) * LANES + c4);
+    for (int m = 0; m < RPT; ++m) {
+        const int64_t i4 = (int64_t)p * DK * DV / 4 + (int64_t)(g * RPT + m) * LANES + c4;
+        s[m] = KDA_INDEX_OK(i4, n_state4, status) ? __ldcs(Sp + (size_t)(g * RPT + m) * LANES + c4)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 
     // The vectors of all T tokens of this sequence (rows n*T .. n*T+T-1) are staged in
     // shared memory once, next to the state read, so the token loop below waits on no
@@ -84,18 +91,24 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     __shared__ __align__(16) float red_n[DV / 32];
     if (MAXT == 1) T = 1;                   // a compile-time trip count for the single-token step
     const size_t row0 = n * (size_t)T * H + h;         // row of token 0; token t is row0 + t * H
+    const int64_t n_rows = (int64_t)gridDim.x * T;     // rows of q, k, v, out: num_seqs x T x H
     for (int i = threadIdx.x; i < T * DK; i += kThreads) {
         const int tok = i / DK, c = i % DK;
         const size_t e = (row0 + (size_t)tok * H) * DK + c;
-        ks[tok][c] = to_f32(k[e]);
-        qs[tok][c] = to_f32(q[e]);
-        al[tok][c] = expf(log_alpha[e]);
+        const bool ok = KDA_INDEX_OK(e, n_rows * DK, status);
+        ks[tok][c] = ok ? to_f32(k[e]) : 0.f;
+        qs[tok][c] = ok ? to_f32(q[e]) : 0.f;
+        al[tok][c] = ok ? expf(log_alpha[e]) : 1.f;
     }
     for (int i = threadIdx.x; i < T * DV; i += kThreads) {
         const int tok = i / DV, j = i % DV;
-        vs[tok][j] = to_f32(v[(row0 + (size_t)tok * H) * DV + j]);
+        const size_t e = (row0 + (size_t)tok * H) * DV + j;
+        vs[tok][j] = KDA_INDEX_OK(e, n_rows * DV, status) ? to_f32(v[e]) : 0.f;
     }
-    if (threadIdx.x < T) bt[threadIdx.x] = to_f32(beta[row0 + (size_t)threadIdx.x * H]);
+    if (threadIdx.x < T) {
+        const size_t e = row0 + (size_t)threadIdx.x * H;
+        bt[threadIdx.x] = KDA_INDEX_OK(e, n_rows, status) ? to_f32(beta[e]) : 0.f;
+    }
     __syncthreads();
     {                                       // k . q of every token, one warp per token
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -145,7 +158,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
             const float d = bt[tok] * (vs[tok][j] - rj);
             dl[j] = d;
             oj = fmaf(kq[tok], d, yj);
-            if (!gate) store_as(&out[row * DV + j], oj);
+            if (!gate && KDA_INDEX_OK(row * DV + j, n_rows * DV, status)) store_as(&out[row * DV + j], oj);
         }
         if (gate) {   // gated output: RMSNorm over the DV channels (warps 0 .. DV/32-1) x weight x sigmoid(gate)
             float ss = oj * oj;
@@ -158,8 +171,10 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
 #pragma unroll
                 for (int w = 0; w < DV / 32; ++w) tot += red_n[w];
                 const float rn = rsqrtf(tot * (1.f / DV) + norm_eps);
-                const float gv = to_f32(gate[row * DV + j]);
-                store_as(&out[row * DV + j], oj * rn * norm_w[j] / (1.f + __expf(-gv)));
+                if (KDA_INDEX_OK(row * DV + j, n_rows * DV, status)) {
+                    const float gv = to_f32(gate[row * DV + j]);
+                    store_as(&out[row * DV + j], oj * rn * norm_w[j] / (1.f + __expf(-gv)));
+                }
             }
         }
         __syncthreads();
@@ -180,7 +195,9 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
         // thread reaches after this update
     }
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) __stcs(Sp + (size_t)(g * RPT + m) * LANES + c4, s[m]);
+    for (int m = 0; m < RPT; ++m)
+        if (KDA_INDEX_OK((int64_t)p * DK * DV / 4 + (int64_t)(g * RPT + m) * LANES + c4, n_state4, status))
+            __stcs(Sp + (size_t)(g * RPT + m) * LANES + c4, s[m]);
 }
 
 template <int DK, int DV, int MAXT>
@@ -191,13 +208,13 @@ cudaError_t launch_dims_t(const DecodeArgs& a, cudaStream_t st) {
             static_cast<const float*>(a.q), static_cast<const float*>(a.k),
             static_cast<const float*>(a.v), a.log_alpha, static_cast<const float*>(a.beta),
             a.state, static_cast<float*>(a.out), a.H, a.tokens_per_seq, static_cast<const float*>(a.gate),
-            a.norm_w, a.norm_eps);
+            a.norm_w, a.norm_eps, a.status);
     } else {
         decode_kernel<DK, DV, __nv_bfloat16, MAXT><<<blocks, kThreads, 0, st>>>(
             static_cast<const __nv_bfloat16*>(a.q), static_cast<const __nv_bfloat16*>(a.k),
             static_cast<const __nv_bfloat16*>(a.v), a.log_alpha,
             static_cast<const __nv_bfloat16*>(a.beta), a.state, static_cast<__nv_bfloat16*>(a.out), a.H,
-            a.tokens_per_seq, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w, a.norm_eps);
+            a.tokens_per_seq, static_cast<const __nv_bfloat16*>(a.gate), a.norm_w, a.norm_eps, a.status);
     }
     return cudaGetLastError();
 }

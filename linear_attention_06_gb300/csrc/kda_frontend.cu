@@ -207,11 +207,15 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
     const float* __restrict__ conv = which == 0 ? a.conv_q : which == 1 ? a.conv_k : a.conv_v;
     const bool norm = which != 2;
 
+    const int64_t n_elems = a.total_tokens * H * d;      // elements of src and dst
     float wt[W][CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c)
 #pragma unroll
-        for (int i = 0; i < W; ++i) wt[i][c] = conv[((int64_t)h * d + c0 + c) * W + i];
+        for (int i = 0; i < W; ++i) {
+            const int64_t e = ((int64_t)h * d + c0 + c) * W + i;
+            wt[i][c] = KDA_INDEX_OK(e, (int64_t)H * d * W, a.status) ? conv[e] : 0.f;
+        }
 
     int64_t bos, eos;
     seq_of(a, t_begin, bos, eos);
@@ -222,7 +226,8 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
         const int64_t sr = t_begin - (W - 1) + i;
 #pragma unroll
         for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
-        if (W > 1 && sr >= bos) load_row<T, CPL>(src + (sr * H + h) * d + c0, hist[i]);
+        if (W > 1 && sr >= bos && KDA_INDEX_OK((sr * H + h) * d + c0 + CPL - 1, n_elems, a.status))
+            load_row<T, CPL>(src + (sr * H + h) * d + c0, hist[i]);
     }
     uint8_t* mine = &stage[warp][sub][0][ll * kSeg];
     const int64_t rstride = (int64_t)H * d;              // elements from one token's row to the next
@@ -230,7 +235,9 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
     T* dp = dst + (t_begin * H + h) * d + c0;
     for (int64_t ts = t_begin; ts < t_end; ts += kStage) {
         const int n = (int)min((int64_t)kStage, t_end - ts);
-        for (int j = 0; j < n; ++j, sp += rstride) cp_async<kSeg>(mine + j * kRow, sp);
+        for (int j = 0; j < n; ++j, sp += rstride)
+            if (KDA_INDEX_OK(((ts + j) * H + h) * d + c0 + CPL - 1, n_elems, a.status))
+                cp_async<kSeg>(mine + j * kRow, sp);
         cp_async_wait_all();                             // this lane's own copies
 #pragma unroll 4
         for (int j = 0; j < n; ++j, dp += rstride) {
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
             load_row<T, CPL>(reinterpret_cast<const T*>(mine + j * kRow), xr);
             conv_step<CPL, W, sizeof(T) == 2>(xr, hist, wt, y);   // bf16 outputs: the tanh form
             if (norm) l2_normalize<CPL, LPR>(y, a.eps, mask);
-            store_row<T, CPL>(dp, y);
+            if (KDA_INDEX_OK((t * H + h) * d + c0 + CPL - 1, n_elems, a.status)) store_row<T, CPL>(dp, y);
         }
     }
 }
@@ -263,16 +270,18 @@ __global__ void __launch_bounds__(kWarps * 32) gate_kernel(FrontendArgs a) {
     float x[kRowsPerWarp][CPL];
 #pragma unroll
     for (int j = 0; j < kRowsPerWarp; ++j)
-        if (r0 + j < rows) load_row<float, CPL>(a.a_raw + (r0 + j) * a.dk + c0, x[j]);
+        if (r0 + j < rows && KDA_INDEX_OK((r0 + j) * a.dk + c0 + CPL - 1, rows * a.dk, a.status))
+            load_row<float, CPL>(a.a_raw + (r0 + j) * a.dk + c0, x[j]);
 #pragma unroll
     for (int j = 0; j < kRowsPerWarp; ++j) {
         if (r0 + j >= rows) break;
         float y[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) y[c] = logsigmoid(x[j][c]);
-        store_row<float, CPL>(a.log_alpha + (r0 + j) * a.dk + c0, y);
+        if (KDA_INDEX_OK((r0 + j) * a.dk + c0 + CPL - 1, rows * a.dk, a.status))
+            store_row<float, CPL>(a.log_alpha + (r0 + j) * a.dk + c0, y);
     }
-    if (lane < kRowsPerWarp && r0 + lane < rows) {
+    if (lane < kRowsPerWarp && r0 + lane < rows && KDA_INDEX_OK(r0 + lane, rows, a.status)) {
         const T* br = static_cast<const T*>(a.b_raw);
         static_cast<T*>(a.beta)[r0 + lane] = from_f<T>(sigmoid(to_f(br[r0 + lane])));
     }

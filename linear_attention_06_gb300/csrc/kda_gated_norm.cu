@@ -70,7 +70,8 @@ template <> struct Vec<float, 2> {
 template <typename T, int CPL>
 __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* __restrict__ out, const T* __restrict__ gate,
                                                                  const float* __restrict__ w, float eps,
-                                                                 int64_t rows) {
+                                                                 int64_t rows, unsigned int* status) {
+    (void)status;                          // read by the index checks of bounds-checked builds
     constexpr int DV = 32 * CPL;
     const int lane = threadIdx.x & 31;
     const int64_t row0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows;
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* __restrict__
     float x[kRows][CPL], g[kRows][CPL];
 #pragma unroll
     for (int r = 0; r < kRows; ++r) {
-        if (row0 + r < rows) {
+        if (row0 + r < rows && KDA_INDEX_OK((row0 + r) * DV + c0 + CPL - 1, rows * DV, status)) {
             Vec<T, CPL>::ld(out + (row0 + r) * DV + c0, x[r]);
             Vec<T, CPL>::ld(gate + (row0 + r) * DV + c0, g[r]);
         }
@@ -98,26 +99,26 @@ __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* __restrict__
         float y[CPL];
 #pragma unroll
         for (int i = 0; i < CPL; ++i) y[i] = x[r][i] * rr * wv[i] * __fdividef(1.f, 1.f + __expf(-g[r][i]));
-        Vec<T, CPL>::st(out + (row0 + r) * DV + c0, y);
+        if (KDA_INDEX_OK((row0 + r) * DV + c0 + CPL - 1, rows * DV, status)) Vec<T, CPL>::st(out + (row0 + r) * DV + c0, y);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float eps, int64_t rows, int dv,
-                              DType dt, cudaStream_t s) {
+                              DType dt, cudaStream_t s, unsigned int* status) {
     if (rows == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((rows + kWarps * kRows - 1) / (kWarps * kRows));
     if (dt == DType::BF16) {
         auto* o = static_cast<__nv_bfloat16*>(out);
         auto* g = static_cast<const __nv_bfloat16*>(gate);
-        if (dv == 128) gated_norm_kernel<__nv_bfloat16, 4><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows);
-        else gated_norm_kernel<__nv_bfloat16, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows);
+        if (dv == 128) gated_norm_kernel<__nv_bfloat16, 4><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
+        else gated_norm_kernel<__nv_bfloat16, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
     } else {
         auto* o = static_cast<float*>(out);
         auto* g = static_cast<const float*>(gate);
-        if (dv == 128) gated_norm_kernel<float, 4><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows);
-        else gated_norm_kernel<float, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows);
+        if (dv == 128) gated_norm_kernel<float, 4><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
+        else gated_norm_kernel<float, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
     }
     return cudaGetLastError();
 }

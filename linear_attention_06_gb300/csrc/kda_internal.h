@@ -53,10 +53,11 @@ struct DecodeArgs {
     const void* gate = nullptr;   // optional gated output, as in PrefillArgs
     const float* norm_w = nullptr;
     float norm_eps = 0.f;
+    unsigned int* status = nullptr;   // device status word (bounds-checked builds)
 };
 // In-place gated RMSNorm over rows of dv values (after the fp32 recurrent prefill).
 cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float eps, int64_t rows, int dv,
-                              DType dt, cudaStream_t s);
+                              DType dt, cudaStream_t s, unsigned int* status = nullptr);
 
 // Layer front end: projections -> recurrence inputs (see kda_frontend in kda.h).
 struct FrontendArgs {
@@ -80,6 +81,7 @@ struct FrontendArgs {
     int32_t conv_width;           // 1..4
     float eps;                    // L2-norm epsilon
     DType dtype;
+    unsigned int* status = nullptr;   // device status word (bounds-checked builds)
 };
 cudaError_t launch_frontend(const FrontendArgs& a, cudaStream_t s);
 
@@ -96,5 +98,21 @@ constexpr int kMaxDecodeTokens = 16;
 
 // Bits of the device status word.
 constexpr unsigned int kStatusTimeout = 1u;
+constexpr unsigned int kStatusBounds = 2u;    // bounds-checked builds: an index left its buffer
+
+// Index check of a global-memory access computed from indices (not TMA, whose tensor
+// maps bound it in hardware).  In a build with -DKDA_CHECK_BOUNDS an index outside
+// [0, n) sets kStatusBounds in the status word and the access is skipped; otherwise it
+// is always true and compiles away.
+#ifdef KDA_CHECK_BOUNDS
+__device__ __forceinline__ bool index_ok(int64_t i, int64_t n, unsigned int* status) {
+    if (i >= 0 && i < n) return true;
+    if (status) atomicOr(status, kStatusBounds);
+    return false;
+}
+#define KDA_INDEX_OK(i, n, status) ::kda::index_ok((int64_t)(i), (int64_t)(n), (status))
+#else
+#define KDA_INDEX_OK(i, n, status) true
+#endif
 
 }  // namespace kda

@@ -55,7 +55,8 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                          const int32_t* __restrict__ cu, Tin* __restrict__ out,
                          float* __restrict__ hT, int64_t T, int num_seqs, int H, int dv,
                          const int32_t* __restrict__ ck_cu, const int32_t* __restrict__ ck_pos,
-                         float* __restrict__ ck_states) {
+                         float* __restrict__ ck_states, unsigned int* status) {
+    (void)status;                          // read by the index checks of bounds-checked builds
     const int tiles = dv / kCols;
     const int n = blockIdx.x / tiles;
     const int j = (blockIdx.x % tiles) * kCols + threadIdx.x;
@@ -69,8 +70,10 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
 
     float s[DK];
     const size_t sbase = ((size_t)n * H + h) * DK * dv + j;
+    const int64_t n_state = (int64_t)num_seqs * H * DK * dv, n_k = T * H * DK, n_v = T * H * dv;
 #pragma unroll
-    for (int i = 0; i < DK; ++i) s[i] = h0 ? h0[sbase + (size_t)i * dv] : 0.f;
+    for (int i = 0; i < DK; ++i)
+        s[i] = (h0 && KDA_INDEX_OK(sbase + (size_t)i * dv, n_state, status)) ? h0[sbase + (size_t)i * dv] : 0.f;
 
     constexpr int PER = DK / kCols;   // vector elements each thread stages
     auto stage = [&](int64_t t, int buf) {
@@ -78,9 +81,10 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
 #pragma unroll
         for (int m = 0; m < PER; ++m) {
             const int i = threadIdx.x + m * kCols;
-            ks[buf][i] = to_f32(k[base + i]);
-            qs[buf][i] = to_f32(q[base + i]);
-            as[buf][i] = expf(log_alpha[base + i]);
+            const bool ok = KDA_INDEX_OK(base + i, n_k, status);
+            ks[buf][i] = ok ? to_f32(k[base + i]) : 0.f;
+            qs[buf][i] = ok ? to_f32(q[base + i]) : 0.f;
+            as[buf][i] = ok ? expf(log_alpha[base + i]) : 1.f;
         }
     };
     if (bos < eos) stage(bos, 0);
@@ -104,14 +108,15 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
 #pragma unroll
             for (int m = 0; m < PER; ++m) {
                 const int i = threadIdx.x + m * kCols;
-                pk[m] = to_f32(k[base + i]);
-                pq[m] = to_f32(q[base + i]);
-                pa[m] = log_alpha[base + i];
+                const bool ok = KDA_INDEX_OK(base + i, n_k, status);
+                pk[m] = ok ? to_f32(k[base + i]) : 0.f;
+                pq[m] = ok ? to_f32(q[base + i]) : 0.f;
+                pa[m] = ok ? log_alpha[base + i] : 0.f;
             }
         }
         const size_t th = (size_t)t * H + h;
-        const float vj = to_f32(v[th * dv + j]);
-        const float b = to_f32(beta[th]);
+        const float vj = KDA_INDEX_OK(th * dv + j, n_v, status) ? to_f32(v[th * dv + j]) : 0.f;
+        const float b = KDA_INDEX_OK(th, T * H, status) ? to_f32(beta[th]) : 0.f;
 
         float r[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f}, kq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -142,14 +147,16 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
             s[i + 2] = fmaf(k4.z, delta, s[i + 2]);
             s[i + 3] = fmaf(k4.w, delta, s[i + 3]);
         }
-        store_as(&out[th * dv + j], fmaf(kqs, delta, yj));   // read after write
+        if (KDA_INDEX_OK(th * dv + j, n_v, status)) store_as(&out[th * dv + j], fmaf(kqs, delta, yj));   // read after write
         if (ck_next > 0) {
             const int64_t done = t - bos + 1;
             while (ck < ck_end && ck_next <= done) {   // positions not on a chunk end are skipped
                 if (ck_next == done && (done % 64 == 0 || t + 1 == eos)) {
                     const size_t cb = ((size_t)ck * H + h) * DK * dv + j;
+                    const int64_t n_ck = (int64_t)ck_cu[num_seqs] * H * DK * dv;
 #pragma unroll
-                    for (int i = 0; i < DK; ++i) ck_states[cb + (size_t)i * dv] = s[i];
+                    for (int i = 0; i < DK; ++i)
+                        if (KDA_INDEX_OK(cb + (size_t)i * dv, n_ck, status)) ck_states[cb + (size_t)i * dv] = s[i];
                 }
                 ++ck;
                 ck_next = (ck < ck_end) ? ck_pos[ck] : -1;
@@ -171,7 +178,8 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
     }
     if (hT) {
 #pragma unroll
-        for (int i = 0; i < DK; ++i) hT[sbase + (size_t)i * dv] = s[i];
+        for (int i = 0; i < DK; ++i)
+            if (KDA_INDEX_OK(sbase + (size_t)i * dv, n_state, status)) hT[sbase + (size_t)i * dv] = s[i];
     }
 }
 
@@ -183,7 +191,7 @@ cudaError_t launch_typed(const PrefillArgs& a, cudaStream_t st) {
         static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
         a.log_alpha, static_cast<const Tin*>(a.beta), a.initial_state, a.cu_seqlens,
         static_cast<Tin*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.dv, a.ckpt_cu,
-        a.ckpt_pos, a.ckpt_states);
+        a.ckpt_pos, a.ckpt_states, a.status);
     return cudaGetLastError();
 }
 

@@ -42,6 +42,7 @@ def test_exports_every_declared_symbol(L):
 def test_status_strings_and_version(L):
     assert _lib.status_string(0) == "KDA_OK"
     assert _lib.status_string(4) == "KDA_ERR_TIMEOUT"
+    assert _lib.status_string(5) == "KDA_ERR_BOUNDS"
     assert _lib.status_string(99) == "KDA_ERR_UNKNOWN"
     assert "sm_103a" in _lib.version()
 
