@@ -24,7 +24,8 @@
  * - All tensor arguments are DEVICE pointers to row-major, contiguous memory
  *   owned by the caller.  The library allocates no memory and keeps no state
  *   between calls, except one device status word used to report a timed-out
- *   wait inside a kernel (see kda_device_status).
+ *   wait inside a kernel, and, in bounds-checked diagnostic builds, an index
+ *   that left its buffer (see kda_device_status).
  * - Layouts (T = shape->total_tokens, N = shape->num_seqs):
  *     q, k       [T, H, dk]   dtype
  *     v, out     [T, H, dv]   dtype
