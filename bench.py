@@ -382,6 +382,38 @@ def run_ours(args):
             layer["multi"][tm] = timed(lambda: kda.kda_decode_step(mw.q, mw.k, mw.v, mw.log_alpha, mw.beta,
                                                                    ms_state, m_out, stream=stream))
             del mw, ms_state, m_out
+
+        # the other prefill workloads: one 131072-token sequence (whole, and resumed from the
+        # state after its first half), and 64 log-uniform lengths packed with per-sequence
+        # initial states (load imbalance: the longest sequence sets the time)
+        lw = workloads.long_prefill(device=dev, seed=3 + rank)
+        Tl = lw.q.shape[0]
+        l_out = torch.empty_like(lw.v)
+        l_fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+        half = Tl // 2
+        l_mid = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+        layer["t_long"] = timed(lambda: kda.kda_prefill(lw.q, lw.k, lw.v, lw.log_alpha, lw.beta, None, None,
+                                                        l_out, l_fin, num_seqs=1, stream=stream))
+
+        def resume_step():
+            kda.kda_prefill(lw.q[:half], lw.k[:half], lw.v[:half], lw.log_alpha[:half], lw.beta[:half], None,
+                            None, l_out[:half], l_mid, num_seqs=1, stream=stream)
+            kda.kda_prefill(lw.q[half:], lw.k[half:], lw.v[half:], lw.log_alpha[half:], lw.beta[half:], l_mid,
+                            None, l_out[half:], l_fin, num_seqs=1, stream=stream)
+
+        layer["t_resume"] = timed(resume_step)
+        layer["long_tokens"] = Tl
+        del lw, l_out
+        vw = workloads.varlen_prefill(device=dev, seed=4 + rank)
+        v_cu = vw.cu_seqlens.to(dev)
+        v_out = torch.empty_like(vw.v)
+        v_fin = torch.empty_like(vw.initial_state)
+        layer["t_varlen"] = timed(lambda: kda.kda_prefill(vw.q, vw.k, vw.v, vw.log_alpha, vw.beta, vw.initial_state,
+                                                          v_cu, v_out, v_fin, stream=stream))
+        layer["varlen_tokens"] = vw.q.shape[0]
+        layer["varlen_seqs"] = v_cu.numel() - 1
+        layer["varlen_longest"] = int((v_cu[1:] - v_cu[:-1]).max().item())
+        del vw, v_out, v_fin
     clocks = sampler.stop()
 
     # ---- end to end through the public API with host buffers (pinned).  Every step copies
@@ -493,6 +525,25 @@ def run_ours(args):
                              "algorithmic_bytes_per_launch": dgbytes, "kernels": ["decode_kernel (gate and norm in its store)"]},
         }
         ckbytes = pbytes + layer["n_ck"] * H * D * D * 4        # + every checkpoint state written once
+        lt, nv = layer["long_tokens"], layer["varlen_seqs"]
+        lbytes = prefill_bytes(lt, H, 1)
+        vbytes = prefill_bytes(layer["varlen_tokens"], H, nv, with_h0=True)
+        line["other_prefill_configs"] = {
+            "long_prefill": {"workload": f"kda_prefill_bf16_B1_H{H}_T{lt}_d{D}", "ms_per_step": layer["t_long"] * 1e3,
+                             "value": world * lt / layer["t_long"], "unit": UNIT,
+                             "achieved_gbs": lbytes / layer["t_long"] / 1e9,
+                             "frac": lbytes / layer["t_long"] / 1e9 / hbm, "algorithmic_bytes_per_launch": lbytes,
+                             "note": f"{H} blocks (one per head) on {lt // 64} chunks each: one block per SM"},
+            "long_prefill_resumed": {"workload": f"kda_prefill_bf16_B1_H{H}_T{lt}_d{D}_resume_at_{lt // 2}",
+                                     "ms_per_step": layer["t_resume"] * 1e3,
+                                     "value": world * lt / layer["t_resume"], "unit": UNIT,
+                                     "note": "two calls: the first half, then the second half from its final state"},
+            "varlen": {"workload": f"kda_prefill_bf16_varlen_N{nv}_H{H}_d{D}", "tokens": layer["varlen_tokens"],
+                       "longest_sequence": layer["varlen_longest"], "ms_per_step": layer["t_varlen"] * 1e3,
+                       "value": world * layer["varlen_tokens"] / layer["t_varlen"], "unit": UNIT,
+                       "achieved_gbs": vbytes / layer["t_varlen"] / 1e9,
+                       "frac": vbytes / layer["t_varlen"] / 1e9 / hbm, "algorithmic_bytes_per_launch": vbytes},
+        }
         line["next"] = {
             "prefill_checkpointed": {"workload": WORKLOAD + f"_ckpt{CKPT_EVERY}", "checkpoints": layer["n_ck"],
                                      "ms_per_step": layer["t_ck"] * 1e3, "value": world * B * T / layer["t_ck"],
