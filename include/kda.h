@@ -146,7 +146,8 @@ kda_status kda_prefill_checkpointed(const kda_shape* shape, const void* q, const
  * (an RMSNorm over the dv value channels with one weight per channel shared by
  * the heads -- the figure says only "a norm"; this is the reading).
  * gate:        [T, H, dv] in dtype, the gate logits, 16-byte aligned.
- * norm_weight: [dv] fp32.   norm_eps: finite, >= 0.
+ * norm_weight: [dv] fp32.   norm_eps: finite and > 0 (an all-zero output row, which
+ *              beta = 0 from a zero state produces, is then mapped to zero, not 0/0).
  * All other arguments are those of kda_prefill; final_state is unchanged by the
  * gate.  The gate is applied by a second, memory-bound pass over out on the same
  * stream (one read of o and of the gate, one write).
@@ -210,7 +211,8 @@ kda_status kda_decode_step(const kda_shape* shape, const void* q, const void* k,
  * q_raw, k_raw, a_raw [T, H, dk]; v_raw [T, H, dv]; b_raw [T, H].
  * conv_q, conv_k [H, dk, W], conv_v [H, dv, W]: fp32 taps, tap W-1 on the current
  *            token; 1 <= W <= 4.
- * eps:       added to the sum of squares of the L2 norm, finite and >= 0.
+ * eps:       added to the sum of squares of the L2 norm, finite and > 0 (so an
+ *            all-zero row normalises to zero instead of 0/0).
  * q, k, v, log_alpha, beta: written in kda_prefill's input layout; they must not
  *            overlap the raw inputs.
  * cu_seqlens: as kda_prefill (NULL: N equal sequences).
@@ -228,7 +230,7 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps,
 /*
  * kda_decode_step_gated -- kda_decode_step whose stored output is the gated
  * output of kda_prefill_gated (gate [N*T, H, dv] in dtype, norm_weight [dv]
- * fp32, norm_eps >= 0), fused into the step's output store.  The state update
+ * fp32, norm_eps finite and > 0), fused into the step's output store.  The state update
  * is that of kda_decode_step.  Errors: those of kda_decode_step and of the gate
  * arguments of kda_prefill_gated.
  */
@@ -258,8 +260,12 @@ kda_status kda_check_cu_seqlens(const int32_t* host_cu_seqlens, int32_t num_seqs
 kda_status kda_selftest_timeout(uint64_t limit_ns, kda_stream_t stream);
 
 /*
- * kda_device_status -- synchronise `stream`, then read and clear the device
- * status word.  Returns KDA_ERR_TIMEOUT if a kernel's bounded wait gave up
+ * kda_device_status -- synchronise `stream`, then read the device status word
+ * and clear the bits that were read (an atomic clear on `stream`, so a bit set
+ * meanwhile by a kernel on another stream survives for the next call).  The
+ * word is one per device, shared by every stream and every call of the
+ * library: a bit reports an event since it was last read, whichever stream's
+ * kernel caused it.  Returns KDA_ERR_TIMEOUT if a kernel's bounded wait gave up
  * since the last call (that kernel's outputs are then undefined), KDA_ERR_BOUNDS
  * if, in a library built with -DKDA_CHECK_BOUNDS (a diagnostic build), a kernel
  * skipped a global-memory access whose index left its buffer, KDA_OK otherwise,

@@ -50,6 +50,12 @@ __global__ void selftest_timeout_kernel(unsigned int* status, uint64_t limit_ns)
     }
 }
 
+// Clears the given bits of the status word and nothing else: a bit that a kernel on
+// another stream sets between the host's read and this clear is kept for the next read.
+__global__ void status_clear_kernel(unsigned int* status, unsigned int bits) {
+    atomicAnd(status, ~bits);
+}
+
 bool env_flag(const char* name) {
     const char* v = getenv(name);
     return v && v[0] && strcmp(v, "0") != 0;
@@ -77,10 +83,11 @@ kda_status check_tensor_ptrs(const kda_shape* s, const void* q, const void* k, c
     return KDA_OK;
 }
 
-// Gated-output arguments: gate [T, H, dv] like out, weight [dv] fp32, eps finite and >= 0.
+// Gated-output arguments: gate [T, H, dv] like out, weight [dv] fp32, eps finite and > 0
+// (a zero eps would turn an all-zero output row into 0 / 0).
 kda_status check_gate(const kda_shape* s, const void* gate, const float* norm_w, float eps) {
     if (!gate || !norm_w) return KDA_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
     if (!aligned(gate, 16) || !aligned(norm_w, 4)) return KDA_ERR_UNSUPPORTED;
     (void)s;
     return KDA_OK;
@@ -260,7 +267,7 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, c
         return KDA_ERR_INVALID_ARG;
     if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_UNSUPPORTED;
     if (conv_width < 1 || conv_width > 4) return KDA_ERR_UNSUPPORTED;
-    if (!(eps >= 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;   // an all-zero row needs eps > 0
     if (shape->total_tokens == 0) return KDA_OK;
     // the raw inputs and the outputs follow kda_prefill's pointer rules
     st = check_tensor_ptrs(shape, q_raw, k_raw, v_raw, a_raw, b_raw, q);
@@ -296,9 +303,9 @@ kda_status kda_device_status(kda_stream_t stream) {
     unsigned int word = 0;
     if (cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (word) {
-        const unsigned int zero = 0;
-        if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    if (word) {                       // clear exactly the bits that were read, atomically
+        status_clear_kernel<<<1, 1, 0, s>>>(p, word);
+        if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
             return KDA_ERR_CUDA;
     }
     if (word & kda::kStatusTimeout) return KDA_ERR_TIMEOUT;

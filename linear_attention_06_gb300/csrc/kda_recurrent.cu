@@ -148,7 +148,7 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
             s[i + 3] = fmaf(k4.w, delta, s[i + 3]);
         }
         if (KDA_INDEX_OK(th * dv + j, n_v, status)) store_as(&out[th * dv + j], fmaf(kqs, delta, yj));   // read after write
-        if (ck_next > 0) {
+        if (ck < ck_end) {                       // positions <= 0 are passed over like any other bad one
             const int64_t done = t - bos + 1;
             while (ck < ck_end && ck_next <= done) {   // positions not on a chunk end are skipped
                 if (ck_next == done && (done % 64 == 0 || t + 1 == eos)) {

@@ -11,7 +11,7 @@ are plain GEMMs outside this library.  This module restates, in plain numpy
 fp64, the steps between the projections and the recurrence (``frontend``) and
 the step after it (``gated_rmsnorm``).
 
-Readings where the figure is silent (each also listed in the design notes):
+Readings where the figure is silent:
 - the short convolution is depthwise and causal over the tokens of one
   sequence, width W (the figure gives no width; the library takes W <= 4),
   with zero history before the sequence start and no bias:

@@ -158,8 +158,8 @@ def frontend_call(L, sh, W=4, eps=1e-6, ptrs=None, conv=FAKE):
                           P(conv), P(conv), P(conv), None, P(p), P(p), P(p), P(p), P(p), None)
 
 
-@pytest.mark.parametrize("W,eps,code", [(0, 1e-6, 2), (5, 1e-6, 2), (4, -1.0, 1), (4, float("nan"), 1),
-                                        (4, float("inf"), 1)])
+@pytest.mark.parametrize("W,eps,code", [(0, 1e-6, 2), (5, 1e-6, 2), (4, -1.0, 1), (4, 0.0, 1),
+                                        (4, float("nan"), 1), (4, float("inf"), 1)])
 def test_frontend_rejects_width_and_eps(L, W, eps, code):
     assert frontend_call(L, shape(), W=W, eps=eps) == code
 
@@ -182,6 +182,7 @@ def test_gated_prefill_rejects_gate_arguments(L):
     assert gated_prefill_call(L, shape(), gate=0) == 1
     assert gated_prefill_call(L, shape(), w=0) == 1
     assert gated_prefill_call(L, shape(), eps=-1.0) == 1
+    assert gated_prefill_call(L, shape(), eps=0.0) == 1             # 0/0 on an all-zero row
     assert gated_prefill_call(L, shape(), eps=float("nan")) == 1
     assert gated_prefill_call(L, shape(), gate=FAKE_MIS) == 2
     assert gated_prefill_call(L, shape(n=0, T=0), gate=0) == 0      # empty: nothing checked, nothing enqueued
@@ -195,4 +196,5 @@ def test_gated_decode_rejects_gate_arguments(L):
     assert call(0, FAKE, 1e-6) == 1
     assert call(FAKE, 0, 1e-6) == 1
     assert call(FAKE, FAKE, -2.0) == 1
+    assert call(FAKE, FAKE, 0.0) == 1
     assert call(FAKE_MIS, FAKE, 1e-6) == 2

@@ -166,3 +166,34 @@ def test_decode_gated(T):
     ref = lo.gated_rmsnorm(ro, np64(x.g_raw), np64(x.norm_weight), 1e-6)
     assert rel_l2(np64(out), ref) <= 5e-3
     assert rel_l2(np64(S), rf) <= 5e-3
+
+
+@pytest.mark.parametrize("impl", ["tensor_core", "recurrent"])
+def test_prefill_gated_all_zero_rows_stay_finite(impl, monkeypatch):
+    # beta = 0 from a zero state leaves S = 0, so every output row is exactly zero; the gated
+    # output must then be zero (eps > 0 is required), never 0/0
+    if impl == "recurrent":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "recurrent")
+    cu = [0, 70, 200]
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, dtype=torch.bfloat16, seed=68, cu_seqlens=cu)
+    w.beta.zero_()
+    x = workloads.make_layer_inputs(cu[-1], 2, 128, 128, dtype=torch.bfloat16, seed=69, cu_seqlens=cu)
+    out, fin, _ = run_gated(w, x, eps=1e-6)
+    assert torch.isfinite(out.float()).all()
+    assert torch.count_nonzero(out) == 0 and torch.count_nonzero(fin) == 0
+    ro, _ = gated_ref(w, x, eps=1e-6)
+    assert np.all(ro == 0.0)
+
+
+def test_decode_gated_all_zero_rows_stay_finite():
+    n, T = 4, 3
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, 2, 128, 128, dtype=torch.bfloat16, seed=70, cu_seqlens=cu)
+    x = workloads.make_layer_inputs(n * T, 2, 128, 128, dtype=torch.bfloat16, seed=71, cu_seqlens=cu)
+    d = w.to(DEV)
+    d.beta.zero_()
+    S = torch.zeros((n, 2, 128, 128), dtype=torch.float32, device=DEV)
+    out = kda.kda_decode_step_gated(d.q, d.k, d.v, d.log_alpha, d.beta, x.g_raw.to(DEV), x.norm_weight.to(DEV),
+                                    S, norm_eps=1e-6)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.count_nonzero(out) == 0

@@ -267,8 +267,29 @@ def test_decode_multi_token_equals_repeated_single_steps():
 
 
 # ---- checkpoint emission during prefill ---------------------------------------------
+def oracle_checkpoints(w, ck, heads=None):
+    """fp64 oracle state after each checkpoint position: each sequence is run as a chain of
+    oracle prefills over the segments between its positions, every segment starting from the
+    previous one's final state (the resume property the oracle is pinned to)."""
+    sel = slice(None) if heads is None else list(heads)
+    cu = [int(x) for x in w.cu_seqlens]
+    pick = lambda t, s, e: np64(t[s:e, sel])          # noqa: E731
+    states = []
+    for n, positions in enumerate(ck):
+        S = None if w.initial_state is None else np64(w.initial_state[n:n + 1, sel])
+        done = 0
+        for p in positions:
+            s, e = cu[n] + done, cu[n] + p
+            _, S = kda_oracle.prefill(pick(w.q, s, e), pick(w.k, s, e), pick(w.v, s, e),
+                                      pick(w.log_alpha, s, e), pick(w.beta, s, e), S,
+                                      cu_seqlens=[0, e - s])
+            states.append(S[0])
+            done = p
+    return np.stack(states)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_checkpoints_equal_prefix_final_states(dtype):
+def test_checkpoints_match_oracle_and_prefix_runs(dtype):
     lens = [200, 64, 300, 30]
     cu = workloads.cu_from_lengths(lens)
     ck = [[64, 128, 200], [64], [192, 256, 300], [30]]
@@ -276,8 +297,18 @@ def test_checkpoints_equal_prefix_final_states(dtype):
                               state_std=0.05).to(DEV)
     out, fin, cks = kda.kda_prefill_checkpointed(w.q, w.k, w.v, w.log_alpha, w.beta, ck,
                                                  w.initial_state, cu, final_state=True)
+    torch.cuda.synchronize()
+    # every checkpoint against the fp64 oracle's state at that position
+    ref = oracle_checkpoints(w, ck)
+    assert rel_l2(np64(cks), ref) <= TOL[dtype]
+    for c in range(ref.shape[0]):                      # and each one on its own
+        assert rel_l2(np64(cks[c]), ref[c]) <= TOL[dtype], c
+    ro, rf = oracle_prefill(w)
+    assert rel_l2(np64(out), ro) <= TOL[dtype] and rel_l2(np64(fin), rf) <= TOL[dtype]
+    # the same call without checkpoints gives the same out and final state, bit for bit
     ref_out, ref_fin = gpu_prefill(w)
     assert torch.equal(out, ref_out) and torch.equal(fin, ref_fin)
+    # and a checkpoint equals the final state of a prefill over the same prefix
     c = 0
     for n, positions in enumerate(ck):
         for p in positions:
@@ -287,6 +318,55 @@ def test_checkpoints_equal_prefix_final_states(dtype):
             torch.cuda.synchronize()
             assert torch.equal(cks[c], f[0]), (n, p)
             c += 1
+
+
+def test_checkpoints_full_size_sampled_heads():
+    # the benchmark prefill (4 x 8192 tokens, 32 heads) saving every sequence's state each
+    # 1024 tokens; sampled heads against the oracle's chained segments
+    w = workloads.prefill_bf16(device=DEV)
+    B, T = 4, 8192
+    ck = [list(range(1024, T + 1, 1024)) for _ in range(B)]
+    out, fin, cks = kda.kda_prefill_checkpointed(w.q, w.k, w.v, w.log_alpha, w.beta, ck, None,
+                                                 w.cu_seqlens, final_state=True)
+    torch.cuda.synchronize()
+    heads = [0, 31]
+    ref = oracle_checkpoints(w, ck, heads)
+    got = np64(cks[:, heads])
+    assert rel_l2(got, ref) <= 5e-3
+    for c in range(ref.shape[0]):
+        assert rel_l2(got[c], ref[c]) <= 5e-3, c
+    ro, rf = oracle_prefill(w, heads)
+    assert rel_l2(np64(out[:, heads]), ro) <= 5e-3 and rel_l2(np64(fin[:, heads]), rf) <= 5e-3
+
+
+@pytest.mark.parametrize("impl", ["tensor_core", "recurrent"])
+def test_checkpoint_nonpositive_positions_do_not_drop_later_ones(impl, monkeypatch):
+    # Straight through the C ABI (no host validation): a position <= 0 is skipped like any
+    # other bad position, and the valid checkpoints after it are still written.
+    import ctypes
+    from linear_attention_06_gb300 import _lib
+    if impl == "recurrent":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "recurrent")
+    lens = [256, 192]
+    cu = workloads.cu_from_lengths(lens)
+    w = workloads.make_inputs(cu[-1], 2, 128, 128, seed=52, cu_seqlens=cu, state_std=0.05).to(DEV)
+    ck = [[0, 64, 192], [-5, 128]]
+    d_cu = torch.tensor(cu, dtype=torch.int32, device=DEV)
+    ck_cu = torch.tensor([0, 3, 5], dtype=torch.int32, device=DEV)
+    ck_pos = torch.tensor([p for ps in ck for p in ps], dtype=torch.int32, device=DEV)
+    cks = torch.full((5, 2, 128, 128), float("nan"), device=DEV)
+    out = torch.empty_like(w.v)
+    shape = _lib.KdaShape(2, cu[-1], 2, 128, 128, _lib.KDA_BF16)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = _lib.lib().kda_prefill_checkpointed(ctypes.byref(shape), p(w.q), p(w.k), p(w.v), p(w.log_alpha),
+                                             p(w.beta), p(w.initial_state), p(d_cu), p(out), None, p(ck_cu),
+                                             p(ck_pos), p(cks), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0
+    assert torch.isnan(cks[0]).all() and torch.isnan(cks[3]).all()      # the bad positions
+    ref = oracle_checkpoints(w, [[64, 192], [128]])
+    for got, r in zip((cks[1], cks[2], cks[4]), ref):
+        assert rel_l2(np64(got), r) <= 5e-3
 
 
 def test_checkpoint_positions_off_chunk_ends_are_not_written():
