@@ -549,9 +549,17 @@ __device__ void decay_state(uint32_t tb, const float* gam) {
     tmem_wait_st();
 }
 
+// The warp's 4 KB of the W / staging area may still be read by its last output TMA store:
+// wait for that read (lane 0 issued it) before the area is written again.
+__device__ __forceinline__ void staging_ready() {
+    if ((threadIdx.x & 31) == 0) bulk_wait_read();
+    __syncwarp();
+}
+
 // Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
 __device__ void read_w(uint32_t tb, uint32_t col, uint8_t* wt) {
     const int c = lt();
+    staging_ready();
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
         uint32_t v[32];
@@ -631,44 +639,54 @@ __device__ void store_state(uint32_t tb, float* hT, size_t base, int64_t lim, un
 // write).  log_alpha in the A slot is first turned into alpha in place.
 // The outputs o_r go to TMEM column ucol + r of the thread's lane (its value
 // channel), where the chunk's output is stored from like any other chunk's.
+// The row stays in TMEM and is walked 32 columns at a time (two passes per
+// token: decay and the read under k, then the write and the read with q), so the
+// path needs few registers; it is rare (only chunks with |G| > kMaxExponent).
 __device__ __noinline__ void token_chunk(uint32_t tb, float* A, const uint8_t* qk, const uint8_t* vv,
-                            const __nv_bfloat16* beta, uint32_t ucol, int L) {
+                                            const __nv_bfloat16* beta, uint32_t ucol, int L) {
     const int j = lt();
+#pragma unroll 1
     for (int r = 0; r < L; ++r) A[r * D + j] = expf(A[r * D + j]);
     group_sync(kBarB);
-    float s[D];
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * cb + i] = __uint_as_float(u[i]);
-    }
+#pragma unroll 1
     for (int r = 0; r < L; ++r) {
         const float* al = A + r * D;
         float rk = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {              // decay, and what S holds under k
+            uint32_t u[32];
+            tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < D; ++c) {
-            s[c] *= al[c];
-            rk = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), rk);
+            for (int i = 0; i < 32; ++i) {
+                const int c = 32 * cb + i;
+                const float sc = __uint_as_float(u[i]) * al[c];
+                u[i] = __float_as_uint(sc);
+                rk = fmaf(sc, bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), rk);
+            }
+            tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+            tmem_wait_st();
         }
         const float vj = bf2f(*reinterpret_cast<const __nv_bfloat16*>(vv + half_off(r, j)));
         const float d = bf2f(beta[r]) * (vj - rk);
         float y = 0.f;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {              // erase and write with the same beta, read with q
+            uint32_t u[32];
+            tmem_ld32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < D; ++c) {
-            s[c] = fmaf(bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), d, s[c]);
-            y = fmaf(s[c], bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(true, r, c))), y);
+            for (int i = 0; i < 32; ++i) {
+                const int c = 32 * cb + i;
+                const float sc = fmaf(bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(false, r, c))), d,
+                                      __uint_as_float(u[i]));
+                u[i] = __float_as_uint(sc);
+                y = fmaf(sc, bf2f(*reinterpret_cast<const __nv_bfloat16*>(qk + qk_off(true, r, c))), y);
+            }
+            tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
+            tmem_wait_st();
         }
         tmem_st1(tmem_addr(tb, lane0(), ucol + r), __float_as_uint(y));
-    }
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-        uint32_t u[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(s[32 * cb + i]);
-        tmem_st32(tmem_addr(tb, lane0(), kTmS + 32 * cb), u);
     }
     tmem_wait_st();
 }
@@ -1053,6 +1071,7 @@ __device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint
     const bool odd = t & 1;
     uint8_t* stg = stg_all + wq * 4096;
     const uint32_t cb = (uint32_t)(lane & ~1) * 2;
+    staging_ready();
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const uint32_t mine = opk[i];
@@ -1066,9 +1085,7 @@ __device__ __forceinline__ void o_store_warp_tma(const uint32_t (&opk)[32], uint
     if (lane == 0) {
         tma_store_3d(&maps.o, 32 * wq, h, (int)t0, stg);
         bulk_commit();
-        bulk_wait_read();
     }
-    __syncwarp();
 }
 
 // Store the output a chunk left in its U slot, then release that U slot to
