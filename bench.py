@@ -402,8 +402,15 @@ def run_ours(args):
                             None, l_out[half:], l_fin, num_seqs=1, stream=stream)
 
         layer["t_resume"] = timed(resume_step)
+        # the same sequence through the split prefill (chunk-local kernel over all chunks of all
+        # heads, then the state chain per head); its workspace is allocated once, outside the timing
+        l_ws = torch.empty(kda.kda_prefill_split_workspace_size(Tl, 1, H), dtype=torch.uint8, device=dev)
+        layer["t_long_split"] = timed(lambda: kda.kda_prefill_split(lw.q, lw.k, lw.v, lw.log_alpha, lw.beta, None,
+                                                                    None, l_out, l_fin, num_seqs=1, workspace=l_ws,
+                                                                    stream=stream))
+        layer["long_split_ws"] = l_ws.numel()
         layer["long_tokens"] = Tl
-        del lw, l_out
+        del lw, l_out, l_ws
         vw = workloads.varlen_prefill(device=dev, seed=4 + rank)
         v_cu = vw.cu_seqlens.to(dev)
         v_out = torch.empty_like(vw.v)
@@ -534,6 +541,17 @@ def run_ours(args):
                              "achieved_gbs": lbytes / layer["t_long"] / 1e9,
                              "frac": lbytes / layer["t_long"] / 1e9 / hbm, "algorithmic_bytes_per_launch": lbytes,
                              "note": f"{H} blocks (one per head) on {lt // 64} chunks each: one block per SM"},
+            "long_prefill_split": {"workload": f"kda_prefill_bf16_B1_H{H}_T{lt}_d{D}_split",
+                                   "ms_per_step": layer["t_long_split"] * 1e3,
+                                   "value": world * lt / layer["t_long_split"], "unit": UNIT,
+                                   "achieved_gbs": lbytes / layer["t_long_split"] / 1e9,
+                                   "frac": lbytes / layer["t_long_split"] / 1e9 / hbm,
+                                   "algorithmic_bytes_per_launch": lbytes,
+                                   "workspace_bytes": layer["long_split_ws"],
+                                   "kernels": ["chunk_local_kernel", "chunk_chain_kernel"],
+                                   "note": "kda_prefill_split: per-chunk records of every head first (all SMs), "
+                                           "then one state chain per head; bytes counted as for the fused kernel "
+                                           "(the records' round trip through HBM is not in the algorithmic bytes)"},
             "long_prefill_resumed": {"workload": f"kda_prefill_bf16_B1_H{H}_T{lt}_d{D}_resume_at_{lt // 2}",
                                      "ms_per_step": layer["t_resume"] * 1e3,
                                      "value": world * lt / layer["t_resume"], "unit": UNIT,

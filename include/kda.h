@@ -50,6 +50,7 @@
 #ifndef KDA_H_
 #define KDA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -159,6 +160,41 @@ kda_status kda_prefill_gated(const kda_shape* shape, const void* q, const void* 
                              const float* initial_state, const int32_t* cu_seqlens,
                              const void* gate, const float* norm_weight, float norm_eps,
                              void* out, float* final_state, kda_stream_t stream);
+
+/*
+ * kda_prefill_split -- kda_prefill for inputs with few (sequence, head) pairs and
+ * long sequences (the 1M-token contexts of "Kimi K3 Architecture Teardown", section
+ * "Hybrid Attention for 1M Tokens").  kda_prefill runs each (sequence, head) on one
+ * SM, so one sequence with 32 heads keeps 32 SMs busy whatever its length.  Here the
+ * work that does not depend on the state entering a chunk (the decayed factors, the
+ * Gram products, the UT solve and the WY factors W' and U) first runs for every chunk
+ * of every head at once, leaving one record per chunk in `workspace`; a second kernel
+ * per (sequence, head) then carries the state through the records in order.
+ *
+ * All arguments but the workspace are those of kda_prefill, with the same results
+ * (the same arithmetic in a different order of kernels; within the tolerances of the
+ * tensor-core path).  workspace: DEVICE memory of at least
+ * kda_prefill_split_workspace_size bytes, 256-byte aligned, owned by the caller,
+ * overwritten by the call and free again once the call's work on `stream` is done;
+ * two calls in flight at once need two workspaces.  For shapes the split kernels do
+ * not take (anything but bf16 with dk = dv = 128) the call runs kda_prefill's kernels
+ * and leaves the workspace untouched.
+ * Errors: those of kda_prefill, plus KDA_ERR_INVALID_ARG for a NULL or too small
+ * workspace and KDA_ERR_UNSUPPORTED for a misaligned one.
+ */
+kda_status kda_prefill_split(const kda_shape* shape, const void* q, const void* k, const void* v,
+                             const float* log_alpha, const void* beta, const float* initial_state,
+                             const int32_t* cu_seqlens, void* out, float* final_state, void* workspace,
+                             size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_prefill_split_workspace_size -- bytes of workspace kda_prefill_split needs for
+ * `shape`: H * (ceil(T / 64) + N) chunk records of 96 KB plus a 4-byte mode word each
+ * (about 1.5 KB per token and head).  Depends on the shape only, not on the sequence
+ * lengths.  Writes *bytes; KDA_ERR_INVALID_ARG for a NULL pointer, otherwise the shape
+ * errors of kda_prefill.  No CUDA call.
+ */
+kda_status kda_prefill_split_workspace_size(const kda_shape* shape, size_t* bytes);
 
 /*
  * kda_check_checkpoints -- validate HOST copies of a cu_seqlens table and of a

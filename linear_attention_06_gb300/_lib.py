@@ -64,6 +64,10 @@ def lib():
         L.kda_decode_step_gated.restype = ctypes.c_int
         L.kda_frontend.argtypes = [sp, ctypes.c_int32, ctypes.c_float] + [vp] * 15
         L.kda_frontend.restype = ctypes.c_int
+        L.kda_prefill_split.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.kda_prefill_split.restype = ctypes.c_int
+        L.kda_prefill_split_workspace_size.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
+        L.kda_prefill_split_workspace_size.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_version.argtypes = []
@@ -147,6 +151,46 @@ def kda_prefill(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None, o
                            _ptr(beta), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
                            _ptr(final_state), _stream(stream))
     _check("kda_prefill", st)
+    return out, final_state
+
+
+def kda_prefill_split_workspace_size(total_tokens: int, num_seqs: int, H: int, dk: int = 128, dv: int = 128,
+                                     dtype=torch.bfloat16) -> int:
+    """Bytes of workspace kda_prefill_split needs for this shape (see ``include/kda.h``)."""
+    shape = KdaShape(int(num_seqs), int(total_tokens), int(H), int(dk), int(dv),
+                     KDA_BF16 if dtype == torch.bfloat16 else KDA_F32)
+    n = ctypes.c_size_t(0)
+    _check("kda_prefill_split_workspace_size", lib().kda_prefill_split_workspace_size(ctypes.byref(shape),
+                                                                                      ctypes.byref(n)))
+    return int(n.value)
+
+
+def kda_prefill_split(q, k, v, log_alpha, beta, initial_state=None, cu_seqlens=None, out=None,
+                      final_state=None, num_seqs=None, workspace=None, stream=None):
+    """kda_prefill for few (sequence, head) pairs and long sequences: a chunk-local
+    kernel over every chunk of every head, then a state-chain kernel per (sequence,
+    head) (see ``include/kda.h``).  ``workspace`` is a CUDA uint8 tensor of at least
+    kda_prefill_split_workspace_size bytes, allocated here when not given.  Returns
+    (out, final_state)."""
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is not None and not (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda):
+        host_cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+        kda_check_cu_seqlens(host_cu, T)
+        cu_seqlens = host_cu.to(q.device)
+    n = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is True:
+        final_state = torch.empty((n, H, dk, dv), dtype=torch.float32, device=q.device)
+    shape = KdaShape(n, T, H, dk, dv, _dtype_code(q))
+    need = kda_prefill_split_workspace_size(T, n, H, dk, dv, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib().kda_prefill_split(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("kda_prefill_split", st)
     return out, final_state
 
 

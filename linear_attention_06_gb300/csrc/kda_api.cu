@@ -192,6 +192,55 @@ kda_status kda_prefill_gated(const kda_shape* shape, const void* q, const void* 
                         nullptr, nullptr, nullptr, stream, gate, norm_weight, norm_eps);
 }
 
+kda_status kda_prefill_split_workspace_size(const kda_shape* shape, size_t* bytes) {
+    if (!bytes) return KDA_ERR_INVALID_ARG;
+    *bytes = 0;
+    const kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    *bytes = kda::split_workspace_bytes(shape->total_tokens, shape->num_seqs, shape->H);
+    return KDA_OK;
+}
+
+kda_status kda_prefill_split(const kda_shape* shape, const void* q, const void* k, const void* v,
+                             const float* log_alpha, const void* beta, const float* initial_state,
+                             const int32_t* cu_seqlens, void* out, float* final_state, void* workspace,
+                             size_t workspace_bytes, kda_stream_t stream) {
+    kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens && shape->num_seqs > 0 && shape->total_tokens % shape->num_seqs != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_UNSUPPORTED;
+    if (shape->total_tokens > 0) {
+        st = check_tensor_ptrs(shape, q, k, v, log_alpha, beta, out);
+        if (st != KDA_OK) return st;
+    }
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
+        return KDA_ERR_UNSUPPORTED;
+    const bool split_shape = shape->dtype == KDA_BF16 && shape->dk == 128 && shape->dv == 128;
+    if (split_shape && shape->total_tokens > 0) {
+        if (!workspace) return KDA_ERR_INVALID_ARG;
+        if (!aligned(workspace, 256)) return KDA_ERR_UNSUPPORTED;
+        if (workspace_bytes < kda::split_workspace_bytes(shape->total_tokens, shape->num_seqs, shape->H))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if (shape->num_seqs == 0) return KDA_OK;
+    unsigned int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    kda::PrefillArgs a{q, k, v, log_alpha, beta, initial_state, cu_seqlens, out, final_state,
+                       shape->total_tokens, shape->num_seqs, shape->H, shape->dk, shape->dv,
+                       shape->dtype == KDA_BF16 ? kda::DType::BF16 : kda::DType::F32, status};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!split_shape || !kda::split_supported(a)) {   // the shapes the split kernels do not take
+        const cudaError_t e = kda::chunk_tc_supported(a) ? kda::launch_chunk_tc_prefill(a, s)
+                                                         : kda::launch_recurrent_prefill(a, s);
+        return finish(e, s);
+    }
+    return finish(kda::launch_split_prefill(a, workspace, s), s);
+}
+
 kda_status kda_check_checkpoints(const int32_t* cu, int32_t num_seqs, int64_t total_tokens,
                                  const int32_t* ckpt_cu, const int32_t* ckpt_pos) {
     if (kda_check_cu_seqlens(cu, num_seqs, total_tokens) != KDA_OK) return KDA_ERR_INVALID_ARG;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace kda {
@@ -90,6 +91,11 @@ cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);
 // Chunkwise tensor-core prefill: bf16, dk = dv = 128.
 bool chunk_tc_supported(const PrefillArgs& a);
 cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s);
+// The same prefill split into a chunk-local kernel over every (head, chunk) and a
+// state-chain kernel per (sequence, head), with per-chunk records in a caller workspace.
+bool split_supported(const PrefillArgs& a);
+size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
+cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s);
 // One decode step of T tokens per sequence (state in place).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

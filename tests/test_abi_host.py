@@ -198,3 +198,38 @@ def test_gated_decode_rejects_gate_arguments(L):
     assert call(FAKE, FAKE, -2.0) == 1
     assert call(FAKE, FAKE, 0.0) == 1
     assert call(FAKE_MIS, FAKE, 1e-6) == 2
+
+
+def split(L, sh, ws=FAKE, nbytes=1 << 40, **kw):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)  # noqa: E731
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, b=FAKE, h0=None, cu=None, out=FAKE, fin=None)
+    a.update(kw)
+    return L.kda_prefill_split(ctypes.byref(sh), p(a["q"]), p(a["k"]), p(a["v"]), p(a["la"]), p(a["b"]),
+                               p(a["h0"]), p(a["cu"]), p(a["out"]), p(a["fin"]), p(ws), nbytes, None)
+
+
+def test_split_workspace_size_depends_on_the_shape_only(L):
+    def size(n, T, H):
+        b = ctypes.c_size_t(0)
+        assert L.kda_prefill_split_workspace_size(ctypes.byref(shape(n=n, T=T, H=H)), ctypes.byref(b)) == 0
+        return b.value
+    rec = 12 * 8192
+    slots = 32 * ((131072 + 63) // 64 + 1)
+    assert size(1, 131072, 32) == (slots * 4 + 1023) // 1024 * 1024 + slots * rec
+    assert size(3, 100, 2) == 1024 + 2 * (2 + 3) * rec          # ceil(100/64) + 3 slots a head
+    assert size(0, 0, 4) == 0
+    assert L.kda_prefill_split_workspace_size(ctypes.byref(shape()), None) == _lib.KDA_ERR_INVALID_ARG
+    b = ctypes.c_size_t(7)
+    assert L.kda_prefill_split_workspace_size(ctypes.byref(shape(dk=96)), ctypes.byref(b)) == _lib.KDA_ERR_UNSUPPORTED
+    assert b.value == 0
+
+
+def test_split_rejects_bad_workspace_before_any_cuda_call(L):
+    E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
+    assert split(L, shape(), ws=None) == E_ARG
+    assert split(L, shape(), ws=FAKE + 16) == E_UNS           # not 256-byte aligned
+    assert split(L, shape(), nbytes=1024) == E_ARG            # too small
+    assert split(L, shape(), q=None) == E_ARG
+    assert split(L, shape(n=3, T=128)) == E_ARG
+    assert split(L, shape(dk=96)) == E_UNS
+    assert split(L, shape(n=0, T=0), ws=None, q=None, k=None, v=None, la=None, b=None, out=None) == 0
