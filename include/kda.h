@@ -197,6 +197,34 @@ kda_status kda_prefill_split(const kda_shape* shape, const void* q, const void* 
 kda_status kda_prefill_split_workspace_size(const kda_shape* shape, size_t* bytes);
 
 /*
+ * kda_prefill_split_static -- kda_prefill_split for callers that cannot allocate device
+ * memory: the same two kernels and results, with the workspace in a fixed array that the
+ * library itself owns (KDA_PREFILL_SPLIT_STATIC_BYTES, 64 MiB) instead of caller memory.
+ * The pages have no counterpart of this entry point; it exists for code that runs where a
+ * cudaMalloc is not allowed or not possible (inside another framework's memory pool, under
+ * a fixed memory budget, without an allocator handle).  It allocates nothing.
+ *
+ * Arguments, layouts and results are those of kda_prefill_split without the workspace.
+ * Limits: bf16 with dk = dv = 128 only, and the shape's workspace
+ * (kda_prefill_split_workspace_size: 96 KB per chunk record, H * (ceil(T/64) + N) records)
+ * must fit the array, about 680 records (e.g. 32 heads and up to 1,280 tokens in one
+ * sequence); otherwise KDA_ERR_UNSUPPORTED and nothing is enqueued.
+ * Every GPU that loads the library holds the array until the process exits.  All calls on
+ * a device share it and it keeps the last call's contents; nothing in it needs to start at
+ * zero.  Calls whose work overlaps on the GPU (two streams, or two host threads) race on
+ * the array: order them on one stream or synchronise between them.  The first call on a
+ * device looks up the array's device address with that device current (no allocation),
+ * so make that first call before any stream capture.
+ * Errors: those of kda_prefill_split (other than the workspace ones), KDA_ERR_UNSUPPORTED
+ * for a shape beyond the limits above, KDA_ERR_CUDA if the address lookup or a launch fails.
+ */
+#define KDA_PREFILL_SPLIT_STATIC_BYTES (64u << 20)
+kda_status kda_prefill_split_static(const kda_shape* shape, const void* q, const void* k, const void* v,
+                                    const float* log_alpha, const void* beta, const float* initial_state,
+                                    const int32_t* cu_seqlens, void* out, float* final_state,
+                                    kda_stream_t stream);
+
+/*
  * kda_check_checkpoints -- validate HOST copies of a cu_seqlens table and of a
  * checkpoint table against the rules of kda_prefill_checkpointed.  Returns
  * KDA_OK or KDA_ERR_INVALID_ARG.  No CUDA call.

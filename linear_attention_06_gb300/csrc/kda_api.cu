@@ -101,6 +101,8 @@ kda_status finish(cudaError_t e, cudaStream_t st) {
 
 }  // namespace
 
+unsigned int* kda::device_status_word() { return status_word(); }
+
 extern "C" {
 
 kda_status kda_check_cu_seqlens(const int32_t* cu, int32_t num_seqs, int64_t total_tokens) {

@@ -96,6 +96,8 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s);
 bool split_supported(const PrefillArgs& a);
 size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
 cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s);
+// The library's device status word on the current device (nullptr if it cannot be found).
+unsigned int* device_status_word();
 // One decode step of T tokens per sequence (state in place).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
