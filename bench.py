@@ -337,11 +337,15 @@ def run_ours(args):
                                               lx.conv_k, lx.conv_v, num_seqs=B, out=fe_out, stream=stream))
         t_pg = timed(lambda: kda.kda_prefill_gated(w.q, w.k, w.v, w.log_alpha, w.beta, lx.g_raw, lx.norm_weight,
                                                    cu_seqlens=cu, out=out, final_state=fin, stream=stream))
+        # the front end fused into the prefill: raw projections in, out and final states out
+        t_pf = timed(lambda: kda.kda_prefill_frontend(lx.q_raw, lx.k_raw, lx.v_raw, lx.a_raw, lx.b_raw, lx.conv_q,
+                                                      lx.conv_k, lx.conv_v, cu_seqlens=cu, out=out, final_state=fin,
+                                                      stream=stream))
         gx = workloads.make_layer_inputs(DEC_N, H, D, D, dtype=torch.bfloat16, seed=12 + rank,
                                          cu_seqlens=list(range(DEC_N + 1)), device=dev)
         t_dg = timed(lambda: kda.kda_decode_step_gated(dw.q, dw.k, dw.v, dw.log_alpha, dw.beta, gx.g_raw,
                                                        gx.norm_weight, S, out=dout, stream=stream))
-        layer = {"t_fe": t_fe, "t_pg": t_pg, "t_dg": t_dg}
+        layer = {"t_fe": t_fe, "t_pg": t_pg, "t_dg": t_dg, "t_pf": t_pf}
 
         # NEXT-1: the benchmark prefill also saving every sequence's state each CKPT_EVERY
         # tokens.  The checkpoint tables go to the device once (the binding would validate
@@ -521,6 +525,15 @@ def run_ours(args):
                          "us_per_step": layer["t_fe"] * 1e6, "achieved_gbs": fbytes / layer["t_fe"] / 1e9,
                          "peak_gbs": hbm, "frac": fbytes / layer["t_fe"] / 1e9 / hbm,
                          "algorithmic_bytes_per_launch": fbytes, "kernels": ["conv_kernel", "gate_kernel"]},
+            "prefill_frontend": {"workload": WORKLOAD + "_frontend_W4",
+                                 "ms_per_step": layer["t_pf"] * 1e3, "value": world * B * T / layer["t_pf"],
+                                 "unit": UNIT, "achieved_gbs": pbytes / layer["t_pf"] / 1e9,
+                                 "frac": pbytes / layer["t_pf"] / 1e9 / hbm, "algorithmic_bytes_per_launch": pbytes,
+                                 "two_pass_ms": (layer["t_fe"] + t_prefill) * 1e3,
+                                 "kernels": ["chunk_tc_kernel (front end in team P)"],
+                                 "note": "kda_prefill_frontend: raw projections in (the same bytes as the prefill's "
+                                         "inputs), the front end run on each chunk's tiles in shared memory; "
+                                         "two_pass_ms = kda_frontend + kda_prefill"},
             "prefill_gated": {"workload": WORKLOAD + "_gated", "ms_per_step": layer["t_pg"] * 1e3,
                               "value": world * B * T / layer["t_pg"], "unit": UNIT,
                               "achieved_gbs": gbytes / layer["t_pg"] / 1e9,

@@ -292,6 +292,29 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps,
                         float* log_alpha, void* beta, kda_stream_t stream);
 
 /*
+ * kda_prefill_frontend -- kda_frontend and kda_prefill in one pass: the prefill reads the
+ * raw projections and runs the front end of Visual 1 ("Kimi K3 architecture: KDA, MLA
+ * and MoE", section "Scale: Total vs Active Parameters and Serving Economics", the KDA
+ * inset: short convolution, SiLU and L2 norm for q and k, convolution and SiLU for v,
+ * sigmoid gates) on each chunk's tiles as they arrive, before the recurrence.  The
+ * processed q, k, v, log_alpha and beta never go to memory.
+ *
+ * Arguments: the raw inputs, taps, conv_width and eps of kda_frontend (same layouts and
+ * readings), and initial_state, cu_seqlens, out, final_state of kda_prefill.  out and
+ * final_state are those kda_prefill gives on kda_frontend's outputs, within the bf16
+ * tolerance (the front end's values are rounded to bf16 at the same points).
+ * Supported: bf16 with dk = dv = 128 (otherwise KDA_ERR_UNSUPPORTED; run kda_frontend
+ * and kda_prefill instead).
+ * Errors: the shape and pointer errors of kda_prefill, and those of kda_frontend for
+ * conv_width, eps and the taps.
+ */
+kda_status kda_prefill_frontend(const kda_shape* shape, int32_t conv_width, float eps, const void* q_raw,
+                                const void* k_raw, const void* v_raw, const float* a_raw, const void* b_raw,
+                                const float* conv_q, const float* conv_k, const float* conv_v,
+                                const float* initial_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, kda_stream_t stream);
+
+/*
  * kda_decode_step_gated -- kda_decode_step whose stored output is the gated
  * output of kda_prefill_gated (gate [N*T, H, dv] in dtype, norm_weight [dv]
  * fp32, norm_eps finite and > 0), fused into the step's output store.  The state update

@@ -68,6 +68,8 @@ def lib():
         L.kda_prefill_split.restype = ctypes.c_int
         L.kda_prefill_split_workspace_size.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t)]
         L.kda_prefill_split_workspace_size.restype = ctypes.c_int
+        L.kda_prefill_frontend.argtypes = [sp, ctypes.c_int32, ctypes.c_float] + [vp] * 13
+        L.kda_prefill_frontend.restype = ctypes.c_int
         L.kda_status_string.argtypes = [ctypes.c_int]
         L.kda_status_string.restype = ctypes.c_char_p
         L.kda_version.argtypes = []
@@ -312,6 +314,31 @@ def kda_frontend(q_raw, k_raw, v_raw, a_raw, b_raw, conv_q, conv_k, conv_v, cu_s
                             _stream(stream))
     _check("kda_frontend", st)
     return q, k, v, la, beta
+
+
+def kda_prefill_frontend(q_raw, k_raw, v_raw, a_raw, b_raw, conv_q, conv_k, conv_v, initial_state=None,
+                         cu_seqlens=None, out=None, final_state=None, num_seqs=None, eps=1e-6, stream=None):
+    """The layer front end and the prefill in one pass (see ``include/kda.h``): raw
+    projections in (as kda_frontend takes them), (out, final_state) out."""
+    T, H, dk = q_raw.shape
+    dv = v_raw.shape[2]
+    W = conv_q.shape[-1]
+    if cu_seqlens is not None and not (isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda):
+        host_cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu()
+        kda_check_cu_seqlens(host_cu, T)
+        cu_seqlens = host_cu.to(q_raw.device)
+    n = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=q_raw.dtype, device=q_raw.device)
+    if final_state is True:
+        final_state = torch.empty((n, H, dk, dv), dtype=torch.float32, device=q_raw.device)
+    shape = KdaShape(n, T, H, dk, dv, _dtype_code(q_raw))
+    st = lib().kda_prefill_frontend(ctypes.byref(shape), int(W), float(eps), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                                    _ptr(a_raw), _ptr(b_raw), _ptr(conv_q), _ptr(conv_k), _ptr(conv_v),
+                                    _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                    _stream(stream))
+    _check("kda_prefill_frontend", st)
+    return out, final_state
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):

@@ -337,6 +337,44 @@ kda_status kda_frontend(const kda_shape* shape, int32_t conv_width, float eps, c
     return finish(kda::launch_frontend(a, s), s);
 }
 
+kda_status kda_prefill_frontend(const kda_shape* shape, int32_t conv_width, float eps, const void* q_raw,
+                                const void* k_raw, const void* v_raw, const float* a_raw, const void* b_raw,
+                                const float* conv_q, const float* conv_k, const float* conv_v,
+                                const float* initial_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, kda_stream_t stream) {
+    kda_status st = check_shape(shape);
+    if (st != KDA_OK) return st;
+    if (shape->dtype != KDA_BF16 || shape->dk != 128 || shape->dv != 128) return KDA_ERR_UNSUPPORTED;
+    if (shape->total_tokens > 0 && shape->num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (shape->total_tokens > (int64_t)INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (!cu_seqlens && shape->num_seqs > 0 && shape->total_tokens % shape->num_seqs != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && !aligned(cu_seqlens, 4)) return KDA_ERR_UNSUPPORTED;
+    if (conv_width < 1 || conv_width > 4) return KDA_ERR_UNSUPPORTED;
+    if (!(eps > 0.f) || !(eps < INFINITY)) return KDA_ERR_INVALID_ARG;
+    if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
+        return KDA_ERR_UNSUPPORTED;
+    if (shape->total_tokens > 0) {
+        st = check_tensor_ptrs(shape, q_raw, k_raw, v_raw, a_raw, b_raw, out);
+        if (st != KDA_OK) return st;
+        if (!conv_q || !conv_k || !conv_v) return KDA_ERR_INVALID_ARG;
+        if (!aligned(conv_q, 4) || !aligned(conv_k, 4) || !aligned(conv_v, 4)) return KDA_ERR_UNSUPPORTED;
+    }
+    if (shape->num_seqs == 0) return KDA_OK;
+    unsigned int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    kda::PrefillArgs a{q_raw, k_raw, v_raw, a_raw, b_raw, initial_state, cu_seqlens, out, final_state,
+                       shape->total_tokens, shape->num_seqs, shape->H, shape->dk, shape->dv, kda::DType::BF16,
+                       status};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!kda::chunk_tc_supported(a)) return KDA_ERR_UNSUPPORTED;
+    kda::FrontendArgs f{q_raw, k_raw, v_raw, conv_q, conv_k, conv_v, a_raw, b_raw, cu_seqlens,
+                        nullptr, nullptr, nullptr, nullptr, nullptr, shape->total_tokens, shape->num_seqs,
+                        shape->H, shape->dk, shape->dv, conv_width, eps, kda::DType::BF16};
+    f.status = status;
+    return finish(kda::launch_chunk_tc_frontend(a, f, s), s);
+}
+
 kda_status kda_selftest_timeout(uint64_t limit_ns, kda_stream_t stream) {
     if (limit_ns < 1000ull || limit_ns > 1000000000ull) return KDA_ERR_INVALID_ARG;
     unsigned int* p = status_word();

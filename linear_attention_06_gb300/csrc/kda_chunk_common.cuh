@@ -602,6 +602,129 @@ struct Ckpt {
     }
 };
 
+// ---- the layer's front end, in place on a chunk's tiles ---------------------------
+// "Kimi K3 architecture: KDA, MLA and MoE", section "Scale: Total vs Active Parameters and
+// Serving Economics", Visual 1 (the KDA inset): q and k pass a short convolution, SiLU and
+// an L2 norm, v a short convolution and SiLU, the decay and beta a sigmoid.  The
+// convolution is causal and depthwise over the tokens of one sequence with zero history
+// before its start, tap W-1 on the current token (the readings of kda_frontend).  These
+// helpers turn the raw projection tiles a chunk's TMA loads brought in into the recurrence
+// inputs, in the same slots, before the operand build reads them.
+
+// Conv weights of one channel pair as four taps, tap 3 on the current token (taps before
+// 4 - W are zero).
+struct ConvTaps {
+    float2 w[4];
+};
+__device__ __forceinline__ ConvTaps load_taps(const float* __restrict__ conv, int h, int d, int c0, int W) {
+    ConvTaps t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = i - (4 - W);                        // the weight's own tap index
+        t.w[i] = j >= 0 ? make_float2(conv[((size_t)h * d + c0) * W + j], conv[((size_t)h * d + c0 + 1) * W + j])
+                        : make_float2(0.f, 0.f);
+    }
+    return t;
+}
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// SiLU through one hardware tanh: y sigmoid(y) = y/2 (1 + tanh(y/2)).
+__device__ __forceinline__ float silu_tanh_f(float y) {
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * y));
+    return 0.5f * y * (1.f + th);
+}
+
+// Convolution + SiLU of one channel pair down rows [r0, r0 + R) of a bf16 tile (row r's pair
+// at byte offset off(r)), in place; rows >= L are zeroed.  h0, h1, h2: the raw pair of the
+// three tokens before row r0 (zeros before the sequence start), oldest first.  Rows are
+// read eight at a time before any of them is written, so the loads of a batch overlap.
+template <int R, typename Off>
+__device__ __forceinline__ void conv_silu_pair(uint8_t* tile, Off off, int r0, int L, const ConvTaps& tp,
+                                               float2 h0, float2 h1, float2 h2) {
+#pragma unroll 1
+    for (int rb = 0; rb < R; rb += 8) {
+        float2 x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(tile + off(r0 + rb + i)));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + rb + i;
+            float2 y = make_float2(tp.w[3].x * x[i].x, tp.w[3].y * x[i].y);
+            y.x = fmaf(tp.w[0].x, h0.x, fmaf(tp.w[1].x, h1.x, fmaf(tp.w[2].x, h2.x, y.x)));
+            y.y = fmaf(tp.w[0].y, h0.y, fmaf(tp.w[1].y, h1.y, fmaf(tp.w[2].y, h2.y, y.y)));
+            h0 = h1; h1 = h2; h2 = x[i];
+            *reinterpret_cast<uint32_t*>(tile + off(r)) = r < L ? pack_bf16x2(silu_tanh_f(y.x), silu_tanh_f(y.y)) : 0u;
+        }
+    }
+}
+
+// Raw pair of channels (c0, c0 + 1) of the three tokens before t0 (zero before bos).
+__device__ __forceinline__ void conv_halo(const __nv_bfloat16* __restrict__ raw, int64_t t0, int64_t bos, int H,
+                                          int h, int d, int c0, float2& h0, float2& h1, float2& h2) {
+    float2 hv[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int64_t t = t0 - 3 + i;
+        hv[i] = t >= bos ? unpack_bf16x2(*reinterpret_cast<const uint32_t*>(raw + ((size_t)t * H + h) * d + c0))
+                         : make_float2(0.f, 0.f);
+    }
+    h0 = hv[0]; h1 = hv[1]; h2 = hv[2];
+}
+
+// L2 norm over the 128 channels of row r of a q or k tile (two 64-channel halves 16 KB
+// apart, 128-byte swizzled rows): x / sqrt(sum x^2 + eps), in place, bf16.
+__device__ __forceinline__ void l2norm_row(uint8_t* tile, int r, float eps) {
+    float ss = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            const uint4 u = *reinterpret_cast<const uint4*>(tile + hf * 16384 + sw128_offset(r, 16 * ch));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = unpack_bf16x2(w[i]);
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            }
+        }
+    const float rn = rsqrtf(ss + eps);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4* q = reinterpret_cast<uint4*>(tile + hf * 16384 + sw128_offset(r, 16 * ch));
+            const uint4 u = *q;
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = unpack_bf16x2(w[i]);
+                o[i] = pack_bf16x2(f.x * rn, f.y * rn);
+            }
+            *q = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+}
+
+// logsigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the log of a number in (1, 2] through the
+// hardware log2 is accurate to a few 1e-7 absolute, far below what log alpha needs.
+__device__ __forceinline__ float logsigmoid_f(float x) { return fminf(x, 0.f) - __logf(1.f + __expf(-fabsf(x))); }
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
+// log alpha = logsigmoid(decay logits) over a [64][128] fp32 tile, column c = the thread's
+// channel, in place (rows >= L are set to 0: no decay).
+__device__ __forceinline__ void logsigmoid_col(float* A, int c, int L) {
+#pragma unroll 1
+    for (int rb = 0; rb < C; rb += 16) {
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = A[(rb + i) * D + c];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) A[(rb + i) * D + c] = rb + i < L ? logsigmoid_f(x[i]) : 0.f;
+    }
+}
+
 // ---- MMA groups (each issued by one thread) --------------------------------------
 // AP = [Khat; Qhat] x Kb^T : M = 128, N = 64, K = 128 (both K-major).
 __device__ __forceinline__ void mma_gram(uint32_t tb, uint32_t dcol, uint32_t sQK, uint32_t sKB) {

@@ -126,6 +126,20 @@ struct Ctx {
     unsigned int* status;
 };
 
+// The layer's front end, for the instance that reads the raw projections (FRONT): the raw
+// q, k, v (bf16, for the convolution's halo rows), the conv taps [H][128][W] fp32, W in
+// 1..4 and the L2 norm's eps.  The TMA maps of that instance point at the raw tensors.
+struct Front {
+    const __nv_bfloat16* q_raw;
+    const __nv_bfloat16* k_raw;
+    const __nv_bfloat16* v_raw;
+    const float* conv_q;
+    const float* conv_k;
+    const float* conv_v;
+    int W;
+    float eps;
+};
+
 enum { kLdQK = 0, kLdV = 1, kLdA = 2 };
 
 // TMA refill of slot s with the tiles of chunk c (issued by one thread).
@@ -158,11 +172,27 @@ __device__ __forceinline__ void prefetch_chunk(const Ctx& x, const Maps& maps, i
 // W'/U of chunk n-2 (its loads), Kb / P / beta / gamma for chunk n-2's state
 // product (kbp_free), and the Gram columns for chunk n-2's W' read, which comes
 // before that product.
-__device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __restrict__ beta) {
+// With FRONT, the tiles that land are the raw projections: before the build the team turns
+// the decay logits into log alpha (a column per thread), the beta logits into beta, and
+// q, k, v into the recurrence inputs (convolution + SiLU down a channel pair per thread,
+// then the L2 norm of each q and k row), all in place.
+template <bool FRONT>
+__device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __restrict__ beta, const Front fe) {
     const Ctx x = x_in;
     Small& sw = *x.sw;
     const int t = lt();
     bool ok = true, issued = false;
+    // front end: thread t convolves channel pair (t & 63) of k (t < 64) or q (t >= 64) down
+    // all rows, then pair (t & 63) of v down rows [32 (t >> 6), 32 (t >> 6) + 32)
+    const int fpair = t & 63, fc0 = 2 * fpair;
+    const bool fq = t >= 64;
+    ConvTaps tap_qk, tap_v;
+    if constexpr (FRONT) {
+        tap_qk = load_taps(fq ? fe.conv_q : fe.conv_k, x.h, D, fc0, fe.W);
+        tap_v = load_taps(fe.conv_v, x.h, D, fc0, fe.W);
+    }
+    auto qk_pair_off = [fq, fc0](int r) { return qk_off(fq, (uint32_t)r, (uint32_t)fc0); };
+    auto v_pair_off = [fc0](int r) { return half_off((uint32_t)r, (uint32_t)fc0); };
     float braw_next = (t < C && x.bos + t < x.eos && KDA_INDEX_OK((x.bos + t) * x.H + x.h, x.T * x.H, x.status))
                           ? bf2f(beta[(x.bos + t) * x.H + x.h]) : 0.f;
     for (int n = 0; n < x.nchunks; ++n) {
@@ -179,17 +209,38 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
         uint8_t* aslot = x.sm + kA0 + s * kABytes;
         uint8_t* qk = x.sm + kQK0 + s * kQKBytes;
         uint8_t* kb = x.sm + kKB0 + s * 16384;
+        float2 hq0, hq1, hq2, hv0, hv1, hv2;           // the convolution's halo (raw rows before its first row)
+        if constexpr (FRONT) {
+            conv_halo(fq ? fe.q_raw : fe.k_raw, t0, x.bos, x.H, x.h, D, fc0, hq0, hq1, hq2);
+            if (!fq) conv_halo(fe.v_raw, t0, x.bos, x.H, x.h, D, fc0, hv0, hv1, hv2);
+        }
 
         if (!(ok = group_wait(kBarP, &sw.a_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdA][s];
+        if constexpr (FRONT) logsigmoid_col(reinterpret_cast<float*>(aslot), t, L);   // thread t: column t
         float gval = 0.f;
         const bool fast = build_suffix(reinterpret_cast<float*>(aslot), L, gval);
         // Kb / P / beta / gamma and the q/k tiles of this slot are chunk n-2's until its state product
         if (n >= 2 && !(ok = group_wait(kBarP, &sw.kbp_free[s], ((n - 2) >> 1) & 1))) break;
-        if (t < C) sw.beta[s][t] = __float2bfloat16_rn((t < L) ? braw : 0.f);
+        if (t < C) sw.beta[s][t] = __float2bfloat16_rn((t < L) ? (FRONT ? sigmoid_f(braw) : braw) : 0.f);
         if (fast) sw.gam[s][t] = gval;
         if (!(ok = group_wait(kBarP, &sw.qk_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdQK][s];
+        if constexpr (FRONT) {
+            conv_silu_pair<C>(qk, qk_pair_off, 0, L, tap_qk, hq0, hq1, hq2);
+            group_sync(kBarP);
+            l2norm_row(qk + (fq ? 8192 : 0), fpair, fe.eps);   // thread t: row t & 63 of k or q
+            if (!(ok = group_wait(kBarP, &sw.v_full[s], ph))) break;
+            uint8_t* vt = x.sm + kV0 + s * kVBytes;
+            if (fq) {                                    // rows 32-63: the halo is rows 29-31, still raw
+                hv0 = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(vt + v_pair_off(29)));
+                hv1 = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(vt + v_pair_off(30)));
+                hv2 = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(vt + v_pair_off(31)));
+            }
+            group_sync(kBarP);                           // every halo read before any row is written
+            conv_silu_pair<C / 2>(vt, v_pair_off, fq ? 32 : 0, L, tap_v, hv0, hv1, hv2);
+            group_sync(kBarP);
+        }
         if (fast) build_tiles(qk, kb, reinterpret_cast<const float*>(aslot), L);
         if (!fast) {                                     // token-by-token chunk: no Gram product
             if (t == 0) {
@@ -430,12 +481,13 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
 }
 
 
+template <bool FRONT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
                 const float* __restrict__ h0, const int32_t* __restrict__ cu,
                 __nv_bfloat16* __restrict__ out, float* __restrict__ hT, int64_t T, int num_seqs,
                 int H, unsigned int* status, const int32_t* __restrict__ ck_cu,
-                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states) {
+                const int32_t* __restrict__ ck_pos, float* __restrict__ ck_states, const Front fe) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -498,7 +550,7 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
 
     bool ok = true;
     if (in_team_p())
-        ok = run_team_p(x, beta);
+        ok = run_team_p<FRONT>(x, beta, fe);
     else if (in_group_a())
         ok = run_team_s(x);
     else if (tid < kProducer)
@@ -532,7 +584,11 @@ bool chunk_tc_supported(const PrefillArgs& a) {
            encode_fn() != nullptr;
 }
 
-cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
+namespace {
+// Maps, shared-memory opt-in and launch of one instance (q, k, v, log_alpha, beta are the
+// raw projections for FRONT).
+template <bool FRONT>
+cudaError_t launch_instance(const PrefillArgs& a, const Front& fe, cudaStream_t s) {
     Maps maps;
     if (!make_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.total_tokens, a.H, 64,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -551,17 +607,28 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel<FRONT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)kSmemDynamic);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_release);
     }
     const unsigned blocks = (unsigned)((int64_t)a.num_seqs * a.H);
-    chunk_tc_kernel<<<blocks, kThreads, kSmemDynamic, s>>>(
+    chunk_tc_kernel<FRONT><<<blocks, kThreads, kSmemDynamic, s>>>(
         maps, static_cast<const __nv_bfloat16*>(a.beta), a.initial_state, a.cu_seqlens,
         static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, a.status,
-        a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
+        a.ckpt_cu, a.ckpt_pos, a.ckpt_states, fe);
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s) {
+    return launch_instance<false>(a, Front{}, s);
+}
+
+cudaError_t launch_chunk_tc_frontend(const PrefillArgs& a, const FrontendArgs& f, cudaStream_t s) {
+    const Front fe{static_cast<const __nv_bfloat16*>(f.q_raw), static_cast<const __nv_bfloat16*>(f.k_raw),
+                   static_cast<const __nv_bfloat16*>(f.v_raw), f.conv_q, f.conv_k, f.conv_v, f.conv_width, f.eps};
+    return launch_instance<true>(a, fe, s);
 }
 
 }  // namespace kda

@@ -85,6 +85,11 @@ struct FrontendArgs {
     unsigned int* status = nullptr;   // device status word (bounds-checked builds)
 };
 cudaError_t launch_frontend(const FrontendArgs& a, cudaStream_t s);
+// The chunkwise tensor-core prefill reading the raw projections (q, k, v, log_alpha and
+// beta of `a` point at q_raw, k_raw, v_raw, a_raw and b_raw), the front end done in place
+// on each chunk's tiles before the recurrence (bf16, dk = dv = 128).
+struct PrefillArgs;
+cudaError_t launch_chunk_tc_frontend(const PrefillArgs& a, const FrontendArgs& f, cudaStream_t s);
 
 // fp32 recurrent prefill (any supported dtype / head size).
 cudaError_t launch_recurrent_prefill(const PrefillArgs& a, cudaStream_t s);

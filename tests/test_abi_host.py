@@ -233,3 +233,20 @@ def test_split_rejects_bad_workspace_before_any_cuda_call(L):
     assert split(L, shape(n=3, T=128)) == E_ARG
     assert split(L, shape(dk=96)) == E_UNS
     assert split(L, shape(n=0, T=0), ws=None, q=None, k=None, v=None, la=None, b=None, out=None) == 0
+
+
+def test_prefill_frontend_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    def call(sh, W=4, eps=1e-6, ptrs=FAKE, conv=FAKE, out=FAKE):
+        return L.kda_prefill_frontend(ctypes.byref(sh), W, ctypes.c_float(eps), P(ptrs), P(ptrs), P(ptrs), P(ptrs),
+                                      P(ptrs), P(conv), P(conv), P(conv), None, None, P(out), None, None)
+    E_ARG, E_UNS = _lib.KDA_ERR_INVALID_ARG, _lib.KDA_ERR_UNSUPPORTED
+    assert call(shape(), W=0) == E_UNS and call(shape(), W=5) == E_UNS
+    assert call(shape(), eps=0.0) == E_ARG and call(shape(), eps=float("nan")) == E_ARG
+    assert call(shape(), conv=0) == E_ARG
+    assert call(shape(), ptrs=0) == E_ARG
+    assert call(shape(), ptrs=FAKE_MIS) == E_UNS
+    assert call(shape(dk=64, dv=64)) == E_UNS                  # the tensor-core path only
+    assert call(shape(dt=_lib.KDA_F32)) == E_UNS
+    assert call(shape(n=3, T=128)) == E_ARG
+    assert call(shape(n=0, T=0), ptrs=0, conv=0, out=0) == 0

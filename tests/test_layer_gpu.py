@@ -197,3 +197,69 @@ def test_decode_gated_all_zero_rows_stay_finite():
                                     S, norm_eps=1e-6)
     torch.cuda.synchronize()
     assert torch.isfinite(out.float()).all() and torch.count_nonzero(out) == 0
+
+
+# ---- the front end fused into the prefill (kda_prefill_frontend) --------------------
+
+def fused_layer_ref(x, heads=None, h0=None, eps=1e-6):
+    """fp64 oracle: the layer front end, then the recurrence, on the same raw inputs."""
+    from oracle import kda_oracle
+    sel = slice(None) if heads is None else list(heads)
+    cu = x.cu_seqlens.numpy()
+    q, k, v, la, b = lo.frontend(np64(x.q_raw[:, sel]), np64(x.k_raw[:, sel]), np64(x.v_raw[:, sel]),
+                                 np64(x.conv_q[sel]), np64(x.conv_k[sel]), np64(x.conv_v[sel]),
+                                 np64(x.a_raw[:, sel]), np64(x.b_raw[:, sel]), cu_seqlens=cu, eps=eps)
+    return kda_oracle.prefill(q, k, v, la, b, None if h0 is None else np64(h0[:, sel]), cu_seqlens=cu)
+
+
+def run_fused_layer(x, h0=None, eps=1e-6):
+    d = x.to(DEV)
+    out, fin = kda.kda_prefill_frontend(d.q_raw, d.k_raw, d.v_raw, d.a_raw, d.b_raw, d.conv_q, d.conv_k,
+                                        d.conv_v, initial_state=h0, cu_seqlens=d.cu_seqlens, final_state=True,
+                                        eps=eps)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_prefill_frontend_matches_oracle(W):
+    # ragged sequences: the convolution's halo crosses chunk boundaries inside a sequence and
+    # restarts at each sequence start (one-token and empty sequences included)
+    cu = [0, 1, 77, 77, 200, 333, 500]
+    x = workloads.make_layer_inputs(cu[-1], 2, 128, 128, W=W, dtype=torch.bfloat16, seed=80 + W, cu_seqlens=cu)
+    h0 = torch.randn((6, 2, 128, 128), generator=torch.Generator().manual_seed(81), dtype=torch.float32) * 0.05
+    out, fin = run_fused_layer(x, h0=h0.to(DEV))
+    ro, rf = fused_layer_ref(x, h0=h0)
+    assert rel_l2(np64(out), ro) <= 5e-3 and rel_l2(np64(fin), rf) <= 5e-3
+
+
+def test_prefill_frontend_agrees_with_two_pass_path():
+    cu = [0, 300, 640, 700]
+    x = workloads.make_layer_inputs(cu[-1], 3, 128, 128, W=4, dtype=torch.bfloat16, seed=82, cu_seqlens=cu)
+    out, fin = run_fused_layer(x, eps=1e-5)
+    d = x.to(DEV)
+    q, k, v, la, b = kda.kda_frontend(d.q_raw, d.k_raw, d.v_raw, d.a_raw, d.b_raw, d.conv_q, d.conv_k, d.conv_v,
+                                      cu_seqlens=d.cu_seqlens, eps=1e-5)
+    o2, f2 = kda.kda_prefill(q, k, v, la, b, None, d.cu_seqlens, final_state=True)
+    torch.cuda.synchronize()
+    assert rel_l2(np64(out), np64(o2)) <= 5e-3 and rel_l2(np64(fin), np64(f2)) <= 5e-3
+
+
+def test_prefill_frontend_token_by_token_chunks():
+    # decay logits far below zero make log alpha ~ a_raw, so some chunks leave the factored
+    # range and run token by token from the processed tiles
+    cu = [0, 64, 64 + 150, 400]
+    x = workloads.make_layer_inputs(cu[-1], 2, 128, 128, W=4, dtype=torch.bfloat16, seed=83, cu_seqlens=cu)
+    x.a_raw[70:90, :, ::3] = -200.0
+    out, fin = run_fused_layer(x)
+    ro, rf = fused_layer_ref(x)
+    assert rel_l2(np64(out), ro) <= 5e-3 and rel_l2(np64(fin), rf) <= 5e-3
+
+
+def test_prefill_frontend_full_size_sampled_heads():
+    x = workloads.make_layer_inputs(4 * 8192, 32, 128, 128, W=4, dtype=torch.bfloat16, seed=84, num_seqs=4,
+                                    device=DEV)
+    out, fin = run_fused_layer(x)
+    heads = [0, 31]
+    ro, rf = fused_layer_ref(x, heads=heads)
+    assert rel_l2(np64(out[:, heads]), ro) <= 5e-3 and rel_l2(np64(fin[:, heads]), rf) <= 5e-3
