@@ -229,6 +229,7 @@ cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t st) {
     if (a.num_seqs == 0) return cudaSuccess;
+    if (decode_chunk_supported(a)) return launch_decode_chunk(a, st);
     if (a.dk == 128 && a.dv == 128) return launch_dims<128, 128>(a, st);
     if (a.dk == 128 && a.dv == 64) return launch_dims<128, 64>(a, st);
     if (a.dk == 64 && a.dv == 128) return launch_dims<64, 128>(a, st);

@@ -88,6 +88,19 @@ def main() -> int:
             kda.kda_decode_step_gated(d.q, d.k, d.v, d.log_alpha, d.beta, g.g_raw, g.norm_weight, S)
             check(f"gated decode T={T} dk={dk} dv={dv}")
 
+    # multi-token decode: the fp32 token loop, and bf16 steps whose decay sends them token by token
+    for T in (5, 16):
+        n = 9
+        c = [T * i for i in range(n + 1)]
+        d = workloads.make_inputs(n * T, 3, 128, 128, dtype=torch.float32, seed=T, cu_seqlens=c,
+                                  state_std=0.05).to(dev)
+        kda.kda_decode_step(d.q, d.k, d.v, d.log_alpha, d.beta, d.initial_state.clone())
+        check(f"decode fp32 T={T}")
+        d = workloads.make_inputs(n * T, 3, 128, 128, seed=T + 1, cu_seqlens=c, state_std=0.05).to(dev)
+        d.log_alpha.mul_(200.0)
+        kda.kda_decode_step(d.q, d.k, d.v, d.log_alpha, d.beta, d.initial_state.clone())
+        check(f"decode strong decay T={T}")
+
     if failures:
         print("index checks failed:", ", ".join(failures))
         return 1

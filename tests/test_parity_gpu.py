@@ -235,7 +235,10 @@ def test_device_status_is_clean():
 
 
 # ---- multi-token decode (T tokens per sequence through the decode path) -------------
-@pytest.mark.parametrize("T", [2, 5, 16])
+# At dk = dv = 128 a step of 2..16 tokens takes the chunk form (bf16: tensor cores, T <= 8
+# and T <= 16 instances) or the fp32 token loop (fp32 inputs, and any step whose decay over the
+# step passes e^-60 in some channel); other head sizes keep the token loop of the one-token step.
+@pytest.mark.parametrize("T", [2, 5, 8, 9, 16])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_decode_multi_token_matches_oracle(T, dtype):
     n = 24
@@ -249,21 +252,75 @@ def test_decode_multi_token_matches_oracle(T, dtype):
     assert rel_l2(np64(out), ro) < TOL[dtype] and rel_l2(np64(S), rf) < TOL[dtype]
 
 
-def test_decode_multi_token_equals_repeated_single_steps():
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64), (64, 64)])
+def test_decode_multi_token_other_head_sizes(dk, dv):
+    n, T = 12, 6
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, 3, dk, dv, seed=31, cu_seqlens=cu, state_std=0.05).to(DEV)
+    S = w.initial_state.clone()
+    out = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(w)
+    assert rel_l2(np64(out), ro) < TOL[torch.bfloat16] and rel_l2(np64(S), rf) < TOL[torch.bfloat16]
+
+
+def test_decode_multi_token_strong_decay_mixed_with_chunk_form():
+    # sequences 0, 5 and 11 decay past e^-60 within the step (some channels reach -inf): their
+    # (sequence, head) blocks run token by token, the others in the chunk form, in one launch
+    n, T, H = 12, 16, 4
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, H, 128, 128, seed=32, cu_seqlens=cu, state_std=0.05)
+    for seq in (0, 5, 11):
+        w.log_alpha[seq * T:(seq + 1) * T] *= 100.0
+    w.log_alpha[5 * T + 3, 1, :7] = -float("inf")            # a full reset of a few channels
+    d = w.to(DEV)
+    S = d.initial_state.clone()
+    out = kda.kda_decode_step(d.q, d.k, d.v, d.log_alpha, d.beta, S)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(S).all()
+    ro, rf = oracle_prefill(w)
+    assert rel_l2(np64(out), ro) < TOL[torch.bfloat16] and rel_l2(np64(S), rf) < TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_multi_token_agrees_with_repeated_single_steps(dtype):
+    # the chunk form and the fp32 token loop are exact rewrites of T one-token steps, not the
+    # same sequence of roundings: they agree within the tolerance of the dtype
     n, T, H = 16, 7, 4
     cu = [T * i for i in range(n + 1)]
-    w = workloads.make_inputs(n * T, H, 128, 128, seed=40, cu_seqlens=cu, state_std=0.05).to(DEV)
+    w = workloads.make_inputs(n * T, H, 128, 128, dtype=dtype, seed=40, cu_seqlens=cu, state_std=0.05).to(DEV)
     S_multi = w.initial_state.clone()
     out_multi = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S_multi)
     S_step = w.initial_state.clone()
     rows = torch.arange(n, device=DEV) * T
+    outs = torch.empty_like(out_multi)
     for t in range(T):
         r = rows + t
-        o_t = kda.kda_decode_step(w.q[r].contiguous(), w.k[r].contiguous(), w.v[r].contiguous(),
-                                  w.log_alpha[r].contiguous(), w.beta[r].contiguous(), S_step)
-        assert torch.equal(o_t, out_multi[r])
+        outs[r] = kda.kda_decode_step(w.q[r].contiguous(), w.k[r].contiguous(), w.v[r].contiguous(),
+                                      w.log_alpha[r].contiguous(), w.beta[r].contiguous(), S_step)
     torch.cuda.synchronize()
-    assert torch.equal(S_step, S_multi)
+    assert rel_l2(np64(out_multi), np64(outs)) < TOL[dtype]
+    assert rel_l2(np64(S_multi), np64(S_step)) < TOL[dtype]
+
+
+def test_decode_multi_token_zero_beta_is_pure_decay():
+    # beta = 0: no erase and no write, so the state is only decayed: S = Diag(e^G) S0 exactly
+    # up to the fp32 product of the decay factors, and o_t = (e^{g_t} o q_t)^T S0
+    n, T, H = 6, 10, 2
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, H, 128, 128, seed=41, cu_seqlens=cu, state_std=0.05)
+    w.beta.zero_()
+    d = w.to(DEV)
+    S = d.initial_state.clone()
+    out = kda.kda_decode_step(d.q, d.k, d.v, d.log_alpha, d.beta, S)
+    torch.cuda.synchronize()
+    la = np64(w.log_alpha).reshape(n, T, H, 128)
+    G = la.sum(axis=1)                                        # [n, H, dk]
+    S_ref = np.exp(G)[..., None] * np64(w.initial_state)
+    assert rel_l2(np64(S), S_ref) < 1e-5
+    g = np.cumsum(la, axis=1)
+    o_ref = np.einsum("nthk,nhkv->nthv", np.exp(g) * np64(w.q).reshape(n, T, H, 128), np64(w.initial_state))
+    assert rel_l2(np64(out).reshape(n, T, H, 128), o_ref) < TOL[torch.bfloat16]
 
 
 # ---- checkpoint emission during prefill ---------------------------------------------
