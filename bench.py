@@ -51,9 +51,6 @@ def frontend_bytes(tokens, heads, d=128, width=4):
     return tokens * heads * per + 3 * heads * d * width * 4
 
 
-# fp32 CUDA-core rate for the decode step's arithmetic: 152 SMs x 128 fp32 lanes x 2 flop (FMA)
-# x 2.07 GHz (the GB300's maximum SM clock)
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # decode arithmetic per token-head (dk = dv = D): decay D*D multiplies, r = S^T k, y = S^T q and
 # the rank-1 update D*D fused multiply-adds each (2 flop)
 DECODE_FLOP_PER_TOKEN_HEAD = D * D + 3 * 2 * D * D
@@ -65,18 +62,18 @@ def decode_bytes(n, heads, tokens=1):
 
 
 def _multi_decode_entry(tm, t_m, world, hbm):
-    """One multi-token decode line: HBM and fp32-ALU fractions; the bound is the roof
-    whose ideal time is longer."""
+    """One multi-token decode line.  Steps of 2..16 tokens at d = 128 run the chunk form: its
+    three state products are TF32 tensor-core work far below the tensor roof, so HBM is the
+    bound; the fp32 CUDA-core flops of the token-by-token form are kept for comparison."""
     nbytes = decode_bytes(DEC_N, H, tm)
     flops = DEC_N * tm * H * DECODE_FLOP_PER_TOKEN_HEAD
-    t_hbm, t_alu = nbytes / (hbm * 1e9), flops / (FP32_ALU_TFLOPS * 1e12)
+    t_hbm = nbytes / (hbm * 1e9)
     return {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}_T{tm}", "tokens_per_seq": tm,
             "us_per_step": t_m * 1e6, "value": world * DEC_N * tm / t_m, "unit": UNIT,
-            "achieved_gbs": nbytes / t_m / 1e9, "frac_hbm": t_hbm / t_m,
-            "achieved_tflops": flops / t_m / 1e12, "frac_alu": t_alu / t_m,
-            "alu_peak_tflops": FP32_ALU_TFLOPS, "bound": "hbm" if t_hbm >= t_alu else "alu",
-            "frac": max(t_hbm, t_alu) / t_m,
-            "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops, "kernels": ["decode_kernel"]}
+            "achieved_gbs": nbytes / t_m / 1e9, "frac_hbm": t_hbm / t_m, "bound": "hbm", "frac": t_hbm / t_m,
+            "token_loop_flops_per_launch": flops, "tensor_flops_per_launch": DEC_N * H * 6 * tm * D * D,
+            "algorithmic_bytes_per_launch": nbytes,
+            "kernels": ["decode_chunk_kernel" if tm > 1 else "decode_kernel"]}
 
 
 def load_peaks():

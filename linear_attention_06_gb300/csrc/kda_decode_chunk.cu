@@ -9,36 +9,48 @@
 //
 //   K_g = e^{g} o K,  Q_g = e^{g} o Q,  Kb = e^{G-g} o K,
 //   A_ts = sum_c k_tc k_sc e^{g_tc - g_sc}  (s < t),  P_ts = sum_c q_tc k_sc e^{g_tc - g_sc}  (s <= t),
-//   [W | U] = T [K_g | V] with T = (I + Diag(beta) A)^-1 Diag(beta)   (forward substitution),
-//   Delta = U - W S0,   O = Q_g S0 + P Delta,   S = Diag(e^G) S0 + Kb^T Delta.
+//   R = V - K_g S0,   (I + Diag(beta) A) Delta = Diag(beta) R,
+//   O = Q_g S0 + P Delta,   S = Diag(e^G) S0 + Kb^T Delta.
 //
-// A and P are formed as Khat Kb^T and Qhat Kb^T (Khat = e^{g-G} o K, Qhat = e^{g-G} o Q), so
-// the form is taken while every key channel has G >= -60 (e^60 ~ 1e26, far inside the fp32
-// range); a step that decays harder (log_alpha = -inf included) runs token by token in fp32
-// instead, on the same register layout.  All other factors are e^{x} with x <= 0.
+// (Delta = T R with T = (I + Diag(beta) A)^-1 Diag(beta) is the UT / WY form U - W S0 with
+// U = T V and W = T K_g, applied in the other order: no T is formed; each warp solves the
+// triangular system for its own columns of R by forward substitution.)  A and P are formed as
+// Khat Kb^T and Qhat Kb^T (Khat = e^{g-G} o K, Qhat = e^{g-G} o Q), so the form is taken while
+// every key channel has G >= -60 (e^60 ~ 1e26, far inside the fp32 range); a step that decays
+// harder (log_alpha = -inf included) runs token by token in fp32 instead, on the same register
+// layout.  All other factors are e^{x} with x <= 0.
 //
-// Three products touch the state: W S0 and Q_g S0 (T x 128 by 128 x 128) and Kb^T Delta
-// (128 x T by T x 128).  They run on the tensor cores (mma.sync m16n8k8, TF32 operands, fp32
-// accumulation) with the state held in registers.  Warp w of the block owns the value columns
-// 16w .. 16w+15 for all 128 key rows; lane 4 gi + qi holds S0[i][j] for
+// Products.  K_g S0 and Q_g S0 (T x 128 by 128 x 128) and Kb^T Delta (128 x T by T x 128) touch
+// the state; they run on the tensor cores (mma.sync m16n8k8, TF32 operands, fp32 accumulation)
+// with the state held in registers.  Warp w of the block owns the value columns 16w .. 16w+15
+// for all 128 key rows; lane 4 gi + qi holds S0[i][j] for
 //   j in {16w + 2 gi, 16w + 2 gi + 1},  i in {8 b + 2 qi, 8 b + 2 qi + 1 : b = 0..15},
 // which are, element for element, the A fragments of S0^T (fragment row gi <-> column
 // 16w + 2 gi, row gi + 8 <-> column 16w + 2 gi + 1; fragment column qi <-> key row 8b + 2qi,
-// column qi + 4 <-> key row 8b + 2qi + 1) for Delta^T = U^T - S0^T W^T and O^T = S0^T Q_g^T, and
-// the accumulator fragments of S^T += Delta^T Kb.  The token index of Delta, P and Kb is
+// column qi + 4 <-> key row 8b + 2qi + 1) for R^T = V^T - S0^T K_g^T and O^T = S0^T Q_g^T, and
+// the accumulator fragments of S^T += Delta^T Kb.  The token index of R, Delta, P and Kb is
 // permuted the same way (fragment k = qi <-> token 8kk + 2qi, k = qi + 4 <-> 8kk + 2qi + 1), so
-// the accumulator of Delta^T is already the A fragment of the two products that read it.  The
-// state therefore crosses HBM once in each direction, and no product needs a reduction across
-// warps.  The small steps (cumulative decay, A and P, the solve) run in fp32 on the CUDA cores
-// from shared memory; TF32 rounds the operands of the three state products to 11 significant
-// bits while the carried state stays fp32 (the update adds into it in the fp32 accumulator).
+// an accumulator over tokens is already the A fragment of the next product that reads it.  The
+// state crosses HBM once in each direction, and no product needs a reduction across warps.
+// TF32 rounds the operands of these products to 11 significant bits; the carried state stays
+// fp32 (the update adds into it in the fp32 accumulator).  A and P use split TF32 operands
+// (x = hi + lo, three products), close to fp32, and the triangular solve runs in fp32 on the
+// accumulator of R: the lanes holding token s compute Delta_s and pass it by shuffle to the
+// three other lanes of their column pair, which subtract A_ts Delta_s from their later tokens.
 //
-// fp32 inputs always take that fp32 token loop (decay, the two column sums over the warp's own
+// Schedule of one (sequence, head): the state is loaded into registers while the step's token
+// vectors are staged in shared memory; per key channel the cumulative decay and the scaled
+// rows; A and P (2 NT warps) and the first pass over the state (every warp); then per warp the
+// solve, the output and the state update.
+//
+// fp32 inputs always take the fp32 token loop (decay, the two column sums over the warp's own
 // rows, the rank-one update), so they keep fp32 accuracy; in it a warp needs no other warp
 // until the output store.
 //
-// One block of 256 threads per (sequence, head); two blocks fit an SM (84 KB of shared
-// memory and at most 128 registers a thread each).
+// Blocks are persistent, two per SM (81 KB of shared memory and at most 128 registers a thread
+// each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
+// the state and token rows of its next pair into L2 when it starts a pair, so that their DRAM
+// reads overlap its arithmetic.
 #include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -54,28 +66,29 @@ using namespace sm103;
 constexpr int kD = 128;                 // dk = dv
 constexpr int kThreads = 256;           // 8 warps x 16 value columns
 constexpr int kTok = 16;                // tokens per step, padded with zero tokens
-constexpr float kMaxExponent = 60.f;    // factored A and P while every channel has G >= -60
-// Row strides (floats).  132 = 4 (mod 32): rows read as float4 by the A / P dot products, and
-// the accumulator pairs of U (rows 2qi, columns 2gi); 136 = 8 (mod 32) and 24: the B fragments
-// (eight rows gi, each read as a pair at column 2qi).  Each leaves the warp's loads without
+constexpr float kMaxExponent = 60.f;    // chunk form while every channel has G >= -60
+constexpr float kLog2e = 1.4426950408889634f;
+// Row strides (floats).  136 = 8 (mod 32) and 24: fragments read as pairs by eight rows gi at
+// column 2qi; 132 = 4 (mod 32): the accumulator pairs of V and O (rows 2qi, columns 2gi) and the
+// rows of A read as float4 by the solve.  Each leaves the warp's shared-memory loads without
 // bank conflicts.
-constexpr int kLd = 132, kLdB = 136, kLdT = 24;
+constexpr int kLd = 132, kLdB = 136, kLdT = 24, kLdA = 20;
 
 struct Smem {
-    float k[kTok][kLd];     // k; Khat for the factored A and P
-    float q[kTok][kLd];     // q; Qhat
-    float v[kTok][kLd];     // v; U after the solve
-    float g[kTok][kLd];     // log alpha; then g_t (term-by-term A and P) or alpha (token loop)
-    float kg[kTok][kLdB];   // K_g; -W in TF32 after the solve
-    float kb[kTok][kLd];    // Kb
-    float qg[kTok][kLdB];   // Q_g in TF32
-    float kbt[kD][kLdT];    // Kb^T in TF32
-    float pm[kTok][kLdT];   // P (s <= t, else 0) in TF32
-    float am[kTok][kTok];   // A (s < t)
-    float os[kTok][kLd];    // output rows
-    float dec[kD];          // e^G per key channel
+    float k[kTok][kLdB];     // k; Khat
+    float q[kTok][kLdB];     // q; Qhat
+    float v[kTok][kLd];      // v
+    float g[kTok][kLd];      // log alpha; alpha in the token loop
+    float kg[kTok][kLdB];    // -K_g in TF32
+    float kb[kTok][kLdB];    // Kb
+    float qg[kTok][kLdB];    // Q_g in TF32
+    float kbt[kD][kLdT];     // Kb^T in TF32
+    float am[kTok][kLdA];    // A (s < t, else 0)
+    float pm[kTok][kLdT];    // P (s <= t, else 0) in TF32
+    float os[kTok][kLd];     // output rows
+    float dec[kD];           // e^G per key channel
     float beta[kTok];
-    float kq[kTok];         // k_t . q_t (token loop)
+    float kq[kTok];          // k_t . q_t (token loop)
 };
 
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&x)[8]) {
@@ -108,27 +121,16 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
 __device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
-
-// Position of (t, s) in the row-major lower triangle with (DIAG) or without the diagonal.
-template <bool DIAG>
-__device__ __forceinline__ void tri_index(int d, int& t, int& s) {
-    t = DIAG ? 0 : 1;
-    while ((DIAG ? (t + 1) * (t + 2) / 2 : (t + 1) * t / 2) <= d) ++t;
-    s = d - (DIAG ? t * (t + 1) / 2 : t * (t - 1) / 2);
+__device__ __forceinline__ float ex2(float x) {       // 2^x, the SFU's approximation
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-
-// sum_c x[c] y[c] over the 128 key channels (shared-memory rows).
-__device__ __forceinline__ float row_dot(const float* x, const float* y) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < kD; c += 4) {
-        const float4 xv = *reinterpret_cast<const float4*>(x + c), yv = *reinterpret_cast<const float4*>(y + c);
-        a0 = fmaf(xv.x, yv.x, a0);
-        a1 = fmaf(xv.y, yv.y, a1);
-        a0 = fmaf(xv.z, yv.z, a0);
-        a1 = fmaf(xv.w, yv.w, a1);
-    }
-    return a0 + a1;
+// x = hi + lo with both parts TF32: three products of the parts carry a product to about fp32
+// accuracy (the lo x lo term is below it).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
 }
 
 template <typename Tin>
@@ -140,12 +142,56 @@ struct Params {
     const Tin* beta;
     float* S;
     Tin* out;
-    int H, T;
+    int pairs, H, T;
     const Tin* gate;
     const float* norm_w;
     float norm_eps;
     unsigned int* status;
 };
+
+// State of one pair into registers, directly in the fragment layout: two 8-byte loads per b
+// (rows 8b + 2qi and 8b + 2qi + 1, columns jc and jc + 1).
+__device__ __forceinline__ void load_state(const float* Sp, float (&s)[16][4], int64_t first, int64_t n_state,
+                                           unsigned int* status, int jc, int qi) {
+    (void)first; (void)n_state; (void)status;
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+        const int i = 8 * b + 2 * qi;
+        float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+        if (KDA_INDEX_OK(first + (i + 1) * kD + jc + 1, n_state, status)) {
+            r0 = __ldcs(reinterpret_cast<const float2*>(Sp + i * kD + jc));
+            r1 = __ldcs(reinterpret_cast<const float2*>(Sp + (i + 1) * kD + jc));
+        }
+        s[b][0] = r0.x; s[b][1] = r0.y; s[b][2] = r1.x; s[b][3] = r1.y;
+    }
+}
+__device__ __forceinline__ void store_state(float* Sp, const float (&s)[16][4], int64_t first, int64_t n_state,
+                                            unsigned int* status, int jc, int qi) {
+    (void)first; (void)n_state; (void)status;
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+        const int i = 8 * b + 2 * qi;
+        if (KDA_INDEX_OK(first + (i + 1) * kD + jc + 1, n_state, status)) {
+            __stcs(reinterpret_cast<float2*>(Sp + i * kD + jc), make_float2(s[b][0], s[b][1]));
+            __stcs(reinterpret_cast<float2*>(Sp + (i + 1) * kD + jc), make_float2(s[b][2], s[b][3]));
+        }
+    }
+}
+
+// L2 prefetch of a pair's state and token rows (no completion is waited for).
+template <typename Tin>
+__device__ __forceinline__ void prefetch_pair(const Params<Tin>& p, int pair) {
+    const size_t n = (size_t)pair / p.H, h = (size_t)pair % p.H;
+    const size_t row0 = n * (size_t)p.T * p.H + h;
+    if (threadIdx.x == 0) bulk_prefetch_l2(p.S + (size_t)pair * kD * kD, kD * kD * sizeof(float));
+    const int i = (int)threadIdx.x - 32;                 // warps 1 and 2: one token row each
+    if (i >= 0 && i < 4 * p.T) {
+        const int t = i >> 2, a = i & 3;
+        const size_t e = (row0 + (size_t)t * p.H) * kD;
+        if (a == 3) bulk_prefetch_l2(p.log_alpha + e, kD * sizeof(float));
+        else bulk_prefetch_l2((a == 0 ? p.q : a == 1 ? p.k : p.v) + e, kD * sizeof(Tin));
+    }
+}
 
 // The step's token vectors into shared memory (rows T .. 15 zero: tokens that change nothing).
 template <typename Tin>
@@ -255,54 +301,134 @@ __device__ __forceinline__ void token_loop(Smem& sm, float (&s)[16][4], int T, i
     }
 }
 
-// The chunk form after the scaled rows are in shared memory: A and P, the solve, and the three
-// state products on the tensor cores; writes the output rows to sm.os and leaves the new state
-// in s.
+// Per key channel c (threads c and c + 128, one half of the step's token rows each): the
+// cumulative decay in base 2 and the scaled rows.  Returns whether the chunk form holds (the
+// same answer in every thread).
 template <int NT>
-__device__ __forceinline__ void chunk_products(Smem& sm, float (&s)[16][4], int T, int warp, int gi, int qi,
-                                               int jc) {
-    constexpr int kT8 = 8 * NT;
-    (void)warp;
-    // ---- A (s < t: 120 dot products) and P (s <= t: 136), one per thread ----
-    {
-        const int d = threadIdx.x;
-        int t, s2;
-        const bool isA = d < 120;
-        if (isA) tri_index<false>(d, t, s2);
-        else tri_index<true>(d - 120, t, s2);
-        const float val = t < T ? row_dot(isA ? sm.k[t] : sm.q[t], sm.kb[s2]) : 0.f;
-        if (isA) sm.am[t][s2] = val;
-        else sm.pm[t][s2] = tf32f(val);
+__device__ __forceinline__ bool scale_rows(Smem& sm) {
+    constexpr int kT8 = 8 * NT, kTH = kT8 / 2;       // token rows, rows per half
+    const int c = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;
+    float run = 0.f;
+    for (int t = 0; t < half * kTH; ++t) run += sm.g[t][c];
+    float gl[kTH];
+#pragma unroll
+    for (int i = 0; i < kTH; ++i) { run += sm.g[half * kTH + i][c]; gl[i] = run; }
+    for (int t = (half + 1) * kTH; t < kT8; ++t) run += sm.g[t][c];
+    const float G = run;                             // the same order of additions in both halves
+    if (!__syncthreads_and(G >= -kMaxExponent)) return false;   // false for NaN and -inf too
+    const float G2 = G * kLog2e;
+    float kbt[kTH];
+#pragma unroll
+    for (int i = 0; i < kTH; ++i) {
+        const int t = half * kTH + i;
+        const float g2 = gl[i] * kLog2e;
+        const float eg = ex2(g2), eb = ex2(G2 - g2), eh = ex2(g2 - G2);
+        const float kv = sm.k[t][c], qv = sm.q[t][c];
+        const float kb = eb * kv;
+        sm.kb[t][c] = kb;
+        kbt[i] = tf32f(kb);
+        sm.kg[t][c] = -tf32f(eg * kv);
+        sm.k[t][c] = eh * kv;
+        sm.qg[t][c] = tf32f(eg * qv);
+        sm.q[t][c] = eh * qv;
     }
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTH; i += 4)
+        *reinterpret_cast<float4*>(&sm.kbt[c][half * kTH + i]) = make_float4(kbt[i], kbt[i + 1], kbt[i + 2], kbt[i + 3]);
+    if (half == 0) sm.dec[c] = ex2(G2);
+    return true;
+}
 
-    // ---- forward substitution: thread col solves column col of [W | U] = T [K_g | V] ----
-    {
-        const int col = threadIdx.x;
-        float* ycol = col < kD ? &sm.kg[0][col] : &sm.v[0][col - kD];
-        const int ld = col < kD ? kLdB : kLd;
-        float x[kT8];
+// A = Khat Kb^T and P = Qhat Kb^T, 16 x 8 tiles on the tensor cores with split TF32 operands
+// (fragment k = qi <-> channel 8b + 2qi, k = qi + 4 <-> 8b + 2qi + 1); warp w < 2 NT takes tile
+// w (A for w < NT, P after), three independent accumulators over the 128 channels.
+template <int NT>
+__device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
+    const bool isP = warp >= NT;
+    const int nt = warp % NT;
+    const float* X = isP ? &sm.q[0][0] : &sm.k[0][0];
+    float acc[3][4] = {};
 #pragma unroll
-        for (int t = 0; t < kT8; ++t) {
-            float a0 = ycol[t * ld], a1 = 0.f;
+    for (int b = 0; b < 16; ++b) {
+        const float2 x0 = *reinterpret_cast<const float2*>(X + gi * kLdB + 8 * b + 2 * qi);
+        const float2 x1 = *reinterpret_cast<const float2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi);
+        const float2 y = *reinterpret_cast<const float2*>(&sm.kb[8 * nt + gi][8 * b + 2 * qi]);
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(x0.x, ah[0], al[0]); split_tf32(x1.x, ah[1], al[1]);
+        split_tf32(x0.y, ah[2], al[2]); split_tf32(x1.y, ah[3], al[3]);
+        split_tf32(y.x, bh[0], bl[0]); split_tf32(y.y, bh[1], bl[1]);
+        mma_tf32(acc[0], al, bh);
+        mma_tf32(acc[1], ah, bl);
+        mma_tf32(acc[2], ah, bh);
+    }
+    float c[4];
 #pragma unroll
-            for (int u = 0; u < t; ++u) {
-                if (u & 1) a1 = fmaf(-sm.am[t][u], x[u], a1);
-                else a0 = fmaf(-sm.am[t][u], x[u], a0);
-            }
-            x[t] = sm.beta[t] * (a0 + a1);
-            ycol[t * ld] = col < kD ? -tf32f(x[t]) : x[t];
+    for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e] + acc[2][e];
+    // c: (t = gi, s = 8 nt + 2 qi, +1), (t = gi + 8, same s)
+    const int s0 = 8 * nt + 2 * qi;
+    if (isP) {
+        *reinterpret_cast<float2*>(&sm.pm[gi][s0]) =
+            make_float2(s0 <= gi ? tf32f(c[0]) : 0.f, s0 + 1 <= gi ? tf32f(c[1]) : 0.f);
+        *reinterpret_cast<float2*>(&sm.pm[gi + 8][s0]) =
+            make_float2(s0 <= gi + 8 ? tf32f(c[2]) : 0.f, s0 + 1 <= gi + 8 ? tf32f(c[3]) : 0.f);
+    } else {
+        *reinterpret_cast<float2*>(&sm.am[gi][s0]) = make_float2(s0 < gi ? c[0] : 0.f, s0 + 1 < gi ? c[1] : 0.f);
+        *reinterpret_cast<float2*>(&sm.am[gi + 8][s0]) =
+            make_float2(s0 < gi + 8 ? c[2] : 0.f, s0 + 1 < gi + 8 ? c[3] : 0.f);
+    }
+}
+
+// (I + Diag(beta) A) Delta = Diag(beta) R on the warp's columns, in place on the accumulator rt
+// of R^T (rt[nt][p] / rt[nt][2 + p]: token 8 nt + 2 qi + p, columns jc / jc + 1).  Step s: the
+// lanes with qi = (s mod 8) / 2 hold token s and finish Delta_s = beta_s x (R_s - the terms
+// already subtracted); a shuffle gives it to the other lanes of the column pair, which subtract
+// A_ts Delta_s from every later token t they hold (A is zero on and above the diagonal).
+template <int NT>
+__device__ __forceinline__ void solve_delta(const Smem& sm, float (&rt)[NT][4], int lane, int qi) {
+    constexpr int kT8 = 8 * NT;
+#pragma unroll
+    for (int s4 = 0; s4 < kT8; s4 += 4) {
+        float4 a[NT][2];                             // A[8 nt + 2 qi + p][s4 .. s4 + 3]
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) a[nt][p] = *reinterpret_cast<const float4*>(&sm.am[8 * nt + 2 * qi + p][s4]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int s = s4 + u, ns = s >> 3, ps = s & 1, qs = (s & 7) >> 1;
+            const float bs = sm.beta[s];
+            const bool own = qi == qs;
+            const float d0 = bs * rt[ns][ps], d1 = bs * rt[ns][2 + ps];
+            if (own) { rt[ns][ps] = d0; rt[ns][2 + ps] = d1; }
+            const int src = (lane & ~3) | qs;
+            const float D0 = __shfl_sync(0xffffffffu, d0, src), D1 = __shfl_sync(0xffffffffu, d1, src);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const float4 av = a[nt][p];
+                    const float ats = u == 0 ? av.x : u == 1 ? av.y : u == 2 ? av.z : av.w;
+                    rt[nt][p] = fmaf(-ats, D0, rt[nt][p]);
+                    rt[nt][2 + p] = fmaf(-ats, D1, rt[nt][2 + p]);
+                }
         }
     }
-    __syncthreads();
+}
 
-    // ---- the state products on the tensor cores ----
-    float dt[NT][4], ot[NT][4];                      // Delta^T and O^T accumulators
+// Chunk form after scale_rows: returns with the output rows in sm.os and the new state in s.
+template <int NT>
+__device__ __forceinline__ void chunk_products(Smem& sm, float (&s)[16][4], int warp, int lane, int gi, int qi,
+                                               int jc) {
+    if (warp < 2 * NT) gram_tile<NT>(sm, warp, gi, qi);
+
+    // R^T = V^T - S0^T K_g^T and O^T = S0^T Q_g^T (accumulator: row <-> column jc / jc + 1,
+    // column <-> token 8 nt + 2 qi / + 1)
+    float rt[NT][4], ot[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const float2 u0 = *reinterpret_cast<const float2*>(&sm.v[8 * nt + 2 * qi][jc]);
-        const float2 u1 = *reinterpret_cast<const float2*>(&sm.v[8 * nt + 2 * qi + 1][jc]);
-        dt[nt][0] = u0.x; dt[nt][1] = u1.x; dt[nt][2] = u0.y; dt[nt][3] = u1.y;
+        const float2 v0 = *reinterpret_cast<const float2*>(&sm.v[8 * nt + 2 * qi][jc]);
+        const float2 v1 = *reinterpret_cast<const float2*>(&sm.v[8 * nt + 2 * qi + 1][jc]);
+        rt[nt][0] = v0.x; rt[nt][1] = v1.x; rt[nt][2] = v0.y; rt[nt][3] = v1.y;
         ot[nt][0] = ot[nt][1] = ot[nt][2] = ot[nt][3] = 0.f;
     }
 #pragma unroll
@@ -310,32 +436,37 @@ __device__ __forceinline__ void chunk_products(Smem& sm, float (&s)[16][4], int 
         const uint32_t a[4] = {to_tf32(s[b][0]), to_tf32(s[b][1]), to_tf32(s[b][2]), to_tf32(s[b][3])};
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const uint2 bw = *reinterpret_cast<const uint2*>(&sm.kg[8 * nt + gi][8 * b + 2 * qi]);
+            const uint2 bk = *reinterpret_cast<const uint2*>(&sm.kg[8 * nt + gi][8 * b + 2 * qi]);
             const uint2 bq = *reinterpret_cast<const uint2*>(&sm.qg[8 * nt + gi][8 * b + 2 * qi]);
-            const uint32_t fw[2] = {bw.x, bw.y}, fq[2] = {bq.x, bq.y};
-            mma_tf32(dt[nt], a, fw);                 // Delta^T = U^T - S0^T W^T
-            mma_tf32(ot[nt], a, fq);                 // O^T = S0^T Q_g^T
+            const uint32_t fk[2] = {bk.x, bk.y}, fq[2] = {bq.x, bq.y};
+            mma_tf32(rt[nt], a, fk);
+            mma_tf32(ot[nt], a, fq);
         }
     }
+    __syncthreads();                                 // A and P are in shared memory
+
+    solve_delta<NT>(sm, rt, lane, qi);               // rt now holds Delta^T
     uint32_t ad[NT][4];                              // Delta^T as the A fragment (token-permuted k)
 #pragma unroll
     for (int kk = 0; kk < NT; ++kk) {
-        ad[kk][0] = to_tf32(dt[kk][0]); ad[kk][1] = to_tf32(dt[kk][2]);
-        ad[kk][2] = to_tf32(dt[kk][1]); ad[kk][3] = to_tf32(dt[kk][3]);
+        ad[kk][0] = to_tf32(rt[kk][0]); ad[kk][1] = to_tf32(rt[kk][2]);
+        ad[kk][2] = to_tf32(rt[kk][1]); ad[kk][3] = to_tf32(rt[kk][3]);
     }
+    // O^T += Delta^T P^T, then the output rows
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int kk = 0; kk < NT; ++kk) {
             const uint2 bp = *reinterpret_cast<const uint2*>(&sm.pm[8 * nt + gi][8 * kk + 2 * qi]);
             const uint32_t fp[2] = {bp.x, bp.y};
-            mma_tf32(ot[nt], ad[kk], fp);            // O^T += Delta^T P^T
+            mma_tf32(ot[nt], ad[kk], fp);
         }
         *reinterpret_cast<float2*>(&sm.os[8 * nt + 2 * qi][jc]) = make_float2(ot[nt][0], ot[nt][2]);
         *reinterpret_cast<float2*>(&sm.os[8 * nt + 2 * qi + 1][jc]) = make_float2(ot[nt][1], ot[nt][3]);
     }
+    // S^T = S0^T Diag(e^G) + Delta^T Kb
 #pragma unroll
-    for (int b = 0; b < 16; ++b) {                   // S^T = S0^T Diag(e^G) + Delta^T Kb
+    for (int b = 0; b < 16; ++b) {
         const float2 dc = *reinterpret_cast<const float2*>(&sm.dec[8 * b + 2 * qi]);
         float acc[4] = {s[b][0] * dc.x, s[b][2] * dc.y, s[b][1] * dc.x, s[b][3] * dc.y};
 #pragma unroll
@@ -353,102 +484,56 @@ template <typename Tin, int NT>
 __global__ void __launch_bounds__(kThreads, 2) decode_chunk_kernel(const Params<Tin> p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-    constexpr bool kTensor = sizeof(Tin) == 2;     // bf16 inputs: the tensor-core form
+    constexpr bool kTensor = sizeof(Tin) == 2;       // bf16 inputs: the chunk form
 
-    const size_t pair = blockIdx.x;                 // (sequence, head)
-    const size_t n = pair / p.H, h = pair % p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, qi = lane & 3;
-    const int jc = 16 * warp + 2 * gi;              // this lane's value columns jc, jc + 1
-    float* Sp = p.S + pair * kD * kD;
-    const int64_t n_state = (int64_t)gridDim.x * kD * kD;
-    const int64_t n_rows = (int64_t)gridDim.x * p.T;  // rows of q, k, v, out: num_seqs x T x H
-    const size_t row0 = n * (size_t)p.T * p.H + h;    // row of token 0; token t is row0 + t H
+    const int jc = 16 * warp + 2 * gi;               // this lane's value columns jc, jc + 1
+    const int64_t n_state = (int64_t)p.pairs * kD * kD;
+    const int64_t n_rows = (int64_t)p.pairs * p.T;   // rows of q, k, v, out: num_seqs x T x H
+    (void)n_state;                                   // read by the index checks of bounds-checked builds
 
-    // The state first, so its read overlaps everything up to the products.
-    // s[b][0..1] = S0[8b + 2qi][jc, jc+1], s[b][2..3] = S0[8b + 2qi + 1][jc, jc+1].
-    float s[16][4];
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-        const int i = 8 * b + 2 * qi;
-        const bool ok = KDA_INDEX_OK((int64_t)pair * kD * kD + (int64_t)(i + 1) * kD + jc + 1, n_state, p.status);
-        const float2 r0 = ok ? __ldcs(reinterpret_cast<const float2*>(Sp + (size_t)i * kD + jc)) : make_float2(0.f, 0.f);
-        const float2 r1 = ok ? __ldcs(reinterpret_cast<const float2*>(Sp + (size_t)(i + 1) * kD + jc))
-                             : make_float2(0.f, 0.f);
-        s[b][0] = r0.x; s[b][1] = r0.y; s[b][2] = r1.x; s[b][3] = r1.y;
-    }
-    (void)n_state;                                  // read by the index checks of bounds-checked builds
+    for (int pair = blockIdx.x; pair < p.pairs; pair += gridDim.x) {
+        const size_t n = (size_t)pair / p.H, h = (size_t)pair % p.H;
+        const size_t row0 = n * (size_t)p.T * p.H + h;   // row of token 0; token t is row0 + t H
+        float* Sp = p.S + (size_t)pair * kD * kD;
+        if (pair + (int)gridDim.x < p.pairs) prefetch_pair(p, pair + gridDim.x);
 
-    stage_tokens(sm, p, row0, n_rows);
-    __syncthreads();
+        float s[16][4];
+        load_state(Sp, s, (int64_t)pair * kD * kD, n_state, p.status, jc, qi);
+        stage_tokens(sm, p, row0, n_rows);
+        __syncthreads();
 
-    bool chunk_form = false;
-    if constexpr (kTensor) {
-        // ---- per key channel c: the cumulative decay g_t and whether the chunk form holds ----
-        constexpr int kT8 = 8 * NT;                  // token rows the products read
-        const int c = threadIdx.x & (kD - 1);
-        const bool kside = threadIdx.x < kD;
-        float gt[kT8];
-        float run = 0.f;
-#pragma unroll
-        for (int t = 0; t < kT8; ++t) { run += sm.g[t][c]; gt[t] = run; }
-        const float G = gt[kT8 - 1];                 // padded tokens add log alpha = 0
-        chunk_form = __syncthreads_and(G >= -kMaxExponent) != 0;   // false for NaN and -inf too
+        bool chunk_form = false;
+        if constexpr (kTensor) chunk_form = scale_rows<NT>(sm);
         if (chunk_form) {
-            if (kside) {
-#pragma unroll
-                for (int t = 0; t < kT8; ++t) {
-                    const float kv = sm.k[t][c];
-                    const float kb = __expf(G - gt[t]) * kv;
-                    sm.kb[t][c] = kb;
-                    sm.kbt[c][t] = tf32f(kb);
-                    sm.kg[t][c] = __expf(gt[t]) * kv;
-                    sm.k[t][c] = __expf(gt[t] - G) * kv;
-                }
-                sm.dec[c] = __expf(G);
-            } else {
-#pragma unroll
-                for (int t = 0; t < kT8; ++t) {
-                    const float qv = sm.q[t][c];
-                    sm.qg[t][c] = tf32f(__expf(gt[t]) * qv);
-                    sm.q[t][c] = __expf(gt[t] - G) * qv;
-                }
-            }
-            if (threadIdx.x < kTok * kTok / 8) {      // P above the diagonal stays 0
-                const int i = threadIdx.x * 8, t = i / kTok, s0 = i % kTok;
-                *reinterpret_cast<float4*>(&sm.pm[t][s0]) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(&sm.pm[t][s0 + 4]) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
             __syncthreads();
-            chunk_products<NT>(sm, s, p.T, warp, gi, qi, jc);
+            chunk_products<NT>(sm, s, warp, lane, gi, qi, jc);
+        } else {
+            token_loop(sm, s, p.T, warp, lane, qi, jc);
         }
+        store_state(Sp, s, (int64_t)pair * kD * kD, n_state, p.status, jc, qi);
+        __syncthreads();
+        store_outputs(sm, p, row0, n_rows);
     }
-    if (!chunk_form) {
-        token_loop(sm, s, p.T, warp, lane, qi, jc);
-    }
-
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-        const int i = 8 * b + 2 * qi;
-        if (KDA_INDEX_OK((int64_t)pair * kD * kD + (int64_t)(i + 1) * kD + jc + 1, n_state, p.status)) {
-            __stcs(reinterpret_cast<float2*>(Sp + (size_t)i * kD + jc), make_float2(s[b][0], s[b][1]));
-            __stcs(reinterpret_cast<float2*>(Sp + (size_t)(i + 1) * kD + jc), make_float2(s[b][2], s[b][3]));
-        }
-    }
-    __syncthreads();
-    store_outputs(sm, p, row0, n_rows);
 }
 
 template <typename Tin, int NT>
-cudaError_t launch_t(const Params<Tin>& p, unsigned blocks, cudaStream_t st) {
+cudaError_t launch_t(const Params<Tin>& p, cudaStream_t st) {
     static std::atomic<bool> attr_set[64];           // the shared-memory opt-in, once per device
+    static std::atomic<int> sm_count[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        const cudaError_t e = cudaFuncSetAttribute(decode_chunk_kernel<Tin, NT>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+        cudaError_t e = cudaFuncSetAttribute(decode_chunk_kernel<Tin, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+        int sms = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        sm_count[dev].store(sms > 0 ? sms : 1, std::memory_order_relaxed);
         attr_set[dev].store(true, std::memory_order_release);
     }
+    const int resident = 2 * sm_count[dev].load(std::memory_order_relaxed);   // two blocks an SM
+    const unsigned blocks = (unsigned)(p.pairs < resident ? p.pairs : resident);
     decode_chunk_kernel<Tin, NT><<<blocks, kThreads, sizeof(Smem), st>>>(p);
     return cudaGetLastError();
 }
@@ -457,7 +542,8 @@ template <typename Tin>
 Params<Tin> params(const DecodeArgs& a) {
     return Params<Tin>{static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v),
                        a.log_alpha, static_cast<const Tin*>(a.beta), a.state, static_cast<Tin*>(a.out),
-                       a.H, a.tokens_per_seq, static_cast<const Tin*>(a.gate), a.norm_w, a.norm_eps, a.status};
+                       a.num_seqs * a.H, a.H, a.tokens_per_seq, static_cast<const Tin*>(a.gate), a.norm_w,
+                       a.norm_eps, a.status};
 }
 
 }  // namespace
@@ -468,11 +554,10 @@ bool decode_chunk_supported(const DecodeArgs& a) {
 
 cudaError_t launch_decode_chunk(const DecodeArgs& a, cudaStream_t st) {
     if (a.num_seqs == 0) return cudaSuccess;
-    if (!decode_chunk_supported(a)) return cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)((size_t)a.num_seqs * a.H);
-    if (a.dtype == DType::F32) return launch_t<float, 2>(params<float>(a), blocks, st);
-    return a.tokens_per_seq <= 8 ? launch_t<__nv_bfloat16, 1>(params<__nv_bfloat16>(a), blocks, st)
-                                 : launch_t<__nv_bfloat16, 2>(params<__nv_bfloat16>(a), blocks, st);
+    if (!decode_chunk_supported(a) || (int64_t)a.num_seqs * a.H > INT32_MAX / 2) return cudaErrorInvalidValue;
+    if (a.dtype == DType::F32) return launch_t<float, 2>(params<float>(a), st);
+    return a.tokens_per_seq <= 8 ? launch_t<__nv_bfloat16, 1>(params<__nv_bfloat16>(a), st)
+                                 : launch_t<__nv_bfloat16, 2>(params<__nv_bfloat16>(a), st);
 }
 
 }  // namespace kda

@@ -87,15 +87,18 @@ def test_reference_arm_prints_one_json_line():
 
 def test_multi_token_decode_roofs():
     import bench
-    # one token: the state traffic dominates, the line is HBM-bound
+    # one token: the plain decode kernel; the state traffic dominates, the line is HBM-bound
     e1 = bench._multi_decode_entry(1, 160e-6, 1, 6767.4)
-    assert e1["bound"] == "hbm" and e1["frac"] == e1["frac_hbm"] > e1["frac_alu"]
+    assert e1["bound"] == "hbm" and e1["frac"] == e1["frac_hbm"]
     assert e1["algorithmic_bytes_per_launch"] == bench.decode_bytes(bench.DEC_N, bench.H)
-    # the two roofs meet near 16 tokens; far beyond, arithmetic binds
+    assert e1["kernels"] == ["decode_kernel"]
+    # several tokens: the chunk form; its state products (W S0, Q_g S0, Kb^T Delta: 6 T D^2 flop
+    # per head) are tensor-core work, HBM stays the bound
     e16 = bench._multi_decode_entry(16, 500e-6, 1, 6767.4)
-    assert abs(e16["frac_hbm"] - e16["frac_alu"]) / e16["frac_hbm"] < 0.05
-    e64 = bench._multi_decode_entry(64, 2e-3, 1, 6767.4)
-    assert e64["bound"] == "alu" and e64["frac"] == e64["frac_alu"]
-    # flops: decay D^2 + three D^2 multiply-adds per token-head
+    assert e16["bound"] == "hbm" and e16["kernels"] == ["decode_chunk_kernel"]
+    assert e16["tensor_flops_per_launch"] == bench.DEC_N * bench.H * 6 * 16 * bench.D * bench.D
+    # the token-by-token flops for comparison: decay D^2 + three D^2 multiply-adds per token-head
     assert bench.DECODE_FLOP_PER_TOKEN_HEAD == 7 * bench.D * bench.D
-    assert e16["flops_per_launch"] == bench.DEC_N * 16 * bench.H * 7 * bench.D * bench.D
+    assert e16["token_loop_flops_per_launch"] == bench.DEC_N * 16 * bench.H * 7 * bench.D * bench.D
+    nbytes = bench.decode_bytes(bench.DEC_N, bench.H, 16)
+    assert abs(e16["frac"] - nbytes / (6767.4e9 * 500e-6)) < 1e-12
