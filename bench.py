@@ -150,7 +150,7 @@ def source_digest():
     only while it matches the kernel that is running."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("kda_chunk_tc.cu", "sm103_primitives.cuh"):
+    for f in ("kda_chunk_tc.cu", "kda_chunk_common.cuh", "sm103_primitives.cuh"):
         with open(os.path.join(ROOT, "linear_attention_06_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -196,6 +196,36 @@ def oracle_sample(budget_s, threads=0):
         return time.perf_counter() - t0
 
     return run, nseq, cores, used
+
+
+def gpu_numa_node(dev_index):
+    """NUMA node of the host memory nearest the GPU (its PCI function's node), or None."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            node = int(f.read().strip())
+        return node if node >= 0 else None
+    except (AttributeError, OSError, ValueError):
+        return None
+
+
+def node_cpus(node):
+    """CPU ids of a NUMA node from sysfs ("0-3,8-11" ranges), or None."""
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            text = f.read().strip()
+    except OSError:
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus or None
 
 
 class Ranks:
@@ -431,11 +461,20 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         keys = ("q", "k", "v", "log_alpha", "beta")
+        # the pinned host buffers are first touched by a thread on the GPU's NUMA node, so their
+        # pages live in the host memory nearest the GPU; the affinity is restored afterwards
+        numa = gpu_numa_node(dev.index if dev.index is not None else 0)
+        cpus = node_cpus(numa) if numa is not None else None
+        old_aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+        if cpus and old_aff is not None and cpus & old_aff:
+            os.sched_setaffinity(0, cpus & old_aff)
         host = {k: getattr(w, k).cpu().pin_memory() for k in keys}
+        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory().zero_() for _ in range(2)]
+        hfin = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory().zero_() for _ in range(2)]
+        if old_aff is not None:
+            os.sched_setaffinity(0, old_aff)
         dbuf = [{k: torch.empty_like(getattr(w, k)) for k in keys} for _ in range(2)]
         obuf = [(torch.empty_like(out), torch.empty_like(fin)) for _ in range(2)]
-        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        hfin = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = hout[0].numel() * hout[0].element_size() + hfin[0].numel() * hfin[0].element_size()
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -481,8 +520,37 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         t_e2e = max_over_ranks(ev0.elapsed_time(ev1) * 1e-3 / args.steps)
+
+        # each leg alone (same pinned buffers, one stream at a time): the pipelined step can be
+        # no faster than the slowest of the three
+        def alone(s, fn, reps=5):
+            with torch.cuda.stream(s):
+                fn()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                for _ in range(reps):
+                    fn()
+                b.record(s)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e-3 / reps
+
+        def copy_in():
+            for k in keys:
+                dbuf[0][k].copy_(host[k], non_blocking=True)
+
+        def copy_out():
+            hout[0].copy_(obuf[0][0], non_blocking=True)
+            hfin[0].copy_(obuf[0][1], non_blocking=True)
+
+        t_in, t_out = alone(s_in, copy_in), alone(s_out, copy_out)
+        bound = max(t_in, t_out, t_prefill)
         e2e = {"value": world * B * T / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+               "copy_in_ms": t_in * 1e3, "kernel_ms": t_prefill * 1e3, "copy_out_ms": t_out * 1e3,
+               "h2d_gbs_alone": h2d / t_in / 1e9, "d2h_gbs_alone": d2h / t_out / 1e9,
+               "slowest_leg_ms": bound * 1e3, "ms_over_slowest_leg": t_e2e / bound,
+               "host_numa_node": numa,
                "pipelining": "copy-in / compute / copy-out on three streams, two buffer sets"}
 
     if rank != 0:
@@ -591,6 +659,44 @@ def run_ours(args):
     ranks.close()
 
 
+PROFILE_CASES = ("prefill", "decode_chunk_T16", "decode_chunk_T4", "split_T32768")
+
+
+def run_profile_case(name):
+    """Three calls of one kernel family on its bench workload (or, for the split prefill, a
+    32768-token sequence: inputs above L2, a few GB at most), for an ncu capture of one launch
+    (-s 2 -c 1 after the two warm-up calls).  Prints one line."""
+    import torch
+    import linear_attention_06_gb300 as kda
+    from linear_attention_06_gb300 import workloads
+    dev = torch.device("cuda", 0)
+    if name == "prefill":
+        w = workloads.prefill_bf16(device=dev)
+        out, fin = torch.empty_like(w.v), torch.empty((B, H, D, D), dtype=torch.float32, device=dev)
+        cu = w.cu_seqlens.to(dev)
+        call = lambda: kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, None, cu, out, fin)
+    elif name.startswith("decode_chunk_T"):
+        tm = int(name[len("decode_chunk_T"):])
+        w = workloads.make_inputs(DEC_N * tm, H, D, D, dtype=torch.bfloat16, seed=13 + tm,
+                                  cu_seqlens=[tm * i for i in range(DEC_N + 1)], state_std=0.05, device=dev)
+        S, out = w.initial_state.clone(), torch.empty_like(w.v)
+        call = lambda: kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S, out)
+    elif name == "split_T32768":
+        tl = 32768
+        w = workloads.make_inputs(tl, H, D, D, dtype=torch.bfloat16, seed=3, cu_seqlens=[0, tl], device=dev)
+        cu = torch.tensor([0, tl], dtype=torch.int32, device=dev)
+        out, fin = torch.empty_like(w.v), torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(kda.kda_prefill_split_workspace_size(tl, 1, H), dtype=torch.uint8, device=dev)
+        call = lambda: kda.kda_prefill_split(w.q, w.k, w.v, w.log_alpha, w.beta, None, cu, out=out,
+                                             final_state=fin, workspace=ws)
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    print(f"profile case {name}: 3 calls", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -603,7 +709,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-step-budget", type=float, default=4.0,
                     help="seconds of oracle work per step in --impl reference")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="only run three calls of one kernel family (for an ncu capture) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

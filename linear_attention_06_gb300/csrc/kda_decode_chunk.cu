@@ -43,9 +43,10 @@
 // rows; A and P (2 NT warps) and the first pass over the state (every warp); then per warp the
 // solve, the output and the state update.
 //
-// fp32 inputs always take the fp32 token loop (decay, the two column sums over the warp's own
-// rows, the rank-one update), so they keep fp32 accuracy; in it a warp needs no other warp
-// until the output store.
+// The token loop (decay, the two column sums over the warp's own rows, the rank-one update) is
+// exact fp32 arithmetic; in it a warp needs no other warp until the output store.  Inputs in
+// fp32 do not come here: they keep the one-token kernel's token loop, which is as fast for them
+// and gives the same bits as T one-token steps.
 //
 // Blocks are persistent, two per SM (81 KB of shared memory and at most 128 registers a thread
 // each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
@@ -108,13 +109,10 @@ __device__ __forceinline__ void store8(float* s, const float (&x)[8]) {
     reinterpret_cast<float4*>(s)[0] = make_float4(x[0], x[1], x[2], x[3]);
     reinterpret_cast<float4*>(s)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
-__device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void store4(float* p, float4 o) { *reinterpret_cast<float4*>(p) = o; }
 __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 o) {
     *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(o.x, o.y), pack_bf16x2(o.z, o.w));
 }
-__device__ __forceinline__ float4 load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
@@ -484,7 +482,6 @@ template <typename Tin, int NT>
 __global__ void __launch_bounds__(kThreads, 2) decode_chunk_kernel(const Params<Tin> p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-    constexpr bool kTensor = sizeof(Tin) == 2;       // bf16 inputs: the chunk form
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, qi = lane & 3;
     const int jc = 16 * warp + 2 * gi;               // this lane's value columns jc, jc + 1
@@ -503,8 +500,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_chunk_kernel(const Params<
         stage_tokens(sm, p, row0, n_rows);
         __syncthreads();
 
-        bool chunk_form = false;
-        if constexpr (kTensor) chunk_form = scale_rows<NT>(sm);
+        const bool chunk_form = scale_rows<NT>(sm);
         if (chunk_form) {
             __syncthreads();
             chunk_products<NT>(sm, s, warp, lane, gi, qi, jc);
@@ -549,13 +545,12 @@ Params<Tin> params(const DecodeArgs& a) {
 }  // namespace
 
 bool decode_chunk_supported(const DecodeArgs& a) {
-    return a.dk == kD && a.dv == kD && a.tokens_per_seq >= 2 && a.tokens_per_seq <= kTok;
+    return a.dtype == DType::BF16 && a.dk == kD && a.dv == kD && a.tokens_per_seq >= 2 && a.tokens_per_seq <= kTok;
 }
 
 cudaError_t launch_decode_chunk(const DecodeArgs& a, cudaStream_t st) {
     if (a.num_seqs == 0) return cudaSuccess;
     if (!decode_chunk_supported(a) || (int64_t)a.num_seqs * a.H > INT32_MAX / 2) return cudaErrorInvalidValue;
-    if (a.dtype == DType::F32) return launch_t<float, 2>(params<float>(a), st);
     return a.tokens_per_seq <= 8 ? launch_t<__nv_bfloat16, 1>(params<__nv_bfloat16>(a), st)
                                  : launch_t<__nv_bfloat16, 2>(params<__nv_bfloat16>(a), st);
 }

@@ -88,7 +88,8 @@ def main() -> int:
             kda.kda_decode_step_gated(d.q, d.k, d.v, d.log_alpha, d.beta, g.g_raw, g.norm_weight, S)
             check(f"gated decode T={T} dk={dk} dv={dv}")
 
-    # multi-token decode: the fp32 token loop, and bf16 steps whose decay sends them token by token
+    # multi-token decode: fp32 (the one-token kernel's loop), and bf16 steps whose decay sends them
+    # token by token
     for T in (5, 16):
         n = 9
         c = [T * i for i in range(n + 1)]

@@ -235,9 +235,9 @@ def test_device_status_is_clean():
 
 
 # ---- multi-token decode (T tokens per sequence through the decode path) -------------
-# At dk = dv = 128 a step of 2..16 tokens takes the chunk form (bf16: tensor cores, T <= 8
-# and T <= 16 instances) or the fp32 token loop (fp32 inputs, and any step whose decay over the
-# step passes e^-60 in some channel); other head sizes keep the token loop of the one-token step.
+# At dk = dv = 128 a bf16 step of 2..16 tokens takes the chunk form (tensor cores, T <= 8 and
+# T <= 16 instances), or its fp32 token loop when the decay over the step passes e^-60 in some
+# channel; fp32 inputs and other head sizes keep the token loop of the one-token kernel.
 @pytest.mark.parametrize("T", [2, 5, 8, 9, 16])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_decode_multi_token_matches_oracle(T, dtype):
@@ -284,8 +284,9 @@ def test_decode_multi_token_strong_decay_mixed_with_chunk_form():
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_decode_multi_token_agrees_with_repeated_single_steps(dtype):
-    # the chunk form and the fp32 token loop are exact rewrites of T one-token steps, not the
-    # same sequence of roundings: they agree within the tolerance of the dtype
+    # the chunk form (bf16) is an exact rewrite of T one-token steps, not the same sequence of
+    # roundings: it agrees within the tolerance of the dtype; fp32 runs the one-token kernel's
+    # loop T times and gives the same bits
     n, T, H = 16, 7, 4
     cu = [T * i for i in range(n + 1)]
     w = workloads.make_inputs(n * T, H, 128, 128, dtype=dtype, seed=40, cu_seqlens=cu, state_std=0.05).to(DEV)
@@ -301,6 +302,8 @@ def test_decode_multi_token_agrees_with_repeated_single_steps(dtype):
     torch.cuda.synchronize()
     assert rel_l2(np64(out_multi), np64(outs)) < TOL[dtype]
     assert rel_l2(np64(S_multi), np64(S_step)) < TOL[dtype]
+    if dtype == torch.float32:
+        assert torch.equal(out_multi, outs) and torch.equal(S_multi, S_step)
 
 
 def test_decode_multi_token_zero_beta_is_pure_decay():
