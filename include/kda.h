@@ -169,7 +169,13 @@ kda_status kda_prefill_gated(const kda_shape* shape, const void* q, const void* 
  * work that does not depend on the state entering a chunk (the decayed factors, the
  * Gram products, the UT solve and the WY factors W' and U) first runs for every chunk
  * of every head at once, leaving one record per chunk in `workspace`; a second kernel
- * per (sequence, head) then carries the state through the records in order.
+ * per (sequence, head) then carries the state through the records in order.  A single
+ * sequence of at least 16384 tokens (with at most 64 heads) runs in segments of 8192
+ * tokens: the chunk records of segment s + 1 are built, on an internal second stream and
+ * on the SMs the state chains leave free, while the chains of segment s run on `stream`;
+ * the chains carry the fp32 state from segment to segment, so the results are those of
+ * one pass.  The call's work on the second stream is ordered after `stream`'s earlier
+ * work and before its later work; calls from several host threads serialise on it.
  *
  * All arguments but the workspace are those of kda_prefill, with the same results
  * (the same arithmetic in a different order of kernels; within the tolerances of the
@@ -190,9 +196,11 @@ kda_status kda_prefill_split(const kda_shape* shape, const void* q, const void* 
 /*
  * kda_prefill_split_workspace_size -- bytes of workspace kda_prefill_split needs for
  * `shape`: H * (ceil(T / 64) + N) chunk records of 96 KB plus a 4-byte mode word each
- * (about 1.5 KB per token and head).  Depends on the shape only, not on the sequence
- * lengths.  Writes *bytes; KDA_ERR_INVALID_ARG for a NULL pointer, otherwise the shape
- * errors of kda_prefill.  No CUDA call.
+ * (about 1.5 KB per token and head); for a single sequence run in segments (see
+ * kda_prefill_split) the records of two segments, H * 129 each, plus two fp32 states per
+ * head, whatever the length.  Depends on the shape only, not on the sequence lengths.
+ * Writes *bytes; KDA_ERR_INVALID_ARG for a NULL pointer, otherwise the shape errors of
+ * kda_prefill.  No CUDA call.
  */
 kda_status kda_prefill_split_workspace_size(const kda_shape* shape, size_t* bytes);
 

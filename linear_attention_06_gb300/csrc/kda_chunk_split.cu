@@ -28,6 +28,7 @@
 // slot floor(bos_n / 64) + n, so a head needs ceil(T / 64) + N slots whatever the
 // lengths (kda_prefill_split_workspace_size).
 #include <atomic>
+#include <mutex>
 
 #include "kda_chunk_common.cuh"
 
@@ -943,9 +944,146 @@ bool make_input_maps(Maps* maps, const PrefillArgs& a) {
 int record_slots(int64_t T, int num_seqs) { return (int)((T + C - 1) / C) + num_seqs; }
 size_t modes_bytes(int64_t slots) { return (size_t)((slots * 4 + 1023) / 1024) * 1024; }
 
+// A long single sequence is run in time segments of kSegTokens: the chunk-local kernel of
+// segment s + 1 (on a second stream, on the SMs the chains leave free) runs while the state
+// chains of segment s run, the chains carrying the fp32 state from segment to segment through
+// a workspace buffer.  Records then need room for two segments only.
+constexpr int64_t kSegTokens = 8192;
+bool segmented(int64_t T, int num_seqs, int H) { return num_seqs == 1 && H <= 64 && T >= 2 * kSegTokens; }
+size_t carry_bytes(int H) { return (size_t)H * D * D * sizeof(float); }
+size_t seg_buffer_bytes(int H) {
+    const int64_t slots = (int64_t)H * record_slots(kSegTokens, 1);
+    return modes_bytes(slots) + (size_t)slots * kRecBytes;
+}
+
+bool configure_kernels(int* sms) {
+    static std::atomic<bool> attr_set[64];
+    static std::atomic<int> sm_count[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kLocalSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kChainSmem);
+        int n = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return false;
+        sm_count[dev].store(n > 0 ? n : 1, std::memory_order_relaxed);
+        attr_set[dev].store(true, std::memory_order_release);
+    }
+    *sms = sm_count[dev].load(std::memory_order_relaxed);
+    return true;
+}
+
+// One chunk-local pass over all (head, record slot) items of a, spread over `grid` CTAs, and
+// the state chains of a (one CTA per (sequence, head)), each on its own stream.
+cudaError_t enqueue_local(const PrefillArgs& a, void* buf, int grid, cudaStream_t s) {
+    Maps maps;
+    if (!make_input_maps(&maps, a)) return cudaErrorInvalidValue;
+    const int R = record_slots(a.total_tokens, a.num_seqs);
+    const int64_t slots = (int64_t)a.H * R;
+    Workspace ws;
+    ws.R = R;
+    ws.modes = static_cast<int*>(buf);
+    ws.recs = static_cast<uint8_t*>(buf) + modes_bytes(slots);
+    RecMaps rm;
+    if (!make_rec_maps(&rm, ws.recs, slots)) return cudaErrorInvalidValue;
+    const int64_t per = (slots + grid - 1) / grid;
+    const int g = (int)((slots + per - 1) / per);
+    chunk_local_kernel<<<g, kLocalThreads, kLocalSmem, s>>>(maps, rm, static_cast<const __nv_bfloat16*>(a.beta),
+                                                           a.cu_seqlens, a.total_tokens, a.num_seqs, a.H, ws,
+                                                           (int)per, a.status);
+    return cudaGetLastError();
+}
+cudaError_t enqueue_chain(const PrefillArgs& a, void* buf, cudaStream_t s) {
+    Maps maps;
+    if (!make_input_maps(&maps, a)) return cudaErrorInvalidValue;
+    const int R = record_slots(a.total_tokens, a.num_seqs);
+    const int64_t slots = (int64_t)a.H * R;
+    Workspace ws;
+    ws.R = R;
+    ws.modes = static_cast<int*>(buf);
+    ws.recs = static_cast<uint8_t*>(buf) + modes_bytes(slots);
+    RecMaps rm;
+    if (!make_rec_maps(&rm, ws.recs, slots)) return cudaErrorInvalidValue;
+    chunk_chain_kernel<<<(unsigned)((int64_t)a.num_seqs * a.H), kChainThreads, kChainSmem, s>>>(
+        maps, rm, static_cast<const __nv_bfloat16*>(a.beta), a.initial_state, a.cu_seqlens,
+        static_cast<__nv_bfloat16*>(a.out), a.final_state, a.total_tokens, a.num_seqs, a.H, ws, a.status,
+        a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
+    return cudaGetLastError();
+}
+
+// The second stream and the events of the segmented run, one set per device, created on
+// first use and kept.  The mutex keeps one call's enqueue sequence together, so the events'
+// latest records are that call's (calls from several host threads serialise on the second
+// stream).
+struct SegResources {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t fork = nullptr, local_done[2] = {}, chain_done[2] = {};
+};
+SegResources& seg_resources(int dev) {
+    static SegResources r[64];
+    return r[dev];
+}
+
+cudaError_t launch_segmented(const PrefillArgs& a, void* workspace, int sms, cudaStream_t s) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SegResources& r = seg_resources(dev);
+    std::lock_guard<std::mutex> lock(r.mu);
+    if (!r.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&r.aux, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.fork, cudaEventDisableTiming);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = cudaEventCreateWithFlags(&r.local_done[b], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&r.chain_done[b], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return e;
+        r.ready = true;
+    }
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    float* carry[2] = {reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + carry_bytes(a.H))};
+    uint8_t* bufs[2] = {base + 2 * carry_bytes(a.H), base + 2 * carry_bytes(a.H) + seg_buffer_bytes(a.H)};
+    const int pairs = a.H;                            // one sequence
+    const int local_grid = sms - pairs >= sms / 2 ? sms - pairs : sms / 2;
+    const int64_t nseg = (a.total_tokens + kSegTokens - 1) / kSegTokens;
+    const size_t row = (size_t)a.H * D;               // elements of one token row of q, k, v, out
+    cudaError_t e = cudaEventRecord(r.fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(r.aux, r.fork, 0);
+    for (int64_t sg = 0; sg < nseg && e == cudaSuccess; ++sg) {
+        const int b = (int)(sg & 1);
+        const int64_t t0 = sg * kSegTokens;
+        PrefillArgs g = a;
+        g.total_tokens = (a.total_tokens - t0 < kSegTokens) ? a.total_tokens - t0 : kSegTokens;
+        g.q = static_cast<const __nv_bfloat16*>(a.q) + t0 * row;
+        g.k = static_cast<const __nv_bfloat16*>(a.k) + t0 * row;
+        g.v = static_cast<const __nv_bfloat16*>(a.v) + t0 * row;
+        g.log_alpha = a.log_alpha + t0 * row;
+        g.beta = static_cast<const __nv_bfloat16*>(a.beta) + t0 * a.H;
+        g.out = static_cast<__nv_bfloat16*>(a.out) + t0 * row;
+        g.cu_seqlens = nullptr;
+        g.initial_state = sg == 0 ? a.initial_state : carry[b ^ 1];
+        g.final_state = sg == nseg - 1 ? a.final_state : carry[b];
+        // the records of buffer b are free once the chains of segment sg - 2 have read them
+        if (sg >= 2) e = cudaStreamWaitEvent(r.aux, r.chain_done[b], 0);
+        if (e == cudaSuccess) e = enqueue_local(g, bufs[b], sg == 0 ? sms : local_grid, r.aux);
+        if (e == cudaSuccess) e = cudaEventRecord(r.local_done[b], r.aux);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, r.local_done[b], 0);
+        if (e == cudaSuccess) e = enqueue_chain(g, bufs[b], s);
+        if (e == cudaSuccess) e = cudaEventRecord(r.chain_done[b], s);
+    }
+    // every operation on the second stream precedes the last chain launch on s
+    return e;
+}
+
 }  // namespace
 
 size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H) {
+    if (segmented(total_tokens, num_seqs, H)) return 2 * carry_bytes(H) + 2 * seg_buffer_bytes(H);
     const int64_t slots = (int64_t)H * record_slots(total_tokens, num_seqs);
     return modes_bytes(slots) + (size_t)slots * kRecBytes;
 }
@@ -955,41 +1093,12 @@ bool split_supported(const PrefillArgs& a) {
 }
 
 cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s) {
-    Maps maps;
-    if (!make_input_maps(&maps, a)) return cudaErrorInvalidValue;
-    const int R = record_slots(a.total_tokens, a.num_seqs);
-    const int64_t slots = (int64_t)a.H * R;
-    Workspace ws;
-    ws.R = R;
-    ws.modes = static_cast<int*>(workspace);
-    ws.recs = static_cast<uint8_t*>(workspace) + modes_bytes(slots);
-    RecMaps rm;
-    if (!make_rec_maps(&rm, ws.recs, slots)) return cudaErrorInvalidValue;
-    static std::atomic<bool> attr_set[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_set[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kLocalSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kChainSmem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev].store(true, std::memory_order_release);
-    }
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
-    const int64_t per = (slots + sms - 1) / sms;
-    const int grid = (int)((slots + per - 1) / per);
-    const __nv_bfloat16* beta = static_cast<const __nv_bfloat16*>(a.beta);
-    chunk_local_kernel<<<grid, kLocalThreads, kLocalSmem, s>>>(maps, rm, beta, a.cu_seqlens, a.total_tokens,
-                                                              a.num_seqs, a.H, ws, (int)per, a.status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    chunk_chain_kernel<<<(unsigned)((int64_t)a.num_seqs * a.H), kChainThreads, kChainSmem, s>>>(
-        maps, rm, beta, a.initial_state, a.cu_seqlens, static_cast<__nv_bfloat16*>(a.out), a.final_state,
-        a.total_tokens, a.num_seqs, a.H, ws, a.status, a.ckpt_cu, a.ckpt_pos, a.ckpt_states);
-    return cudaGetLastError();
+    int sms = 1;
+    if (!configure_kernels(&sms)) return cudaErrorInvalidDevice;
+    if (segmented(a.total_tokens, a.num_seqs, a.H) && !a.ckpt_cu) return launch_segmented(a, workspace, sms, s);
+    cudaError_t e = enqueue_local(a, workspace, sms, s);
+    if (e == cudaSuccess) e = enqueue_chain(a, workspace, s);
+    return e;
 }
 
 }  // namespace kda

@@ -214,8 +214,16 @@ def test_split_workspace_size_depends_on_the_shape_only(L):
         assert L.kda_prefill_split_workspace_size(ctypes.byref(shape(n=n, T=T, H=H)), ctypes.byref(b)) == 0
         return b.value
     rec = 12 * 8192
-    slots = 32 * ((131072 + 63) // 64 + 1)
-    assert size(1, 131072, 32) == (slots * 4 + 1023) // 1024 * 1024 + slots * rec
+    # one long sequence runs in segments of 8192 tokens: two carried fp32 states per head and
+    # the records of two segments (8192 / 64 + 1 slots a head each)
+    seg_slots = 32 * (8192 // 64 + 1)
+    seg_buf = (seg_slots * 4 + 1023) // 1024 * 1024 + seg_slots * rec
+    assert size(1, 131072, 32) == 2 * 32 * 128 * 128 * 4 + 2 * seg_buf
+    assert size(1, 10 ** 7, 32) == size(1, 131072, 32)           # independent of the length
+    slots = 32 * ((16383 + 63) // 64 + 1)                         # below two segments: one pass
+    assert size(1, 16383, 32) == (slots * 4 + 1023) // 1024 * 1024 + slots * rec
+    slots = 32 * ((131072 + 63) // 64 + 2)                         # two sequences: one pass
+    assert size(2, 131072, 32) == (slots * 4 + 1023) // 1024 * 1024 + slots * rec
     assert size(3, 100, 2) == 1024 + 2 * (2 + 3) * rec          # ceil(100/64) + 3 slots a head
     assert size(0, 0, 4) == 0
     assert L.kda_prefill_split_workspace_size(ctypes.byref(shape()), None) == _lib.KDA_ERR_INVALID_ARG

@@ -125,6 +125,29 @@ def test_split_long_prefill_sampled_heads_and_resume():
     assert torch.equal(torch.cat([o1, o2]), out) and torch.equal(s2, fin)
 
 
+@pytest.mark.parametrize("T", [16384, 20000, 24577])
+def test_split_segmented_single_sequence(T):
+    # one sequence of at least 16384 tokens runs in 8192-token segments (chunk records of the
+    # next segment built while the chains run), the fp32 state carried between segments: a
+    # ragged last segment, an initial state, and agreement with the fused prefill and the oracle
+    w = workloads.make_inputs(T, 4, 128, 128, seed=108 + T % 97, cu_seqlens=[0, T], state_std=0.05).to(DEV)
+    out, fin = check(w, heads=[1])
+    o_f, f_f = gpu_prefill(w)
+    assert rel_l2(np64(out), np64(o_f)) < 1e-3 and rel_l2(np64(fin), np64(f_f)) < 1e-4
+    assert kda.kda_device_status() == 0
+
+
+def test_split_segmented_results_do_not_depend_on_the_workspace_contents():
+    T = 17000
+    w = workloads.make_inputs(T, 2, 128, 128, seed=109, cu_seqlens=[0, T], state_std=0.05).to(DEV)
+    need = kda.kda_prefill_split_workspace_size(T, 1, 2)
+    ws = torch.full((need,), 0x5A, dtype=torch.uint8, device=DEV)
+    o1, f1 = split_prefill(w, workspace=ws)
+    ws.fill_(0xC3)
+    o2, f2 = split_prefill(w, workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
 def test_split_varlen_full_size_sampled_heads():
     w = workloads.varlen_prefill(device=DEV)
     check(w, heads=[0, 31])
