@@ -627,8 +627,10 @@ def run_ours(args):
                                    "algorithmic_bytes_per_launch": lbytes,
                                    "workspace_bytes": layer["long_split_ws"],
                                    "kernels": ["chunk_local_kernel", "chunk_chain_kernel"],
-                                   "note": "kda_prefill_split: per-chunk records of every head first (all SMs), "
-                                           "then one state chain per head; bytes counted as for the fused kernel "
+                                   "note": "kda_prefill_split: the sequence in 8192-token segments; each segment's "
+                                           "per-chunk records of every head (on the SMs the chains leave free, "
+                                           "overlapping the previous segment's chains), then one state chain per "
+                                           "head carrying the fp32 state on; bytes counted as for the fused kernel "
                                            "(the records' round trip through HBM is not in the algorithmic bytes)"},
             "long_prefill_resumed": {"workload": f"kda_prefill_bf16_B1_H{H}_T{lt}_d{D}_resume_at_{lt // 2}",
                                      "ms_per_step": layer["t_resume"] * 1e3,
