@@ -56,6 +56,22 @@ def main() -> int:
     kda.kda_prefill(w.q, w.k, w.v, w.log_alpha, w.beta, w.initial_state,
                     torch.tensor(cu, dtype=torch.int32, device=dev), final_state=True)
     check("prefill, token-by-token chunks")
+    # the split prefill: ragged sequences in one pass, a token-by-token chunk among them, and one
+    # long sequence run in segments (the chunk-local pass of the next segment overlapping the chains)
+    w = workloads.make_inputs(cu[-1], 3, 128, 128, seed=10, cu_seqlens=cu, state_std=0.05).to(dev)
+    w.log_alpha[70:72].mul_(400.0)
+    kda.kda_prefill_split(w.q, w.k, w.v, w.log_alpha, w.beta, w.initial_state,
+                          torch.tensor(cu, dtype=torch.int32, device=dev), final_state=True)
+    check("split prefill, ragged")
+    ws_ = workloads.make_inputs(17000, 2, 128, 128, seed=11, cu_seqlens=[0, 17000], state_std=0.05).to(dev)
+    kda.kda_prefill_split(ws_.q, ws_.k, ws_.v, ws_.log_alpha, ws_.beta, ws_.initial_state,
+                          torch.tensor([0, 17000], dtype=torch.int32, device=dev), final_state=True)
+    check("split prefill, one sequence in segments")
+    # the front end fused into the prefill (ragged sequences, halo rows at sequence starts)
+    x = workloads.make_layer_inputs(cu[-1], 3, 128, 128, W=4, seed=12, cu_seqlens=cu).to(dev)
+    kda.kda_prefill_frontend(x.q_raw, x.k_raw, x.v_raw, x.a_raw, x.b_raw, x.conv_q, x.conv_k, x.conv_v,
+                             cu_seqlens=cu, final_state=True)
+    check("prefill with the front end fused")
     wd = workloads.make_inputs(4 * 128, 2, 128, 128, seed=9, num_seqs=4).to(dev)
     kda.kda_prefill(wd.q, wd.k, wd.v, wd.log_alpha, wd.beta, None, None, final_state=True, num_seqs=4)
     check("prefill, dense batch without cu_seqlens")
