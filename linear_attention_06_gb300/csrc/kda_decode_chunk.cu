@@ -48,7 +48,7 @@
 // fp32 do not come here: they keep the one-token kernel's token loop, which is as fast for them
 // and gives the same bits as T one-token steps.
 //
-// Blocks are persistent, two per SM (81 KB of shared memory and at most 128 registers a thread
+// Blocks are persistent, two per SM (83 KiB of shared memory and at most 128 registers a thread
 // each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
 // the state and token rows of its next pair into L2 when it starts a pair, so that their DRAM
 // reads overlap its arithmetic.
@@ -70,9 +70,9 @@ constexpr int kTok = 16;                // tokens per step, padded with zero tok
 constexpr float kMaxExponent = 60.f;    // chunk form while every channel has G >= -60
 constexpr float kLog2e = 1.4426950408889634f;
 // Row strides (floats).  136 = 8 (mod 32) and 24: fragments read as pairs by eight rows gi at
-// column 2qi; 132 = 4 (mod 32): the accumulator pairs of V and O (rows 2qi, columns 2gi) and the
-// rows of A read as float4 by the solve.  Each leaves the warp's shared-memory loads without
-// bank conflicts.
+// column 2qi; 132 = 4 (mod 32): the accumulator pairs of V and O (rows 2qi, columns 2gi); 20: the
+// rows 2qi (+1) of A read as float4 by the solve.  Each leaves the warp's shared-memory loads
+// without bank conflicts.
 constexpr int kLd = 132, kLdB = 136, kLdT = 24, kLdA = 20;
 
 struct Smem {
