@@ -1082,8 +1082,8 @@ cudaError_t launch_segmented(const PrefillArgs& a, void* workspace, int sms, cud
 
 }  // namespace
 
-size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H) {
-    if (segmented(total_tokens, num_seqs, H)) return 2 * carry_bytes(H) + 2 * seg_buffer_bytes(H);
+size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H, bool segments) {
+    if (segments && segmented(total_tokens, num_seqs, H)) return 2 * carry_bytes(H) + 2 * seg_buffer_bytes(H);
     const int64_t slots = (int64_t)H * record_slots(total_tokens, num_seqs);
     return modes_bytes(slots) + (size_t)slots * kRecBytes;
 }
@@ -1092,10 +1092,11 @@ bool split_supported(const PrefillArgs& a) {
     return a.dtype == DType::BF16 && a.dk == D && a.dv == D && a.total_tokens > 0 && encode_fn() != nullptr;
 }
 
-cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s) {
+cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s, bool segments) {
     int sms = 1;
     if (!configure_kernels(&sms)) return cudaErrorInvalidDevice;
-    if (segmented(a.total_tokens, a.num_seqs, a.H) && !a.ckpt_cu) return launch_segmented(a, workspace, sms, s);
+    if (segments && segmented(a.total_tokens, a.num_seqs, a.H) && !a.ckpt_cu)
+        return launch_segmented(a, workspace, sms, s);
     cudaError_t e = enqueue_local(a, workspace, sms, s);
     if (e == cudaSuccess) e = enqueue_chain(a, workspace, s);
     return e;

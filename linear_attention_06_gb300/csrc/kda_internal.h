@@ -99,8 +99,10 @@ cudaError_t launch_chunk_tc_prefill(const PrefillArgs& a, cudaStream_t s);
 // The same prefill split into a chunk-local kernel over every (head, chunk) and a
 // state-chain kernel per (sequence, head), with per-chunk records in a caller workspace.
 bool split_supported(const PrefillArgs& a);
-size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H);
-cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s);
+// segments = false keeps one pass for every shape (no second stream or events: the entry
+// point on the library's fixed scratch array uses it).
+size_t split_workspace_bytes(int64_t total_tokens, int num_seqs, int H, bool segments = true);
+cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStream_t s, bool segments = true);
 // The library's device status word on the current device (nullptr if it cannot be found).
 unsigned int* device_status_word();
 // One decode step of T tokens per sequence (state in place).

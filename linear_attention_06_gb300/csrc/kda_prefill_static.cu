@@ -72,8 +72,9 @@ extern "C" kda_status kda_prefill_split_static(const kda_shape* shape, const voi
     }
     if ((initial_state && !aligned(initial_state, 16)) || (final_state && !aligned(final_state, 16)))
         return KDA_ERR_UNSUPPORTED;
-    // the one limit of this entry point: the shape's scratch must fit the fixed array
-    if (kda::split_workspace_bytes(shape->total_tokens, shape->num_seqs, shape->H) > kStaticScratchBytes)
+    // the one limit of this entry point: the shape's scratch must fit the fixed array (one pass
+    // for every shape: the segmented run of a long sequence would create a stream and events)
+    if (kda::split_workspace_bytes(shape->total_tokens, shape->num_seqs, shape->H, false) > kStaticScratchBytes)
         return KDA_ERR_UNSUPPORTED;
     if (shape->num_seqs == 0) return KDA_OK;
 
@@ -87,5 +88,5 @@ extern "C" kda_status kda_prefill_split_static(const kda_shape* shape, const voi
     // Nothing in the array has to start at zero: every mode word and record the chain kernel
     // reads is written by this call's chunk-local kernel first.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return kda::launch_split_prefill(a, scratch, s) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda::launch_split_prefill(a, scratch, s, false) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
