@@ -106,6 +106,7 @@ struct Small {
     uint32_t tmem_base;
     int mode[2];                                 // 0 tensor-core chunk, 1 token-by-token chunk
     int cmd_b;                                   // slot of the packed chunk, -1: group B is done
+    int order_seq, order_pad[3];                 // the sequence this block takes (longest first)
     int issued[3][2];                            // TMA loads issued / waited for, per
     int consumed[3][2];                          //   (kind, slot), to drain after a timeout
     __nv_bfloat16 beta[2][C];                    // bf16 inputs: exact
@@ -481,6 +482,33 @@ __device__ __noinline__ bool run_group_b(const Ctx& x_in, const Maps& maps, __nv
 }
 
 
+// Blocks start in index order, so with sequences of mixed lengths the block of sequence slot r
+// takes the sequence of rank r by length (longest first, ties by index): the long sequences
+// start in the first wave and the last wave holds short ones.  All threads; `scratch` holds
+// the lengths.  Up to kOrderMax sequences (a few hundred cycles a block); beyond that the
+// natural order.
+constexpr int kOrderMax = 256;
+__device__ int seq_by_length(const int32_t* cu, int num_seqs, int64_t T, int r, uint8_t* scratch, int* slot) {
+    int64_t* len = reinterpret_cast<int64_t*>(scratch);
+    for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
+        int64_t b, e;
+        seq_bounds(cu, i, num_seqs, T, b, e);
+        len[i] = e - b;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < num_seqs; i += blockDim.x) {
+        const int64_t li = len[i];
+        int rank = 0;
+        for (int j = 0; j < num_seqs; ++j) {
+            const int64_t lj = len[j];
+            rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+        }
+        if (rank == r) *slot = i;
+    }
+    __syncthreads();
+    return *slot;
+}
+
 template <bool FRONT>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restrict__ beta,
@@ -498,7 +526,9 @@ chunk_tc_kernel(const __grid_constant__ Maps maps, const __nv_bfloat16* __restri
     x.sw = sw;
     x.H = H;
     x.h = blockIdx.x % H;
-    const int n = blockIdx.x / H;
+    const int n = (cu && num_seqs > 1 && num_seqs <= kOrderMax)
+                      ? seq_by_length(cu, num_seqs, T, (int)(blockIdx.x / H), sm + kWT, &sw->order_seq)
+                      : (int)(blockIdx.x / H);
     x.seq = n;
     x.T = T;
     x.num_seqs = num_seqs;
