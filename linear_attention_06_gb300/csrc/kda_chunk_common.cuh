@@ -126,12 +126,21 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
 // Operand build, team P (128 threads).
 // Pass 1 (build_suffix, thread = key channel c): suffix sums of log_alpha over the
 // chunk, e[r][c] = sum_{r<t<L} a[t][c]; returns false (leaving log_alpha untouched)
-// when a channel's chunk total leaves +-kMaxExponent, else writes e back in place and
-// returns g = e^{G_c}.  It touches only the log_alpha slot, so it runs before the
+// when a channel's chunk total leaves +-kMaxExponent, else writes e * log2(e) back in
+// place (pass 2 takes base-2 exponentials) and returns g = e^{G_c}.  It touches only the log_alpha slot, so it runs before the
 // chunk's other slots are free; the caller publishes g once they are.
 // Pass 2 (build_tiles, thread = 16-byte chunk of 8 channels of one row):
 // Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector
-// accesses.
+// accesses; the factors are 2^{-+ e log2(e)} from the SFU's base-2 exponential, the scale
+// by log2(e) having been applied once per element in pass 1.
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x, the SFU's approximation (subnormal results flushed to zero)
+__device__ __forceinline__ float ex2f_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ bool build_suffix(float* A, int L, float& g) {
     const int c = lt();
     float e[C];
@@ -147,7 +156,7 @@ __device__ bool build_suffix(float* A, int L, float& g) {
     if (group_or(kBarP, !(fabsf(run) <= kMaxExponent))) return false;
     g = __expf(run);
 #pragma unroll
-    for (int r = 0; r < C; ++r) A[r * D + c] = e[r];
+    for (int r = 0; r < C; ++r) A[r * D + c] = e[r] * kLog2e;
     group_sync(kBarP);
     return true;
 }
@@ -172,8 +181,8 @@ __device__ void build_tiles(uint8_t* qk, uint8_t* kb, const float* A, int L) {
             for (int p = 0; p < 4; ++p) {
                 const float k0 = __uint_as_float(kw[p] << 16), k1 = __uint_as_float(kw[p] & 0xffff0000u);
                 const float q0 = __uint_as_float(qw[p] << 16), q1 = __uint_as_float(qw[p] & 0xffff0000u);
-                const float u0 = __expf(-ev[2 * p]), u1 = __expf(-ev[2 * p + 1]);
-                const float d0 = __expf(ev[2 * p]), d1 = __expf(ev[2 * p + 1]);
+                const float u0 = ex2f_approx(-ev[2 * p]), u1 = ex2f_approx(-ev[2 * p + 1]);
+                const float d0 = ex2f_approx(ev[2 * p]), d1 = ex2f_approx(ev[2 * p + 1]);
                 o1[p] = pack_bf16x2(k0 * u0, k1 * u1);
                 o2[p] = pack_bf16x2(q0 * u0, q1 * u1);
                 o3[p] = pack_bf16x2(k0 * d0, k1 * d1);

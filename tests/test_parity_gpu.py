@@ -306,6 +306,26 @@ def test_decode_multi_token_agrees_with_repeated_single_steps(dtype):
         assert torch.equal(out_multi, outs) and torch.equal(S_multi, S_step)
 
 
+@pytest.mark.parametrize("T", [4, 16])
+def test_decode_multi_token_full_size_sampled_sequences(T):
+    # the bench's multi-token step (256 sequences x 32 heads, one launch of the chunk form on
+    # every SM), checked on sampled (sequence, head) pairs against the oracle
+    n, H = 256, 32
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, H, 128, 128, seed=13 + T, cu_seqlens=cu, state_std=0.05)
+    d = w.to(DEV)
+    S = d.initial_state.clone()
+    out = kda.kda_decode_step(d.q, d.k, d.v, d.log_alpha, d.beta, S)
+    torch.cuda.synchronize()
+    seqs, heads = [0, 77, 128, 255], [0, 13, 31]
+    rows = np.concatenate([np.arange(T * i, T * (i + 1)) for i in seqs])
+    pick = lambda t: np64(t[rows][:, heads])          # noqa: E731
+    ro, rf = kda_oracle.prefill(pick(w.q), pick(w.k), pick(w.v), pick(w.log_alpha), pick(w.beta),
+                                np64(w.initial_state[seqs][:, heads]), cu_seqlens=[T * i for i in range(len(seqs) + 1)])
+    assert rel_l2(np64(out)[rows][:, heads], ro) < TOL[torch.bfloat16]
+    assert rel_l2(np64(S)[seqs][:, heads], rf) < TOL[torch.bfloat16]
+
+
 def test_decode_multi_token_zero_beta_is_pure_decay():
     # beta = 0: no erase and no write, so the state is only decayed: S = Diag(e^G) S0 exactly
     # up to the fp32 product of the decay factors, and o_t = (e^{g_t} o q_t)^T S0
