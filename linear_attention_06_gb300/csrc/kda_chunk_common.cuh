@@ -124,10 +124,13 @@ __device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int num_seq
 // ============================ group A: chunk-local stage =========================
 
 // Operand build, team P (128 threads).
-// Pass 1 (build_suffix, thread = key channel c): suffix sums of log_alpha over the
-// chunk, e[r][c] = sum_{r<t<L} a[t][c]; returns false (leaving log_alpha untouched)
-// when a channel's chunk total leaves +-kMaxExponent, else writes e * log2(e) back in
-// place (pass 2 takes base-2 exponentials) and returns g = e^{G_c}.  It touches only the log_alpha slot, so it runs before the
+// Pass 1 (build_suffix): suffix sums of log_alpha over the chunk, e[r][c] =
+// sum_{r<t<L} a[t][c].  Each warp takes a segment of 16 rows and each lane four channels
+// (16-byte accesses, packed fp32x2 adds): suffix sums inside the segment, then the
+// segments' totals through the slot (each segment's first row) to add the later ones.
+// Returns false (leaving log_alpha as it was) when a channel's chunk total leaves
+// +-kMaxExponent, else writes e * log2(e) back in place (pass 2 takes base-2
+// exponentials) and returns g = e^{G_c} for the thread's own channel c.  It touches only the log_alpha slot, so it runs before the
 // chunk's other slots are free; the caller publishes g once they are.
 // Pass 2 (build_tiles, thread = 16-byte chunk of 8 channels of one row):
 // Khat = e^{-e} k, Qhat = e^{-e} q (in place), Kb = e^{e} k, all as 16-byte vector
@@ -141,22 +144,58 @@ __device__ __forceinline__ float ex2f_approx(float x) {
     return y;
 }
 
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ bool build_suffix(float* A, int L, float& g) {
-    const int c = lt();
-    float e[C];
+    // thread (quad, seg): channels 4 quad .. +3, rows 16 seg .. +15 (a warp per row segment)
+    const int t = lt(), quad = t & 31, seg = t >> 5, c4 = 4 * quad;
+    float2 lo[16], hi[16];                           // rows of this segment: channels c4, c4+1 | c4+2, c4+3
 #pragma unroll
-    for (int r = 0; r < C; ++r) e[r] = (r < L) ? A[r * D + c] : 0.f;
-    float run = 0.f;
-#pragma unroll
-    for (int r = C - 1; r >= 0; --r) {
-        const float ar = e[r];
-        e[r] = run;
-        run += ar;
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * seg + i;
+        const float4 a = (r < L) ? *reinterpret_cast<const float4*>(A + r * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        lo[i] = make_float2(a.x, a.y);
+        hi[i] = make_float2(a.z, a.w);
     }
-    if (group_or(kBarP, !(fabsf(run) <= kMaxExponent))) return false;
-    g = __expf(run);
+    const float2 raw_lo = lo[0], raw_hi = hi[0];
+    float2 rl = make_float2(0.f, 0.f), rh = rl;      // suffix sums inside the segment
 #pragma unroll
-    for (int r = 0; r < C; ++r) A[r * D + c] = e[r] * kLog2e;
+    for (int i = 15; i >= 0; --i) {
+        const float2 al = lo[i], ah = hi[i];
+        lo[i] = rl; hi[i] = rh;
+        rl = add2(rl, al); rh = add2(rh, ah);
+    }
+    // the segment's total into its first row (each thread's own four columns), then every
+    // thread reads the four totals of its columns
+    *reinterpret_cast<float4*>(A + 16 * seg * D + c4) = make_float4(rl.x, rl.y, rh.x, rh.y);
+    group_sync(kBarP);
+    float4 tot[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) tot[u] = *reinterpret_cast<const float4*>(A + 16 * u * D + c4);
+    float gt = A[t];
+#pragma unroll
+    for (int u = 1; u < 4; ++u) gt += A[16 * u * D + t];   // this thread's channel t, same order
+    float2 later_l = make_float2(0.f, 0.f), later_h = later_l, gl = later_l, gh = later_l;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 tl = make_float2(tot[u].x, tot[u].y), th = make_float2(tot[u].z, tot[u].w);
+        gl = add2(gl, tl); gh = add2(gh, th);
+        if (u > seg) { later_l = add2(later_l, tl); later_h = add2(later_h, th); }
+    }
+    const bool out = !(fabsf(gl.x) <= kMaxExponent) || !(fabsf(gl.y) <= kMaxExponent) ||
+                     !(fabsf(gh.x) <= kMaxExponent) || !(fabsf(gh.y) <= kMaxExponent);
+    if (group_or(kBarP, out)) {                      // leave log_alpha as it was
+        *reinterpret_cast<float4*>(A + 16 * seg * D + c4) = make_float4(raw_lo.x, raw_lo.y, raw_hi.x, raw_hi.y);
+        group_sync(kBarP);
+        return false;
+    }
+    g = __expf(gt);
+    const float2 l2 = make_float2(kLog2e, kLog2e);
+    const float2 ll = __fmul2_rn(later_l, l2), lh = __fmul2_rn(later_h, l2);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float2 el = __ffma2_rn(lo[i], l2, ll), eh = __ffma2_rn(hi[i], l2, lh);
+        *reinterpret_cast<float4*>(A + (16 * seg + i) * D + c4) = make_float4(el.x, el.y, eh.x, eh.y);
+    }
     group_sync(kBarP);
     return true;
 }
@@ -427,7 +466,8 @@ __device__ __forceinline__ void staging_ready() {
     __syncwarp();
 }
 
-// Lane c holds W'^T row c (64 tokens): store -W'^T as bf16, MN-major B operand.
+// Lane c holds W'^T row c (64 tokens): store W'^T as bf16, MN-major B operand (the Delta
+// product negates it through its instruction descriptor).
 __device__ void read_w(uint32_t tb, uint32_t col, uint8_t* wt) {
     const int c = lt();
     staging_ready();
@@ -441,7 +481,7 @@ __device__ void read_w(uint32_t tb, uint32_t col, uint8_t* wt) {
             uint32_t w[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                w[u] = pack_bf16x2(-__uint_as_float(v[8 * k + 2 * u]), -__uint_as_float(v[8 * k + 2 * u + 1]));
+                w[u] = pack_bf16x2(__uint_as_float(v[8 * k + 2 * u]), __uint_as_float(v[8 * k + 2 * u + 1]));
             *reinterpret_cast<uint4*>(wt + sw128_offset(c, 16 * (4 * hf + k))) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
@@ -744,9 +784,10 @@ __device__ __forceinline__ void mma_wu(uint32_t tb, uint32_t wcol, uint32_t ucol
     }
 }
 
-// Delta^T = U^T + Ss^T (-W'^T) in the U slot: A = Ss^T from TMEM, K = 128.
+// Delta^T = U^T + Ss^T (-W'^T) in the U slot: A = Ss^T from TMEM, K = 128, B = W'^T negated
+// by the instruction descriptor.
 __device__ __forceinline__ void mma_delta(uint32_t tb, uint32_t ucol, uint32_t sWT) {
-    constexpr uint32_t idw = idesc_bf16_f32(128, 64, false, true);
+    constexpr uint32_t idw = idesc_bf16_f32(128, 64, false, true, false, true);   // B negated: -W'^T
 #pragma unroll
     for (uint32_t ks = 0; ks < 8; ++ks)
         mma_ts(tb + ucol, tb + kTmSbf + ks * 8, smem_desc(sWT + ks * 2048, 16384, 1024, kSwizzle128B),

@@ -87,7 +87,7 @@ constexpr uint32_t kV0 = 65536;       // 2 x 16 KB: [v_h0 | v_h1]
 constexpr uint32_t kA0 = 98304;       // 2 x 32 KB: log_alpha fp32 [64][128]; then solve scratch + T
 constexpr uint32_t kKB0 = 163840;     // 2 x 16 KB: Kb [halves]
 constexpr uint32_t kPP0 = 196608;     // 2 x 8 KB: masked P, K-major
-constexpr uint32_t kWT = 212992;      // 16 KB: -W'^T (MN-major), then 4 x 4 KB output staging tiles
+constexpr uint32_t kWT = 212992;      // 16 KB: W'^T (MN-major), then 4 x 4 KB output staging tiles
 constexpr uint32_t kSmall = 229376;   // 2 KB: barriers, flags, beta, gamma
 constexpr uint32_t kSmemUsed = kSmall + 2048;
 constexpr uint32_t kSmemDynamic = kSmemUsed + 1024;   // + alignment slack = 232448
