@@ -203,7 +203,7 @@ __device__ bool build_suffix(float* A, int L, float& g) {
 __device__ void build_tiles(uint8_t* qk, uint8_t* kb, const float* A, int L) {
     const int c = lt();
     // pass 2: 64 rows x 16 chunks = 1024 units, 8 per thread
-#pragma unroll 2
+#pragma unroll 1
     for (int m = 0; m < 8; ++m) {
         const int u = c + 128 * m, r = u >> 4, j = u & 15;
         const uint32_t ko = qk_off(false, r, 8 * j), qo = qk_off(true, r, 8 * j), bo = half_off(r, 8 * j);
@@ -222,9 +222,12 @@ __device__ void build_tiles(uint8_t* qk, uint8_t* kb, const float* A, int L) {
                 const float q0 = __uint_as_float(qw[p] << 16), q1 = __uint_as_float(qw[p] & 0xffff0000u);
                 const float u0 = ex2f_approx(-ev[2 * p]), u1 = ex2f_approx(-ev[2 * p + 1]);
                 const float d0 = ex2f_approx(ev[2 * p]), d1 = ex2f_approx(ev[2 * p + 1]);
-                o1[p] = pack_bf16x2(k0 * u0, k1 * u1);
-                o2[p] = pack_bf16x2(q0 * u0, q1 * u1);
-                o3[p] = pack_bf16x2(k0 * d0, k1 * d1);
+                const float2 kk = make_float2(k0, k1), uu = make_float2(u0, u1);
+                const float2 a1 = __fmul2_rn(kk, uu), a2 = __fmul2_rn(make_float2(q0, q1), uu),
+                             a3 = __fmul2_rn(kk, make_float2(d0, d1));
+                o1[p] = pack_bf16x2(a1.x, a1.y);
+                o2[p] = pack_bf16x2(a2.x, a2.y);
+                o3[p] = pack_bf16x2(a3.x, a3.y);
             }
             kh = make_uint4(o1[0], o1[1], o1[2], o1[3]);
             qh = make_uint4(o2[0], o2[1], o2[2], o2[3]);
