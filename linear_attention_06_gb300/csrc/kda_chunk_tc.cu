@@ -218,7 +218,10 @@ __device__ __noinline__ bool run_team_p(const Ctx& x_in, const __nv_bfloat16* __
 
         if (!(ok = group_wait(kBarP, &sw.a_full[s], ph))) break;
         if (t == 0) ++sw.consumed[kLdA][s];
-        if constexpr (FRONT) logsigmoid_col(reinterpret_cast<float*>(aslot), t, L);   // thread t: column t
+        if constexpr (FRONT) {
+            logsigmoid_col(reinterpret_cast<float*>(aslot), t, L);   // thread t: column t
+            group_sync(kBarP);                           // build_suffix reads other threads' columns
+        }
         float gval = 0.f;
         const bool fast = build_suffix(reinterpret_cast<float*>(aslot), L, gval);
         // Kb / P / beta / gamma and the q/k tiles of this slot are chunk n-2's until its state product
