@@ -33,10 +33,11 @@
 // an accumulator over tokens is already the A fragment of the next product that reads it.  The
 // state crosses HBM once in each direction, and no product needs a reduction across warps.
 // TF32 rounds the operands of these products to 11 significant bits; the carried state stays
-// fp32 (the update adds into it in the fp32 accumulator).  A and P use split TF32 operands
-// (x = hi + lo, three products), close to fp32, and the triangular solve runs in fp32 on the
-// accumulator of R: the lanes holding token s compute Delta_s and pass it by shuffle to the
-// three other lanes of their column pair, which subtract A_ts Delta_s from their later tokens.
+// fp32 (the update adds into it in the fp32 accumulator).  A and P take TF32 operands too (Khat,
+// Qhat and Kb rounded once when they are formed; the chunked prefill forms them from bf16
+// operands, three bits fewer), and the triangular solve runs in fp32 on the accumulator of R:
+// the lanes holding token s compute Delta_s and pass it by shuffle to the three other lanes of
+// their column pair, which subtract A_ts Delta_s from their later tokens.
 //
 // Schedule of one (sequence, head): the state is loaded into registers while the step's token
 // vectors are staged in shared memory; per key channel the cumulative decay and the scaled
@@ -48,7 +49,7 @@
 // fp32 do not come here: they keep the one-token kernel's token loop, which is as fast for them
 // and gives the same bits as T one-token steps.
 //
-// Blocks are persistent, two per SM (83 KiB of shared memory and at most 128 registers a thread
+// Blocks are persistent, two per SM (66 KiB of shared memory and at most 128 registers a thread
 // each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
 // the state and token rows of its next pair into L2 when it starts a pair, so that their DRAM
 // reads overlap its arithmetic.
@@ -75,18 +76,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 // without bank conflicts.
 constexpr int kLd = 132, kLdB = 136, kLdT = 24, kLdA = 20;
 
+// Arrays whose lives do not overlap share storage: log alpha is dead once the barrier that
+// decides the chunk form has passed, when Kb^T is written; -K_g is dead after the first state
+// pass, before the output rows are written (the token loop uses neither Kb^T nor K_g).  A
+// smaller block footprint measured faster (T = 16: 318 us at 66 KiB, 326 us at 83 KiB).
 struct Smem {
     float k[kTok][kLdB];     // k; Khat
     float q[kTok][kLdB];     // q; Qhat
     float v[kTok][kLd];      // v
-    float g[kTok][kLd];      // log alpha; alpha in the token loop
-    float kg[kTok][kLdB];    // -K_g in TF32
+    union {
+        float g[kTok][kLd];      // log alpha; alpha in the token loop
+        float kbt[kD][kLdT];     // Kb^T in TF32 (written once the chunk form is decided)
+    };
+    union {
+        float kg[kTok][kLdB];    // -K_g in TF32 (read by the first state pass)
+        float os[kTok][kLd];     // output rows (written after it; the token loop has no K_g)
+    };
     float kb[kTok][kLdB];    // Kb
     float qg[kTok][kLdB];    // Q_g in TF32
-    float kbt[kD][kLdT];     // Kb^T in TF32
     float am[kTok][kLdA];    // A (s < t, else 0)
     float pm[kTok][kLdT];    // P (s <= t, else 0) in TF32
-    float os[kTok][kLd];     // output rows
     float dec[kD];           // e^G per key channel
     float beta[kTok];
     float kq[kTok];          // k_t . q_t (token loop)
@@ -123,12 +132,6 @@ __device__ __forceinline__ float ex2(float x) {       // 2^x, the SFU's approxim
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-// x = hi + lo with both parts TF32: three products of the parts carry a product to about fp32
-// accuracy (the lo x lo term is below it).
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
 }
 
 template <typename Tin>
@@ -322,13 +325,13 @@ __device__ __forceinline__ bool scale_rows(Smem& sm) {
         const float g2 = gl[i] * kLog2e;
         const float eg = ex2(g2), eb = ex2(G2 - g2), eh = ex2(g2 - G2);
         const float kv = sm.k[t][c], qv = sm.q[t][c];
-        const float kb = eb * kv;
+        const float kb = tf32f(eb * kv);
         sm.kb[t][c] = kb;
-        kbt[i] = tf32f(kb);
+        kbt[i] = kb;
         sm.kg[t][c] = -tf32f(eg * kv);
-        sm.k[t][c] = eh * kv;
+        sm.k[t][c] = tf32f(eh * kv);
         sm.qg[t][c] = tf32f(eg * qv);
-        sm.q[t][c] = eh * qv;
+        sm.q[t][c] = tf32f(eh * qv);
     }
 #pragma unroll
     for (int i = 0; i < kTH; i += 4)
@@ -337,31 +340,26 @@ __device__ __forceinline__ bool scale_rows(Smem& sm) {
     return true;
 }
 
-// A = Khat Kb^T and P = Qhat Kb^T, 16 x 8 tiles on the tensor cores with split TF32 operands
+// A = Khat Kb^T and P = Qhat Kb^T, 16 x 8 tiles on the tensor cores, TF32 operands as stored
 // (fragment k = qi <-> channel 8b + 2qi, k = qi + 4 <-> 8b + 2qi + 1); warp w < 2 NT takes tile
-// w (A for w < NT, P after), three independent accumulators over the 128 channels.
+// w (A for w < NT, P after), two accumulators (even and odd channel blocks) over the 128 channels.
 template <int NT>
 __device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
     const bool isP = warp >= NT;
     const int nt = warp % NT;
     const float* X = isP ? &sm.q[0][0] : &sm.k[0][0];
-    float acc[3][4] = {};
+    float acc[2][4] = {};                            // two accumulators: even and odd channel blocks
 #pragma unroll
     for (int b = 0; b < 16; ++b) {
-        const float2 x0 = *reinterpret_cast<const float2*>(X + gi * kLdB + 8 * b + 2 * qi);
-        const float2 x1 = *reinterpret_cast<const float2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi);
-        const float2 y = *reinterpret_cast<const float2*>(&sm.kb[8 * nt + gi][8 * b + 2 * qi]);
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(x0.x, ah[0], al[0]); split_tf32(x1.x, ah[1], al[1]);
-        split_tf32(x0.y, ah[2], al[2]); split_tf32(x1.y, ah[3], al[3]);
-        split_tf32(y.x, bh[0], bl[0]); split_tf32(y.y, bh[1], bl[1]);
-        mma_tf32(acc[0], al, bh);
-        mma_tf32(acc[1], ah, bl);
-        mma_tf32(acc[2], ah, bh);
+        const uint2 x0 = *reinterpret_cast<const uint2*>(X + gi * kLdB + 8 * b + 2 * qi);
+        const uint2 x1 = *reinterpret_cast<const uint2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi);
+        const uint2 y = *reinterpret_cast<const uint2*>(&sm.kb[8 * nt + gi][8 * b + 2 * qi]);
+        const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y}, bb[2] = {y.x, y.y};
+        mma_tf32(acc[b & 1], a, bb);
     }
     float c[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e] + acc[2][e];
+    for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e];
     // c: (t = gi, s = 8 nt + 2 qi, +1), (t = gi + 8, same s)
     const int s0 = 8 * nt + 2 * qi;
     if (isP) {
