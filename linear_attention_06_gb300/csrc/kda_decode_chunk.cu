@@ -49,7 +49,7 @@
 // fp32 do not come here: they keep the one-token kernel's token loop, which is as fast for them
 // and gives the same bits as T one-token steps.
 //
-// Blocks are persistent, two per SM (66 KiB of shared memory and at most 128 registers a thread
+// Blocks are persistent, two per SM (58 KiB of shared memory and at most 128 registers a thread
 // each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
 // the state and token rows of its next pair into L2 when it starts a pair, so that their DRAM
 // reads overlap its arithmetic.
@@ -79,7 +79,8 @@ constexpr int kLd = 132, kLdB = 136, kLdT = 24, kLdA = 20;
 // Arrays whose lives do not overlap share storage: log alpha is dead once the barrier that
 // decides the chunk form has passed, when Kb^T is written; -K_g is dead after the first state
 // pass, before the output rows are written (the token loop uses neither Kb^T nor K_g).  A
-// smaller block footprint measured faster (T = 16: 318 us at 66 KiB, 326 us at 83 KiB).
+// smaller block footprint measured faster (T = 16: 318 us at 66 KiB, 326 us at 83 KiB).  The
+// Gram products read Kb from its transposed TF32 copy (no second Kb tile).
 struct Smem {
     float k[kTok][kLdB];     // k; Khat
     float q[kTok][kLdB];     // q; Qhat
@@ -92,7 +93,6 @@ struct Smem {
         float kg[kTok][kLdB];    // -K_g in TF32 (read by the first state pass)
         float os[kTok][kLd];     // output rows (written after it; the token loop has no K_g)
     };
-    float kb[kTok][kLdB];    // Kb
     float qg[kTok][kLdB];    // Q_g in TF32
     float am[kTok][kLdA];    // A (s < t, else 0)
     float pm[kTok][kLdT];    // P (s <= t, else 0) in TF32
@@ -325,9 +325,7 @@ __device__ __forceinline__ bool scale_rows(Smem& sm) {
         const float g2 = gl[i] * kLog2e;
         const float eg = ex2(g2), eb = ex2(G2 - g2), eh = ex2(g2 - G2);
         const float kv = sm.k[t][c], qv = sm.q[t][c];
-        const float kb = tf32f(eb * kv);
-        sm.kb[t][c] = kb;
-        kbt[i] = kb;
+        kbt[i] = tf32f(eb * kv);
         sm.kg[t][c] = -tf32f(eg * kv);
         sm.k[t][c] = tf32f(eh * kv);
         sm.qg[t][c] = tf32f(eg * qv);
@@ -353,8 +351,9 @@ __device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
     for (int b = 0; b < 16; ++b) {
         const uint2 x0 = *reinterpret_cast<const uint2*>(X + gi * kLdB + 8 * b + 2 * qi);
         const uint2 x1 = *reinterpret_cast<const uint2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi);
-        const uint2 y = *reinterpret_cast<const uint2*>(&sm.kb[8 * nt + gi][8 * b + 2 * qi]);
-        const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y}, bb[2] = {y.x, y.y};
+        const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+        const uint32_t bb[2] = {__float_as_uint(sm.kbt[8 * b + 2 * qi][8 * nt + gi]),
+                                __float_as_uint(sm.kbt[8 * b + 2 * qi + 1][8 * nt + gi])};
         mma_tf32(acc[b & 1], a, bb);
     }
     float c[4];
