@@ -49,10 +49,10 @@
 // fp32 do not come here: they keep the one-token kernel's token loop, which is as fast for them
 // and gives the same bits as T one-token steps.
 //
-// Blocks are persistent, two per SM (58 KiB of shared memory and at most 128 registers a thread
-// each), and walk the (sequence, head) pairs with a stride of the grid size; each prefetches
-// the state and token rows of its next pair into L2 when it starts a pair, so that their DRAM
-// reads overlap its arithmetic.
+// Blocks are persistent, two per SM (59,008 bytes of shared memory a block for 9..16 tokens,
+// 35,968 for 2..8, and at most 128 registers a thread), and walk the (sequence, head) pairs
+// with a stride of the grid size; each prefetches the state and token rows of its next pair
+// into L2 when it starts a pair, so that their DRAM reads overlap its arithmetic.
 #include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -80,22 +80,25 @@ constexpr int kLd = 132, kLdB = 136, kLdT = 24, kLdA = 20;
 // decides the chunk form has passed, when Kb^T is written; -K_g is dead after the first state
 // pass, before the output rows are written (the token loop uses neither Kb^T nor K_g).  A
 // smaller block footprint measured faster (T = 16: 318 us at 66 KiB, 326 us at 83 KiB).  The
-// Gram products read Kb from its transposed TF32 copy (no second Kb tile).
+// Gram products read Kb from its transposed TF32 copy (no second Kb tile), and the token rows
+// are sized to the instance (8 NT rows: a step of at most 8 tokens keeps half the rows).
+template <int NT>
 struct Smem {
-    float k[kTok][kLdB];     // k; Khat
-    float q[kTok][kLdB];     // q; Qhat
-    float v[kTok][kLd];      // v
+    static constexpr int R = 8 * NT;   // token rows: the step's tokens padded to whole 8-token blocks
+    float k[R][kLdB];     // k; Khat
+    float q[R][kLdB];     // q; Qhat
+    float v[R][kLd];      // v
     union {
-        float g[kTok][kLd];      // log alpha; alpha in the token loop
+        float g[R][kLd];      // log alpha; alpha in the token loop
         float kbt[kD][kLdT];     // Kb^T in TF32 (written once the chunk form is decided)
     };
     union {
-        float kg[kTok][kLdB];    // -K_g in TF32 (read by the first state pass)
-        float os[kTok][kLd];     // output rows (written after it; the token loop has no K_g)
+        float kg[R][kLdB];    // -K_g in TF32 (read by the first state pass)
+        float os[R][kLd];     // output rows (written after it; the token loop has no K_g)
     };
-    float qg[kTok][kLdB];    // Q_g in TF32
-    float am[kTok][kLdA];    // A (s < t, else 0)
-    float pm[kTok][kLdT];    // P (s <= t, else 0) in TF32
+    float qg[R][kLdB];    // Q_g in TF32
+    float am[R][kLdA];    // A (s < t, else 0)
+    float pm[R][kLdT];    // P (s <= t, else 0) in TF32
     float dec[kD];           // e^G per key channel
     float beta[kTok];
     float kq[kTok];          // k_t . q_t (token loop)
@@ -195,10 +198,10 @@ __device__ __forceinline__ void prefetch_pair(const Params<Tin>& p, int pair) {
 }
 
 // The step's token vectors into shared memory (rows T .. 15 zero: tokens that change nothing).
-template <typename Tin>
-__device__ __forceinline__ void stage_tokens(Smem& sm, const Params<Tin>& p, size_t row0, int64_t n_rows) {
+template <int NT, typename Tin>
+__device__ __forceinline__ void stage_tokens(Smem<NT>& sm, const Params<Tin>& p, size_t row0, int64_t n_rows) {
     (void)n_rows;
-    for (int i = threadIdx.x; i < kTok * (kD / 8); i += kThreads) {
+    for (int i = threadIdx.x; i < Smem<NT>::R * (kD / 8); i += kThreads) {
         const int t = i / (kD / 8), c = (i % (kD / 8)) * 8;
         float kx[8], qx[8], vx[8], ax[8];
         const size_t e = (row0 + (size_t)t * p.H) * kD + c;
@@ -219,8 +222,8 @@ __device__ __forceinline__ void stage_tokens(Smem& sm, const Params<Tin>& p, siz
 
 // out rows of the step from sm.os: plain, or gated (RMSNorm over the 128 channels x weight x
 // sigmoid(gate)).  One warp per token, four channels a lane.
-template <typename Tin>
-__device__ __forceinline__ void store_outputs(const Smem& sm, const Params<Tin>& p, size_t row0, int64_t n_rows) {
+template <int NT, typename Tin>
+__device__ __forceinline__ void store_outputs(const Smem<NT>& sm, const Params<Tin>& p, size_t row0, int64_t n_rows) {
     (void)n_rows;
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = w; t < p.T; t += kThreads / 32) {
@@ -249,7 +252,8 @@ __device__ __forceinline__ void store_outputs(const Smem& sm, const Params<Tin>&
 // over the lane's rows (then across the four lanes qi that share the column pair), the erase /
 // write delta, the output and the rank-one update.  Reads k, q, v, beta and log alpha from
 // shared memory; writes the output rows to sm.os.
-__device__ __forceinline__ void token_loop(Smem& sm, float (&s)[16][4], int T, int warp, int lane, int qi, int jc) {
+template <int NT>
+__device__ __forceinline__ void token_loop(Smem<NT>& sm, float (&s)[16][4], int T, int warp, int lane, int qi, int jc) {
     for (int i = threadIdx.x; i < T * kD; i += kThreads) {
         const int t = i / kD, c = i % kD;
         sm.g[t][c] = expf(sm.g[t][c]);
@@ -306,7 +310,7 @@ __device__ __forceinline__ void token_loop(Smem& sm, float (&s)[16][4], int T, i
 // cumulative decay in base 2 and the scaled rows.  Returns whether the chunk form holds (the
 // same answer in every thread).
 template <int NT>
-__device__ __forceinline__ bool scale_rows(Smem& sm) {
+__device__ __forceinline__ bool scale_rows(Smem<NT>& sm) {
     constexpr int kT8 = 8 * NT, kTH = kT8 / 2;       // token rows, rows per half
     const int c = threadIdx.x & (kD - 1), half = threadIdx.x >> 7;
     float run = 0.f;
@@ -342,7 +346,7 @@ __device__ __forceinline__ bool scale_rows(Smem& sm) {
 // (fragment k = qi <-> channel 8b + 2qi, k = qi + 4 <-> 8b + 2qi + 1); warp w < 2 NT takes tile
 // w (A for w < NT, P after), two accumulators (even and odd channel blocks) over the 128 channels.
 template <int NT>
-__device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
+__device__ __forceinline__ void gram_tile(Smem<NT>& sm, int warp, int gi, int qi) {
     const bool isP = warp >= NT;
     const int nt = warp % NT;
     const float* X = isP ? &sm.q[0][0] : &sm.k[0][0];
@@ -350,7 +354,8 @@ __device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
 #pragma unroll
     for (int b = 0; b < 16; ++b) {
         const uint2 x0 = *reinterpret_cast<const uint2*>(X + gi * kLdB + 8 * b + 2 * qi);
-        const uint2 x1 = *reinterpret_cast<const uint2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi);
+        const uint2 x1 = NT > 1 ? *reinterpret_cast<const uint2*>(X + (gi + 8) * kLdB + 8 * b + 2 * qi)
+                                : make_uint2(0u, 0u);   // padding tokens 8-15 of a one-block step
         const uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
         const uint32_t bb[2] = {__float_as_uint(sm.kbt[8 * b + 2 * qi][8 * nt + gi]),
                                 __float_as_uint(sm.kbt[8 * b + 2 * qi + 1][8 * nt + gi])};
@@ -364,12 +369,14 @@ __device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
     if (isP) {
         *reinterpret_cast<float2*>(&sm.pm[gi][s0]) =
             make_float2(s0 <= gi ? tf32f(c[0]) : 0.f, s0 + 1 <= gi ? tf32f(c[1]) : 0.f);
-        *reinterpret_cast<float2*>(&sm.pm[gi + 8][s0]) =
-            make_float2(s0 <= gi + 8 ? tf32f(c[2]) : 0.f, s0 + 1 <= gi + 8 ? tf32f(c[3]) : 0.f);
+        if (NT > 1)
+            *reinterpret_cast<float2*>(&sm.pm[gi + 8][s0]) =
+                make_float2(s0 <= gi + 8 ? tf32f(c[2]) : 0.f, s0 + 1 <= gi + 8 ? tf32f(c[3]) : 0.f);
     } else {
         *reinterpret_cast<float2*>(&sm.am[gi][s0]) = make_float2(s0 < gi ? c[0] : 0.f, s0 + 1 < gi ? c[1] : 0.f);
-        *reinterpret_cast<float2*>(&sm.am[gi + 8][s0]) =
-            make_float2(s0 < gi + 8 ? c[2] : 0.f, s0 + 1 < gi + 8 ? c[3] : 0.f);
+        if (NT > 1)
+            *reinterpret_cast<float2*>(&sm.am[gi + 8][s0]) =
+                make_float2(s0 < gi + 8 ? c[2] : 0.f, s0 + 1 < gi + 8 ? c[3] : 0.f);
     }
 }
 
@@ -379,7 +386,7 @@ __device__ __forceinline__ void gram_tile(Smem& sm, int warp, int gi, int qi) {
 // already subtracted); a shuffle gives it to the other lanes of the column pair, which subtract
 // A_ts Delta_s from every later token t they hold (A is zero on and above the diagonal).
 template <int NT>
-__device__ __forceinline__ void solve_delta(const Smem& sm, float (&rt)[NT][4], int lane, int qi) {
+__device__ __forceinline__ void solve_delta(const Smem<NT>& sm, float (&rt)[NT][4], int lane, int qi) {
     constexpr int kT8 = 8 * NT;
 #pragma unroll
     for (int s4 = 0; s4 < kT8; s4 += 4) {
@@ -412,7 +419,7 @@ __device__ __forceinline__ void solve_delta(const Smem& sm, float (&rt)[NT][4], 
 
 // Chunk form after scale_rows: returns with the output rows in sm.os and the new state in s.
 template <int NT>
-__device__ __forceinline__ void chunk_products(Smem& sm, float (&s)[16][4], int warp, int lane, int gi, int qi,
+__device__ __forceinline__ void chunk_products(Smem<NT>& sm, float (&s)[16][4], int warp, int lane, int gi, int qi,
                                                int jc) {
     if (warp < 2 * NT) gram_tile<NT>(sm, warp, gi, qi);
 
@@ -478,7 +485,7 @@ __device__ __forceinline__ void chunk_products(Smem& sm, float (&s)[16][4], int 
 template <typename Tin, int NT>
 __global__ void __launch_bounds__(kThreads, 2) decode_chunk_kernel(const Params<Tin> p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+    Smem<NT>& sm = *reinterpret_cast<Smem<NT>*>(smem_raw);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gi = lane >> 2, qi = lane & 3;
     const int jc = 16 * warp + 2 * gi;               // this lane's value columns jc, jc + 1
@@ -518,7 +525,7 @@ cudaError_t launch_t(const Params<Tin>& p, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(decode_chunk_kernel<Tin, NT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem<NT>));
         int sms = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -527,7 +534,7 @@ cudaError_t launch_t(const Params<Tin>& p, cudaStream_t st) {
     }
     const int resident = 2 * sm_count[dev].load(std::memory_order_relaxed);   // two blocks an SM
     const unsigned blocks = (unsigned)(p.pairs < resident ? p.pairs : resident);
-    decode_chunk_kernel<Tin, NT><<<blocks, kThreads, sizeof(Smem), st>>>(p);
+    decode_chunk_kernel<Tin, NT><<<blocks, kThreads, sizeof(Smem<NT>), st>>>(p);
     return cudaGetLastError();
 }
 
