@@ -4,13 +4,16 @@
 // ("Kimi K3 architecture: KDA, MLA and MoE", section "Scale: Total vs Active
 // Parameters and Serving Economics", Visual 1, the KDA inset).
 //
-// Memory-bound.  A convolution warp walks a run of 32 consecutive tokens of one
-// head for one of q, k, v; lane l holds channels [l*CPL, l*CPL + CPL) of each row,
-// so every row access is one coalesced 256-byte (bf16, d = 128) segment.  Rows
-// are loaded eight tokens at a time (all in flight together); the W-1 previous
-// raw rows stay in registers as the warp advances, so each raw row is read once
-// (plus W-1 halo rows per run), and the convolution restarts from zeros at every
-// sequence start.  The decay and beta gates are a separate elementwise kernel.
+// Memory-bound.  A convolution warp walks a run of 256 consecutive tokens of one
+// head for one of q, k, v (bf16 rows: each half warp its own 128-token run); the
+// LPR lanes of a row hold CPL channels each, so every row access is one coalesced
+// segment.  Raw rows are copied into shared memory eight at a time by cp.async,
+// two stages in flight, so the next stage's loads overlap the current stage's
+// arithmetic; the W-1 previous raw rows stay in registers as the warp advances, so
+// each raw row is read once (plus W-1 halo rows per run), and the convolution
+// restarts from zeros at every sequence start.  Runs of 32 tokens with one staged
+// copy each measured 566 us for the bench's front end against 468 us in this form.
+// The decay and beta gates are a separate elementwise kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -20,7 +23,8 @@
 namespace kda {
 namespace {
 
-constexpr int kRun = 32;       // tokens per warp
+constexpr int kRun = 256;      // tokens per warp
+constexpr int kStageRows = 8;  // rows per cp.async stage (two stages in flight)
 constexpr int kWarps = 4;      // warps per block
 
 __device__ __forceinline__ float to_f(float x) { return x; }
@@ -174,16 +178,16 @@ __device__ __forceinline__ void cp_async(void* dst_smem, const void* src) {
     else
         asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(d), "l"(src), "n"(BYTES) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // One of q (tensor z0 + blockIdx.z = 0), k (1) or v (2) for kRun tokens of one head
 // per warp.  LPR lanes hold a row (CPL channels each); with LPR = 16 the two halves of
 // a warp walk two runs of kRun / 2 tokens side by side.  A run's raw rows are copied
-// into shared memory kStage at a time (every lane its own channels, all copies in
-// flight together, no registers held), then convolved with the history kept in
-// registers, passed through SiLU and (q, k) normalised.
+// into shared memory kStage at a time into two alternating buffers (every lane its own
+// channels, no registers held), then convolved with the history kept in registers,
+// passed through SiLU and (q, k) normalised.
 template <typename T, int CPL, int W, int LPR>
 __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z0) {
     static_assert(LPR == 16 || LPR == 32, "a row is half a warp or a warp");
@@ -191,8 +195,8 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
     constexpr int kSub = kRun / RPW;                              // tokens per run
     constexpr int kSeg = CPL * (int)sizeof(T);                    // bytes per lane and row
     constexpr int kRow = LPR * kSeg;                              // bytes per staged row
-    constexpr int kStage = kRow * kRun <= 8192 ? kSub : 8192 / (kRow * RPW);
-    __shared__ __align__(16) uint8_t stage[kWarps][RPW][kStage][kRow];
+    constexpr int kStage = kStageRows;
+    __shared__ __align__(16) uint8_t stage[kWarps][RPW][2][kStage][kRow];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane / LPR, ll = lane % LPR;
     const unsigned mask = LPR == 32 ? 0xffffffffu : (0xffffu << (16 * sub));
@@ -229,16 +233,31 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
         if (W > 1 && sr >= bos && KDA_INDEX_OK((sr * H + h) * d + c0 + CPL - 1, n_elems, a.status))
             load_row<T, CPL>(src + (sr * H + h) * d + c0, hist[i]);
     }
-    uint8_t* mine = &stage[warp][sub][0][ll * kSeg];
     const int64_t rstride = (int64_t)H * d;              // elements from one token's row to the next
     const T* sp = src + (t_begin * H + h) * d + c0;
     T* dp = dst + (t_begin * H + h) * d + c0;
-    for (int64_t ts = t_begin; ts < t_end; ts += kStage) {
+    // stage k (rows t_begin + k kStage ...) goes to buffer k & 1; stages k and k + 1 are in flight
+    // while stage k - 1 is convolved.  Each lane copies and reads back only its own bytes.
+    const int nstages = (int)((t_end - t_begin + kStage - 1) / kStage);
+    auto issue = [&](int k) {
+        if (k < nstages) {
+            const int64_t ts = t_begin + (int64_t)k * kStage;
+            const int n = (int)min((int64_t)kStage, t_end - ts);
+            uint8_t* buf = &stage[warp][sub][k & 1][0][ll * kSeg];
+            const T* p = sp + (int64_t)k * kStage * rstride;
+            for (int j = 0; j < n; ++j, p += rstride)
+                if (KDA_INDEX_OK(((ts + j) * H + h) * d + c0 + CPL - 1, n_elems, a.status))
+                    cp_async<kSeg>(buf + j * kRow, p);
+        }
+        cp_async_commit();                               // an empty group past the end keeps the count
+    };
+    issue(0);
+    issue(1);
+    for (int k = 0; k < nstages; ++k) {
+        cp_async_wait<1>();                              // stage k landed (k + 1 may be in flight)
+        const int64_t ts = t_begin + (int64_t)k * kStage;
         const int n = (int)min((int64_t)kStage, t_end - ts);
-        for (int j = 0; j < n; ++j, sp += rstride)
-            if (KDA_INDEX_OK(((ts + j) * H + h) * d + c0 + CPL - 1, n_elems, a.status))
-                cp_async<kSeg>(mine + j * kRow, sp);
-        cp_async_wait_all();                             // this lane's own copies
+        const uint8_t* buf = &stage[warp][sub][k & 1][0][ll * kSeg];
 #pragma unroll 4
         for (int j = 0; j < n; ++j, dp += rstride) {
             const int64_t t = ts + j;
@@ -250,12 +269,14 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
                     for (int c = 0; c < CPL; ++c) hist[i][c] = 0.f;
             }
             float xr[CPL], y[CPL];
-            load_row<T, CPL>(reinterpret_cast<const T*>(mine + j * kRow), xr);
+            load_row<T, CPL>(reinterpret_cast<const T*>(buf + j * kRow), xr);
             conv_step<CPL, W, sizeof(T) == 2>(xr, hist, wt, y);   // bf16 outputs: the tanh form
             if (norm) l2_normalize<CPL, LPR>(y, a.eps, mask);
             if (KDA_INDEX_OK((t * H + h) * d + c0 + CPL - 1, n_elems, a.status)) store_row<T, CPL>(dp, y);
         }
+        issue(k + 2);                                    // into the buffer just read
     }
+    cp_async_wait<0>();
 }
 
 // log_alpha = logsigmoid(a_raw) and beta = sigmoid(b_raw): elementwise over rows
