@@ -4,16 +4,19 @@
 // ("Kimi K3 architecture: KDA, MLA and MoE", section "Scale: Total vs Active
 // Parameters and Serving Economics", Visual 1, the KDA inset).
 //
-// Memory-bound.  A convolution warp walks a run of 256 consecutive tokens of one
-// head for one of q, k, v (bf16 rows: each half warp its own 128-token run); the
+// Memory-bound.  A convolution warp walks a run of about 256 consecutive tokens of
+// one head for one of q, k, v (bf16 rows: each half warp its own half run; the launch
+// sizes the run so the grid ends just under a whole number of waves); the
 // LPR lanes of a row hold CPL channels each, so every row access is one coalesced
 // segment.  Raw rows are copied into shared memory eight at a time by cp.async,
 // two stages in flight, so the next stage's loads overlap the current stage's
 // arithmetic; the W-1 previous raw rows stay in registers as the warp advances, so
 // each raw row is read once (plus W-1 halo rows per run), and the convolution
 // restarts from zeros at every sequence start.  Runs of 32 tokens with one staged
-// copy each measured 566 us for the bench's front end against 468 us in this form.
+// copy each measured 566 us for the bench's front end, fixed 256-token runs 468 us
+// (a last wave of 32 blocks), runs sized to whole waves 454 us.
 // The decay and beta gates are a separate elementwise kernel.
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,7 +26,7 @@
 namespace kda {
 namespace {
 
-constexpr int kRun = 256;      // tokens per warp
+constexpr int kRun = 256;      // tokens per warp (target; the launch rounds it to fill whole waves)
 constexpr int kStageRows = 8;  // rows per cp.async stage (two stages in flight)
 constexpr int kWarps = 4;      // warps per block
 
@@ -189,10 +192,10 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // channels, no registers held), then convolved with the history kept in registers,
 // passed through SiLU and (q, k) normalised.
 template <typename T, int CPL, int W, int LPR>
-__global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z0) {
+__global__ void __launch_bounds__(kWarps * 32, 5) conv_kernel(FrontendArgs a, int z0, int run) {
     static_assert(LPR == 16 || LPR == 32, "a row is half a warp or a warp");
     constexpr int RPW = 32 / LPR;                                 // runs per warp
-    constexpr int kSub = kRun / RPW;                              // tokens per run
+    const int kSub = run / RPW;                                   // tokens per run
     constexpr int kSeg = CPL * (int)sizeof(T);                    // bytes per lane and row
     constexpr int kRow = LPR * kSeg;                              // bytes per staged row
     constexpr int kStage = kStageRows;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
     const int sub = lane / LPR, ll = lane % LPR;
     const unsigned mask = LPR == 32 ? 0xffffffffu : (0xffffu << (16 * sub));
     const int h = blockIdx.y, which = z0 + (int)blockIdx.z;
-    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + warp) * kRun + (int64_t)sub * kSub;
+    const int64_t t_begin = ((int64_t)blockIdx.x * kWarps + warp) * run + (int64_t)sub * kSub;
     if (t_begin >= a.total_tokens) return;
     const int64_t t_end = min(t_begin + kSub, a.total_tokens);
     const int H = a.H, d = which == 2 ? a.dv : a.dk;
@@ -212,6 +215,7 @@ __global__ void __launch_bounds__(kWarps * 32) conv_kernel(FrontendArgs a, int z
     const bool norm = which != 2;
 
     const int64_t n_elems = a.total_tokens * H * d;      // elements of src and dst
+    (void)n_elems;                                       // read by the index checks of bounds-checked builds
     float wt[W][CPL];
 #pragma unroll
     for (int c = 0; c < CPL; ++c)
@@ -309,12 +313,12 @@ __global__ void __launch_bounds__(kWarps * 32) gate_kernel(FrontendArgs a) {
 }
 
 template <typename T, int CPL, int LPR>
-cudaError_t launch_conv(const FrontendArgs& a, dim3 grid, int z0, cudaStream_t s) {
+cudaError_t launch_conv(const FrontendArgs& a, dim3 grid, int z0, int run, cudaStream_t s) {
     switch (a.conv_width) {
-        case 1: conv_kernel<T, CPL, 1, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 2: conv_kernel<T, CPL, 2, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 3: conv_kernel<T, CPL, 3, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
-        case 4: conv_kernel<T, CPL, 4, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0); break;
+        case 1: conv_kernel<T, CPL, 1, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0, run); break;
+        case 2: conv_kernel<T, CPL, 2, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0, run); break;
+        case 3: conv_kernel<T, CPL, 3, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0, run); break;
+        case 4: conv_kernel<T, CPL, 4, LPR><<<grid, kWarps * 32, 0, s>>>(a, z0, run); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -323,24 +327,61 @@ cudaError_t launch_conv(const FrontendArgs& a, dim3 grid, int z0, cudaStream_t s
 // A row of d channels: bf16 rows are split over half a warp (16-byte accesses), fp32 rows over
 // a warp.
 template <typename T>
-cudaError_t launch_rows(const FrontendArgs& a, int d, dim3 grid, int z0, cudaStream_t s) {
+cudaError_t launch_rows(const FrontendArgs& a, int d, dim3 grid, int z0, int run, cudaStream_t s) {
     if constexpr (sizeof(T) == 2)
-        return d == 128 ? launch_conv<T, 8, 16>(a, grid, z0, s) : launch_conv<T, 4, 16>(a, grid, z0, s);
+        return d == 128 ? launch_conv<T, 8, 16>(a, grid, z0, run, s) : launch_conv<T, 4, 16>(a, grid, z0, run, s);
     else
-        return d == 128 ? launch_conv<T, 4, 32>(a, grid, z0, s) : launch_conv<T, 2, 32>(a, grid, z0, s);
+        return d == 128 ? launch_conv<T, 4, 32>(a, grid, z0, run, s) : launch_conv<T, 2, 32>(a, grid, z0, run, s);
+}
+
+// Tokens per convolution warp: about kRun, rounded so that the grid ends just under a whole
+// number of waves of resident blocks (a last wave of a few blocks would leave the GPU idle), in
+// multiples of 2 kStageRows (whole stages for both half-warp runs).
+int run_length(int64_t tokens, int tensors, int H, int resident_blocks) {
+    const int64_t res_warps = (int64_t)resident_blocks * kWarps;
+    const int64_t per = (int64_t)tensors * H;                     // independent (tensor, head) columns
+    const int64_t want_warps = per * ((tokens + kRun - 1) / kRun);
+    const int64_t waves = want_warps <= res_warps ? 1 : (want_warps + res_warps / 2) / res_warps;
+    const int64_t warps_per_col = (res_warps * waves) / per;      // whole waves, split over the columns
+    if (warps_per_col <= 0) return kRun;
+    const int64_t step = 2 * kStageRows;
+    const int64_t rl = ((tokens + warps_per_col - 1) / warps_per_col + step - 1) / step * step;
+    return (int)(rl < step ? step : (rl > (1 << 20) ? (1 << 20) : rl));
+}
+
+// Resident blocks of the bf16 / fp32 d = 128 convolution instance on this device (once per device).
+template <typename T>
+int resident_conv_blocks() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    int per_sm = 0, sms = 0;
+    constexpr int CPL = sizeof(T) == 2 ? 8 : 4, LPR = sizeof(T) == 2 ? 16 : 32;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, conv_kernel<T, CPL, 4, LPR>, kWarps * 32, 0) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm <= 0 || sms <= 0)
+        return 0;
+    v = per_sm * sms;
+    cached[dev].store(v, std::memory_order_relaxed);
+    return v;
 }
 
 template <typename T>
 cudaError_t launch_t(const FrontendArgs& a, cudaStream_t s) {
-    const int64_t runs = (a.total_tokens + kRun - 1) / kRun;
+    const int resident = resident_conv_blocks<T>();
+    const int tensors = a.dk == a.dv ? 3 : 2;
+    const int run = resident > 0 ? run_length(a.total_tokens, tensors, a.H, resident) : kRun;
+    const int64_t runs = (a.total_tokens + run - 1) / run;
     const unsigned bx = (unsigned)((runs + kWarps - 1) / kWarps);
     cudaError_t e;
     if (a.dk == a.dv) {                                  // q, k, v: grid.z = 0, 1, 2
-        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 3), 0, s);
+        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 3), 0, run, s);
     } else {                                             // q and k, then v with its own width
-        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 2), 0, s);
+        e = launch_rows<T>(a, a.dk, dim3(bx, a.H, 2), 0, run, s);
         if (e == cudaSuccess)
-            e = launch_rows<T>(a, a.dv, dim3(bx, a.H, 1), 2, s);
+            e = launch_rows<T>(a, a.dv, dim3(bx, a.H, 1), 2, run, s);
     }
     if (e != cudaSuccess) return e;
     const int64_t rows = a.total_tokens * a.H;
