@@ -665,7 +665,7 @@ def run_ours(args):
     ranks.close()
 
 
-PROFILE_CASES = ("prefill", "decode_chunk_T16", "decode_chunk_T4", "split_T32768")
+PROFILE_CASES = ("prefill", "decode_chunk_T16", "decode_chunk_T4", "split_T32768", "frontend")
 
 
 def run_profile_case(name):
@@ -695,6 +695,13 @@ def run_profile_case(name):
         ws = torch.empty(kda.kda_prefill_split_workspace_size(tl, 1, H), dtype=torch.uint8, device=dev)
         call = lambda: kda.kda_prefill_split(w.q, w.k, w.v, w.log_alpha, w.beta, None, cu, out=out,
                                              final_state=fin, workspace=ws)
+    elif name == "frontend":
+        lx = workloads.make_layer_inputs(B * T, H, D, D, W=4, dtype=torch.bfloat16, seed=11, num_seqs=B, device=dev)
+        w = workloads.prefill_bf16(device=dev)
+        fe_out = tuple(torch.empty_like(t) for t in (w.q, w.k, w.v, w.log_alpha, w.beta))
+        del w
+        call = lambda: kda.kda_frontend(lx.q_raw, lx.k_raw, lx.v_raw, lx.a_raw, lx.b_raw, lx.conv_q, lx.conv_k,
+                                        lx.conv_v, num_seqs=B, out=fe_out)
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(3):
