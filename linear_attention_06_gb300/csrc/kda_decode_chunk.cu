@@ -394,7 +394,9 @@ __device__ __forceinline__ void solve_delta(const Smem<NT>& sm, float (&rt)[NT][
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int p = 0; p < 2; ++p) a[nt][p] = *reinterpret_cast<const float4*>(&sm.am[8 * nt + 2 * qi + p][s4]);
+            for (int p = 0; p < 2; ++p)
+                if (nt >= s4 / 8)                    // earlier token blocks take no update from here
+                    a[nt][p] = *reinterpret_cast<const float4*>(&sm.am[8 * nt + 2 * qi + p][s4]);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int s = s4 + u, ns = s >> 3, ps = s & 1, qs = (s & 7) >> 1;
@@ -408,6 +410,7 @@ __device__ __forceinline__ void solve_delta(const Smem<NT>& sm, float (&rt)[NT][
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
+                    if (nt < ns) continue;               // tokens of block nt < ns all precede token s
                     const float4 av = a[nt][p];
                     const float ats = u == 0 ? av.x : u == 1 ? av.y : u == 2 ? av.z : av.w;
                     rt[nt][p] = fmaf(-ats, D0, rt[nt][p]);
