@@ -4,7 +4,7 @@
 // "Scale: Total vs Active Parameters and Serving Economics", Visual 1: the KDA
 // output passes a norm and is multiplied by the sigmoid gate).
 //
-// Prefill applies it with this row kernel, in place on `out`, after the
+// Prefill applies it with these row kernels, in place on `out`, after the
 // recurrence: one read of o and of the gate and one write, memory-bound.  (The
 // decode step applies it inside its own output store.)  Done inside the
 // tensor-core prefill's output stores instead, the gate loads, the cross-warp
@@ -103,6 +103,60 @@ __global__ void __launch_bounds__(kWarps * 32) gated_norm_kernel(T* __restrict__
     }
 }
 
+// bf16 rows of 128 channels: a row over half a warp (8 channels a lane, 16-byte accesses),
+// kHalfRows rows a half warp with all their loads issued first.
+constexpr int kHalfRows = 4;
+__global__ void __launch_bounds__(kWarps * 32) gated_norm_bf16_128(__nv_bfloat16* __restrict__ out,
+                                                                   const __nv_bfloat16* __restrict__ gate,
+                                                                   const float* __restrict__ w, float eps,
+                                                                   int64_t rows, unsigned int* status) {
+    (void)status;
+    constexpr int DV = 128;
+    const int lane = threadIdx.x & 31, half = lane >> 4, hl = lane & 15;
+    const unsigned mask = 0xffffu << (16 * half);
+    const int64_t row0 = (((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 2 + half) * kHalfRows;
+    const int c0 = hl * 8;
+    float wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wv[i] = w[c0 + i];
+    uint4 xu[kHalfRows], gu[kHalfRows];
+#pragma unroll
+    for (int r = 0; r < kHalfRows; ++r) {
+        xu[r] = gu[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (row0 + r < rows && KDA_INDEX_OK((row0 + r) * DV + c0 + 7, rows * DV, status)) {
+            xu[r] = *reinterpret_cast<const uint4*>(out + (row0 + r) * DV + c0);
+            gu[r] = *reinterpret_cast<const uint4*>(gate + (row0 + r) * DV + c0);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kHalfRows; ++r) {
+        if (row0 + r >= rows) break;
+        const uint32_t xw[4] = {xu[r].x, xu[r].y, xu[r].z, xu[r].w}, gw[4] = {gu[r].x, gu[r].y, gu[r].z, gu[r].w};
+        float x[8], g[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(xw[i] << 16); x[2 * i + 1] = __uint_as_float(xw[i] & 0xffff0000u);
+            g[2 * i] = __uint_as_float(gw[i] << 16); g[2 * i + 1] = __uint_as_float(gw[i] & 0xffff0000u);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(mask, ss, o);
+        const float rr = rsqrtf(ss * (1.f / DV) + eps);
+        uint32_t yw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float y0 = x[2 * i] * rr * wv[2 * i] * __fdividef(1.f, 1.f + __expf(-g[2 * i]));
+            const float y1 = x[2 * i + 1] * rr * wv[2 * i + 1] * __fdividef(1.f, 1.f + __expf(-g[2 * i + 1]));
+            __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
+            yw[i] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        if (KDA_INDEX_OK((row0 + r) * DV + c0 + 7, rows * DV, status))
+            *reinterpret_cast<uint4*>(out + (row0 + r) * DV + c0) = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float eps, int64_t rows, int dv,
@@ -112,8 +166,12 @@ cudaError_t launch_gated_norm(void* out, const void* gate, const float* w, float
     if (dt == DType::BF16) {
         auto* o = static_cast<__nv_bfloat16*>(out);
         auto* g = static_cast<const __nv_bfloat16*>(gate);
-        if (dv == 128) gated_norm_kernel<__nv_bfloat16, 4><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
-        else gated_norm_kernel<__nv_bfloat16, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
+        if (dv == 128) {
+            const unsigned b16 = (unsigned)((rows + kWarps * 2 * kHalfRows - 1) / (kWarps * 2 * kHalfRows));
+            gated_norm_bf16_128<<<b16, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
+        } else {
+            gated_norm_kernel<__nv_bfloat16, 2><<<blocks, kWarps * 32, 0, s>>>(o, g, w, eps, rows, status);
+        }
     } else {
         auto* o = static_cast<float*>(out);
         auto* g = static_cast<const float*>(gate);
