@@ -607,7 +607,7 @@ def run_ours(args):
                               "value": world * B * T / layer["t_pg"], "unit": UNIT,
                               "achieved_gbs": gbytes / layer["t_pg"] / 1e9,
                               "frac": gbytes / layer["t_pg"] / 1e9 / hbm,
-                              "algorithmic_bytes_per_launch": gbytes, "kernels": ["chunk_tc_kernel", "gated_norm_kernel"]},
+                              "algorithmic_bytes_per_launch": gbytes, "kernels": ["chunk_tc_kernel", "gated_norm_bf16_128"]},
             "decode_gated": {"workload": f"kda_decode_N{DEC_N}_H{H}_d{D}_gated",
                              "us_per_step": layer["t_dg"] * 1e6, "achieved_gbs": dgbytes / layer["t_dg"] / 1e9,
                              "frac": dgbytes / layer["t_dg"] / 1e9 / hbm,
