@@ -665,7 +665,7 @@ def run_ours(args):
     ranks.close()
 
 
-PROFILE_CASES = ("prefill", "decode_chunk_T16", "decode_chunk_T4", "split_T32768", "frontend")
+PROFILE_CASES = ("prefill", "decode_chunk_T16", "decode_chunk_T4", "split_T32768", "frontend", "prefill_gated")
 
 
 def run_profile_case(name):
@@ -702,6 +702,13 @@ def run_profile_case(name):
         del w
         call = lambda: kda.kda_frontend(lx.q_raw, lx.k_raw, lx.v_raw, lx.a_raw, lx.b_raw, lx.conv_q, lx.conv_k,
                                         lx.conv_v, num_seqs=B, out=fe_out)
+    elif name == "prefill_gated":
+        w = workloads.prefill_bf16(device=dev)
+        lx = workloads.make_layer_inputs(B * T, H, D, D, W=4, dtype=torch.bfloat16, seed=11, num_seqs=B, device=dev)
+        out, fin = torch.empty_like(w.v), torch.empty((B, H, D, D), dtype=torch.float32, device=dev)
+        cu = w.cu_seqlens.to(dev)
+        call = lambda: kda.kda_prefill_gated(w.q, w.k, w.v, w.log_alpha, w.beta, lx.g_raw, lx.norm_weight,
+                                             cu_seqlens=cu, out=out, final_state=fin)
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(3):
