@@ -16,7 +16,8 @@
 // same block one after another with the state held in registers, so a short
 // multi-token step costs the same state traffic as a single token; the T tokens'
 // vectors are staged in shared memory up front, so the token loop waits on no
-// global load.
+// global load.  Instances: one token (compile-time trip count), two tokens, and up to
+// kMaxDecodeTokens (bf16 steps of 3..16 tokens at d = 128 take the chunk form instead).
 //
 // Layout of the work: one block of 256 threads per (sequence, head).  A row of
 // S (dv fp32) is covered by dv/4 threads with 16-byte loads, so each warp
@@ -222,7 +223,8 @@ cudaError_t launch_dims_t(const DecodeArgs& a, cudaStream_t st) {
 template <int DK, int DV>
 cudaError_t launch_dims(const DecodeArgs& a, cudaStream_t st) {
     if (a.tokens_per_seq < 1 || a.tokens_per_seq > kMaxDecodeTokens) return cudaErrorInvalidValue;
-    return a.tokens_per_seq == 1 ? launch_dims_t<DK, DV, 1>(a, st) : launch_dims_t<DK, DV, kMaxDecodeTokens>(a, st);
+    if (a.tokens_per_seq == 1) return launch_dims_t<DK, DV, 1>(a, st);
+    return a.tokens_per_seq == 2 ? launch_dims_t<DK, DV, 2>(a, st) : launch_dims_t<DK, DV, kMaxDecodeTokens>(a, st);
 }
 
 }  // namespace

@@ -1,5 +1,6 @@
-// kda_decode_chunk.cu -- a decode step of 2..16 tokens per sequence at dk = dv = 128, the
-// step's tokens taken as one short chunk.
+// kda_decode_chunk.cu -- a decode step of 3..16 tokens per sequence at dk = dv = 128, the
+// step's tokens taken as one short chunk (steps of one or two tokens run faster through the
+// token loop of kda_decode.cu: 199 us against 234 us at two tokens, 256 x 32 heads).
 //
 // The math (one head; tokens t = 0..T-1 of the step, S0 the state entering it, a_t = log
 // alpha_t, g_t = sum_{s<=t} a_s, G = g_{T-1}) is the exact rewrite of the token recurrence of
@@ -50,7 +51,7 @@
 // and gives the same bits as T one-token steps.
 //
 // Blocks are persistent, two per SM (59,008 bytes of shared memory a block for 9..16 tokens,
-// 35,968 for 2..8, and at most 128 registers a thread), and walk the (sequence, head) pairs
+// 35,968 for 3..8, and at most 128 registers a thread), and walk the (sequence, head) pairs
 // with a stride of the grid size; each prefetches the state and token rows of its next pair
 // into L2 when it starts a pair, so that their DRAM reads overlap its arithmetic.
 #include <atomic>
@@ -552,7 +553,7 @@ Params<Tin> params(const DecodeArgs& a) {
 }  // namespace
 
 bool decode_chunk_supported(const DecodeArgs& a) {
-    return a.dtype == DType::BF16 && a.dk == kD && a.dv == kD && a.tokens_per_seq >= 2 && a.tokens_per_seq <= kTok;
+    return a.dtype == DType::BF16 && a.dk == kD && a.dv == kD && a.tokens_per_seq >= 3 && a.tokens_per_seq <= kTok;
 }
 
 cudaError_t launch_decode_chunk(const DecodeArgs& a, cudaStream_t st) {

@@ -107,7 +107,7 @@ cudaError_t launch_split_prefill(const PrefillArgs& a, void* workspace, cudaStre
 unsigned int* device_status_word();
 // One decode step of T tokens per sequence (state in place).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-// Decode steps of 2..16 tokens per sequence at dk = dv = 128, the tokens taken as one chunk
+// Decode steps of 3..16 tokens per sequence at dk = dv = 128, the tokens taken as one chunk
 // (kda_decode_chunk.cu); launch_decode sends those shapes there.
 bool decode_chunk_supported(const DecodeArgs& a);
 cudaError_t launch_decode_chunk(const DecodeArgs& a, cudaStream_t s);

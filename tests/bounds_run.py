@@ -91,8 +91,8 @@ def main() -> int:
                      cu_seqlens=cu)
     check("front end dk=64 dv=128")
 
-    # decode: one, five and sixteen tokens per sequence, plain and gated, every head size
-    for T in (1, 5, 16):
+    # decode: one, two, five and sixteen tokens per sequence, plain and gated, every head size
+    for T in (1, 2, 5, 16):
         for dk, dv in ((128, 128), (64, 128), (128, 64), (64, 64)):
             n = 9
             c = [T * i for i in range(n + 1)]
