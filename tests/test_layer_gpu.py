@@ -148,7 +148,7 @@ def test_prefill_gated_full_size_sampled_heads():
     assert torch.equal(fin, plain_fin)
 
 
-@pytest.mark.parametrize("T", [1, 5, 16])
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
 def test_decode_gated(T):
     from oracle import kda_oracle
     n = 6

@@ -306,6 +306,27 @@ def test_decode_multi_token_agrees_with_repeated_single_steps(dtype):
         assert torch.equal(out_multi, outs) and torch.equal(S_multi, S_step)
 
 
+def test_decode_two_tokens_equals_two_single_steps_bitwise():
+    # a two-token step runs the one-token kernel's loop twice on the state in registers (the
+    # chunk form starts at three tokens): the same arithmetic in the same order as two calls
+    # of the one-token step, so out and the state are equal bit for bit
+    n, T, H = 16, 2, 4
+    cu = [T * i for i in range(n + 1)]
+    w = workloads.make_inputs(n * T, H, 128, 128, dtype=torch.bfloat16, seed=41, cu_seqlens=cu,
+                              state_std=0.05).to(DEV)
+    S_two = w.initial_state.clone()
+    out_two = kda.kda_decode_step(w.q, w.k, w.v, w.log_alpha, w.beta, S_two)
+    S_one = w.initial_state.clone()
+    rows = torch.arange(n, device=DEV) * T
+    outs = torch.empty_like(out_two)
+    for t in range(T):
+        r = rows + t
+        outs[r] = kda.kda_decode_step(w.q[r].contiguous(), w.k[r].contiguous(), w.v[r].contiguous(),
+                                      w.log_alpha[r].contiguous(), w.beta[r].contiguous(), S_one)
+    torch.cuda.synchronize()
+    assert torch.equal(out_two, outs) and torch.equal(S_two, S_one)
+
+
 @pytest.mark.parametrize("T", [4, 16])
 def test_decode_multi_token_full_size_sampled_sequences(T):
     # the bench's multi-token step (256 sequences x 32 heads, one launch of the chunk form on
