@@ -27,6 +27,11 @@
 // runs it token by token from the inputs themselves.  Records of sequence n start at
 // slot floor(bos_n / 64) + n, so a head needs ceil(T / 64) + N slots whatever the
 // lengths (kda_prefill_split_workspace_size).
+//
+// The chain kernel holds two record slots and loads each record in two parts: part A (Kb,
+// -W'^T, e^G, U^T) is read up to the state update, part B (Qhat, P) by the output products,
+// so part A of chunk n + 2 is loaded as soon as chunk n's state update has landed instead of
+// after its output products (4.43 against 4.58 ms for one 131,072-token sequence).
 #include <atomic>
 #include <mutex>
 
@@ -41,8 +46,10 @@ constexpr int kRecUnits = 12;
 constexpr uint32_t kRecBytes = kRecUnits * kUnit;           // 98304
 constexpr int kUQh = 0, kUKb = 2, kUWt = 4, kUP = 6, kUSmall = 7, kUU = 8;
 constexpr uint32_t kGamBytes = D * 4;
-// one record's bytes moved by the chain kernel's loads: 7 bf16 units, e^G and U^T
-constexpr uint32_t kRecLoadBytes = 7 * kUnit + kGamBytes + 4 * kUnit;
+// one record's bytes moved by the chain kernel's loads, in two parts: A (Kb, -W'^T, e^G, U^T) is
+// read up to the state update, B (Qhat, P) by the output products
+constexpr uint32_t kRecLoadBytesA = 4 * kUnit + kGamBytes + 4 * kUnit;
+constexpr uint32_t kRecLoadBytesB = 3 * kUnit;
 constexpr uint32_t kRawLoadBytes = kQKBytes + kVBytes + kABytes;   // q, k, v, log_alpha tiles
 
 struct RecMaps {
@@ -516,8 +523,10 @@ __device__ __forceinline__ uint32_t tm_sbf(int d) { return 128u + 64u * d; }
 __device__ __forceinline__ uint32_t tm_dbf(int d) { return 384u + 32u * d; }
 
 struct ChainSmall {
-    uint64_t rec_full[2];      // producer -> all: the slot's record (or raw tiles) landed
-    uint64_t rec_free[2];      // slot s read by its last reader
+    uint64_t rec_full[2];      // producer -> all: the slot's part A (or raw tiles) landed
+    uint64_t rec_free[2];      // part A read by its last reader (the state update)
+    uint64_t rec_full_b[2];    // producer -> issuer: part B landed (a plain arrival for raw tiles)
+    uint64_t rec_free_b[2];    // part B read by its last reader (the output products)
     uint64_t decayed;          // group B -> issuer: Ss and its bf16 copy in TMEM
     uint64_t packed;           // group B -> issuer: Delta packed
     uint64_t mma1, mma2;       // issuer -> group B: Delta product; state update
@@ -526,7 +535,8 @@ struct ChainSmall {
     uint64_t drain;
     uint32_t tmem_base;
     int mode[2];
-    int issued[2];             // loads the producer issued into each slot
+    int issued[2];             // loads the producer issued into each slot (part A / raw tiles)
+    int issued_b[2];           // phases of rec_full_b the producer started
     alignas(16) __nv_bfloat16 beta[2][C];  // token-by-token chunks only
 };
 static_assert(sizeof(ChainSmall) <= 2048, "small area");
@@ -694,6 +704,7 @@ __device__ __noinline__ bool run_chain_b(const ChainCtx& x_in, const __nv_bfloat
             if (t == 0 && lower) {
                 mbar_arrive(&sw.o_ready[d]);
                 mbar_arrive(&sw.rec_free[s]);
+                mbar_arrive(&sw.rec_free_b[s]);
             }
             continue;
         }
@@ -740,9 +751,11 @@ __device__ __noinline__ bool run_chain_issuer(const ChainCtx& x_in) {
         tc_fence_after();
         mma_state_rec(x.tb, tm_dbf(d), slot + kUKb * kUnit);
         mma_commit(&sw.mma2);                            // the state chain goes on from here
+        mma_commit(&sw.rec_free[s]);                     // part A: Delta, the pack and the update read it
+        if (!(ok = mbar_wait_bounded(&sw.rec_full_b[s], ph, kWaitLimitNs))) break;
         mma_out_rec(x.tb, tm_d(d), tm_sbf(d), tm_dbf(d), slot + kUQh * kUnit, slot + kUP * kUnit);
         mma_commit(&sw.o_ready[d]);
-        mma_commit(&sw.rec_free[s]);
+        mma_commit(&sw.rec_free_b[s]);
         m_ph ^= 1u;
     }
     if (issued) {
@@ -800,22 +813,35 @@ __device__ __noinline__ void run_chain_producer(const ChainCtx& x_in, const Maps
         mode_next = mode_next2;
         mode_next2 = mode_of(n + 2);
         prefetch(n + 4);
-        if (n >= 2 && !mbar_wait_bounded(&sw.rec_free[s], ((n - 2) >> 1) & 1, kWaitLimitNs)) return;
+        const uint32_t fph = ((n - 2) >> 1) & 1;
+        if (n >= 2 && !mbar_wait_bounded(&sw.rec_free[s], fph, kWaitLimitNs)) return;   // part A free
         const int rec = x.rec_base + n;
         sw.mode[s] = mode;
         uint8_t* slot = x.sm + kSlot0 + s * kRecBytes;
         uint64_t* bar = &sw.rec_full[s];
-        ++sw.issued[s];
         if (mode == 0) {
-            mbar_arrive_expect_tx(bar, kRecLoadBytes);
+            ++sw.issued[s];
+            mbar_arrive_expect_tx(bar, kRecLoadBytesA);
             const int u0 = rec * kRecUnits;
 #pragma unroll 1
-            for (int u = 0; u < 7; ++u) tma_load_3d(slot + u * kUnit, &rm.t16, 0, 0, u0 + u, bar);
+            for (int u = kUKb; u < kUP; ++u) tma_load_3d(slot + u * kUnit, &rm.t16, 0, 0, u0 + u, bar);
             bulk_load_1d(slot + kUSmall * kUnit, ws.recs + (size_t)rec * kRecBytes + kUSmall * kUnit, kGamBytes,
                          bar);
             tma_load_3d(slot + kUU * kUnit, &rm.t32, 0, 0, rec * (kRecUnits / 2) + kUU / 2, bar);
             tma_load_3d(slot + kUU * kUnit + 16384, &rm.t32, 0, 0, rec * (kRecUnits / 2) + kUU / 2 + 1, bar);
+            // part B once the output products of chunk n-2 have read the slot's Qhat and P
+            if (n >= 2 && !mbar_wait_bounded(&sw.rec_free_b[s], fph, kWaitLimitNs)) return;
+            uint64_t* bb = &sw.rec_full_b[s];
+            ++sw.issued_b[s];
+            mbar_arrive_expect_tx(bb, kRecLoadBytesB);
+            tma_load_3d(slot + kUQh * kUnit, &rm.t16, 0, 0, u0 + kUQh, bb);
+            tma_load_3d(slot + (kUQh + 1) * kUnit, &rm.t16, 0, 0, u0 + kUQh + 1, bb);
+            tma_load_3d(slot + kUP * kUnit, &rm.t16, 0, 0, u0 + kUP, bb);
         } else {
+            // the raw tiles cover the whole slot: part B must be free too; rec_full_b takes a plain
+            // arrival (its previous phase, a load or an arrival, completed before that release)
+            if (n >= 2 && !mbar_wait_bounded(&sw.rec_free_b[s], fph, kWaitLimitNs)) return;
+            ++sw.issued[s];
             const int tc = (int)(x.bos + (int64_t)n * C);
             mbar_arrive_expect_tx(bar, kRawLoadBytes);
             tma_load_3d(slot + 0, &maps.k, 0, x.h, tc, bar);
@@ -825,6 +851,8 @@ __device__ __noinline__ void run_chain_producer(const ChainCtx& x_in, const Maps
             tma_load_3d(slot + kQKBytes, &maps.v, 0, x.h, tc, bar);
             tma_load_3d(slot + kQKBytes + 8192, &maps.v, 64, x.h, tc, bar);
             tma_load_3d(slot + 2 * kQKBytes, &maps.a, 0, x.h, tc, bar);
+            ++sw.issued_b[s];
+            mbar_arrive(&sw.rec_full_b[s]);
         }
     }
 }
@@ -862,6 +890,9 @@ chunk_chain_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Re
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sw->rec_full[s], 1);
             mbar_init(&sw->rec_free[s], 1);
+            mbar_init(&sw->rec_full_b[s], 1);
+            mbar_init(&sw->rec_free_b[s], 1);
+            sw->issued_b[s] = 0;
             mbar_init(&sw->o_ready[s], 1);
             mbar_init(&sw->d_free[s], 4);
             sw->issued[s] = 0;
@@ -898,6 +929,9 @@ chunk_chain_kernel(const __grid_constant__ Maps maps, const __grid_constant__ Re
     if (tid == 0) {   // every load the producer issued lands before the block exits (bounded)
         for (int s = 0; s < 2; ++s)
             if (sw->issued[s] > 0) mbar_wait_bounded(&sw->rec_full[s], (uint32_t)((sw->issued[s] - 1) & 1), kWaitLimitNs);
+        for (int s = 0; s < 2; ++s)
+            if (sw->issued_b[s] > 0)
+                mbar_wait_bounded(&sw->rec_full_b[s], (uint32_t)((sw->issued_b[s] - 1) & 1), kWaitLimitNs);
     }
     __syncthreads();
     if ((tid >> 5) == 0) tmem_dealloc(x.tb, kTmCols);
