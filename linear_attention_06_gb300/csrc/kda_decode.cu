@@ -67,10 +67,12 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     // Issue the whole state read first so it overlaps the small loads.
     (void)status;                          // read by the index checks of bounds-checked builds
     const int64_t n_state4 = (int64_t)gridDim.x * DK * DV / 4;   // float4s of S over all pairs
+    (void)n_state4;
     float4 s[RPT];
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
         const int64_t i4 = (int64_t)p * DK * DV / 4 + (int64_t)(g * RPT + m) * LANES + c4;
+        (void)i4;
         s[m] = KDA_INDEX_OK(i4, n_state4, status) ? __ldcs(Sp + (size_t)(g * RPT + m) * LANES + c4)
                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -93,6 +95,7 @@ decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* _
     if (MAXT == 1) T = 1;                   // a compile-time trip count for the single-token step
     const size_t row0 = n * (size_t)T * H + h;         // row of token 0; token t is row0 + t * H
     const int64_t n_rows = (int64_t)gridDim.x * T;     // rows of q, k, v, out: num_seqs x T x H
+    (void)n_rows;
     for (int i = threadIdx.x; i < T * DK; i += kThreads) {
         const int tok = i / DK, c = i % DK;
         const size_t e = (row0 + (size_t)tok * H) * DK + c;

@@ -23,20 +23,6 @@ constexpr int kWarps = 8;
 constexpr int kRows = 2;       // rows per warp, loads of both issued first
 
 template <typename T, int CPL> struct Vec;
-template <> struct Vec<__nv_bfloat16, 4> {
-    static __device__ __forceinline__ void ld(const __nv_bfloat16* p, float (&x)[4]) {
-        const uint2 u = *reinterpret_cast<const uint2*>(p);
-        x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
-        x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16* p, const float (&x)[4]) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]), hi = __floats2bfloat162_rn(x[2], x[3]);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&lo);
-        u.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p) = u;
-    }
-};
 template <> struct Vec<__nv_bfloat16, 2> {
     static __device__ __forceinline__ void ld(const __nv_bfloat16* p, float (&x)[2]) {
         const uint32_t u = *reinterpret_cast<const uint32_t*>(p);

@@ -71,6 +71,7 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
     float s[DK];
     const size_t sbase = ((size_t)n * H + h) * DK * dv + j;
     const int64_t n_state = (int64_t)num_seqs * H * DK * dv, n_k = T * H * DK, n_v = T * H * dv;
+    (void)n_state; (void)n_k; (void)n_v;                 // read by the index checks of bounds-checked builds
 #pragma unroll
     for (int i = 0; i < DK; ++i)
         s[i] = (h0 && KDA_INDEX_OK(sbase + (size_t)i * dv, n_state, status)) ? h0[sbase + (size_t)i * dv] : 0.f;
@@ -154,6 +155,7 @@ recurrent_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                 if (ck_next == done && (done % 64 == 0 || t + 1 == eos)) {
                     const size_t cb = ((size_t)ck * H + h) * DK * dv + j;
                     const int64_t n_ck = (int64_t)ck_cu[num_seqs] * H * DK * dv;
+                    (void)n_ck;
 #pragma unroll
                     for (int i = 0; i < DK; ++i)
                         if (KDA_INDEX_OK(cb + (size_t)i * dv, n_ck, status)) ck_states[cb + (size_t)i * dv] = s[i];
